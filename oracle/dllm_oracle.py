@@ -1,0 +1,305 @@
+"""Plain float64 definitions of every output of the partial denoising step.
+
+TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
+and the CPU-baseline leg of ``bench.py``; never by the product path.
+
+Inputs are numpy arrays already decoded to float64 (decoding a bfloat16 or
+float32 value to float64 is exact).  Nothing here is blocked, fused or
+reordered: each function evaluates the definition it cites, with numpy's
+matmul / sum / exp / argmax as the only library steps.
+
+Pages cited (title, then section):
+
+* DyLLM -- "DyLLM: Efficient Diffusion LLM Inference via Saliency-based Token
+  Selection and Partial Attention" (gist.science/nl/paper/2603.08026).
+* SlowFast -- "Accelerating Diffusion Large Language Models with SlowFast
+  Sampling: The Three Golden Principles" (gist.science/it/paper/2506.10848).
+* Attn-Sampler -- "Attention-Based Sampler for Diffusion Language Models"
+  (gist.science/nl/paper/2604.08564).
+* SureLock -- "Stopping Computation for Converged Tokens in Masked
+  Diffusion-LM Decoding" (gist.science/de/paper/2602.06412).
+* LSP -- "Beyond Scattered Acceptance: Fast and Coherent Inference for DLMs via
+  Longest Stable Prefixes" (gist.science/nl/paper/2603.05454).
+
+Readings taken where the pages are silent (each is pinned or listed as
+unpinned in the tests): salient iff cos < tau, so cos == tau is stable and a
+NaN cosine is salient; two zero vectors have cosine 1, one zero vector gives 0;
+compaction keeps ascending positions and pads with -1; confidence is the
+maximum of a temperature-1 softmax; argmax ties go to the lowest vocabulary
+index and then the margin is 0; attention is unmasked (bidirectional) with
+scale 1/sqrt(d); column sums add the row-normalised probabilities of the
+active query rows only; a prefix position is stable iff score >= tau, NaN is
+unstable.
+"""
+from __future__ import annotations
+
+import math
+from typing import Optional
+
+import numpy as np
+
+__all__ = [
+    "saliency_cos",
+    "salient_flags",
+    "compact",
+    "saliency_select",
+    "confidence",
+    "kv_scatter",
+    "partial_attention",
+    "stable_prefix",
+    "step",
+]
+
+
+def _f64(x) -> np.ndarray:
+    return np.asarray(x, dtype=np.float64)
+
+
+# --------------------------------------------------------------------------
+# Saliency: temporal cosine similarity, threshold, ordered compaction
+# --------------------------------------------------------------------------
+
+def saliency_cos(cur, prev) -> np.ndarray:
+    """Temporal cosine similarity of each position's current and cached vector.
+
+    DyLLM, technical summary, Methodology 1 (layer-adaptive saliency
+    selection), "Meting": s_{t,l} is the cosine similarity, per token and per
+    layer, of the vector at step t and the cached one from step t-1.
+
+    ``cur``/``prev``: [..., D].  Returns cos [...] in float64.  Both vectors
+    zero -> 1 (identical); exactly one zero -> 0.
+    """
+    cur = _f64(cur)
+    prev = _f64(prev)
+    dot = np.sum(cur * prev, axis=-1)
+    n_cur = np.sqrt(np.sum(cur * cur, axis=-1))
+    n_prev = np.sqrt(np.sum(prev * prev, axis=-1))
+    out = np.empty(dot.shape, dtype=np.float64)
+    both_zero = (n_cur == 0.0) & (n_prev == 0.0)
+    one_zero = (n_cur == 0.0) != (n_prev == 0.0)
+    regular = ~(both_zero | one_zero)
+    out[regular] = dot[regular] / (n_cur[regular] * n_prev[regular])
+    out[both_zero] = 1.0
+    out[one_zero] = 0.0
+    return out
+
+
+def salient_flags(cos, tau: float, locked=None) -> np.ndarray:
+    """Active = salient and not locked.
+
+    DyLLM, technical summary, Methodology 1, "Selectie": a cosine close to 1 is
+    stable, a low cosine is salient and is recomputed (tau = 0.99 in the
+    results).  SureLock, technical summary section 2 ("Berechnungsoptimierung"):
+    locked positions skip their own recompute.
+
+    The comparison is taken in float32, the precision the kernel stores its
+    cosine in: salient iff float32(cos) < float32(tau), NaN salient.
+    """
+    c32 = np.asarray(cos).astype(np.float32)
+    t32 = np.float32(tau)
+    active = ~(c32 >= t32)
+    if locked is not None:
+        active &= ~np.asarray(locked).astype(bool)
+    return active
+
+
+def compact(flags, idx_base: int = 0):
+    """Ordered stream compaction of the active flags of each batch row.
+
+    DyLLM, technical summary, Methodology 1, "Optimalisatie": only the salient
+    rows are recomputed, the rest reuse the cache -- so the recompute needs the
+    list of salient positions.  Returns idx [B, Lw] int32 (ascending positions
+    + ``idx_base``, padded with -1) and count [B] int32.
+    """
+    flags = np.asarray(flags, dtype=bool)
+    B, Lw = flags.shape
+    idx = np.full((B, Lw), -1, dtype=np.int32)
+    count = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        pos = np.flatnonzero(flags[b])
+        idx[b, : len(pos)] = pos + idx_base
+        count[b] = len(pos)
+    return idx, count
+
+
+def saliency_select(cur, prev, tau: float, locked=None, idx_base: int = 0):
+    """Cosine, threshold and compaction over a [B, Lw, D] window.
+
+    DyLLM, technical summary, Methodology 1 (measurement, selection) and 3
+    (adaptive input: the window is the response rows on most steps and the
+    whole sequence every few steps).  Returns (cos [B, Lw] float64,
+    idx [B, Lw] int32, count [B] int32).
+    """
+    cos = saliency_cos(cur, prev)
+    idx, count = compact(salient_flags(cos, tau, locked), idx_base)
+    return cos, idx, count
+
+
+# --------------------------------------------------------------------------
+# Confidence, argmax and logit margin over the vocabulary
+# --------------------------------------------------------------------------
+
+def confidence(logits, count=None, row_idx=None):
+    """Max softmax probability, argmax and top-1 minus top-2 logit per row.
+
+    SlowFast, section 2 (certainty principle; fast phase unmasks tokens whose
+    confidence exceeds a high threshold); SureLock, technical summary section 2,
+    locking criterion 2 (uncertainty 1 - max_v p(v)); LSP, technical summary
+    section 2, step 1 (logit margin = highest minus second-highest logit).
+
+    ``logits``: [B, R, V].  Row r of batch b reads ``logits[b, row_idx[b, r]]``
+    when ``row_idx`` ([B, R_max]) is given, else ``logits[b, r]``; rows
+    r >= count[b] are skipped (NaN / -1).  Returns conf, argmax, margin, each
+    [B, R_max].
+    """
+    z_all = _f64(logits)
+    B, R, V = z_all.shape
+    R_max = R if row_idx is None else np.asarray(row_idx).shape[1]
+    if count is None:
+        count = np.full(B, R_max, dtype=np.int64)
+    conf = np.full((B, R_max), np.nan)
+    amax = np.full((B, R_max), -1, dtype=np.int32)
+    margin = np.full((B, R_max), np.nan)
+    for b in range(B):
+        for r in range(int(count[b])):
+            row = r if row_idx is None else int(row_idx[b][r])
+            z = z_all[b, row]
+            j = int(np.argmax(z))  # first occurrence: lowest index on ties
+            m = z[j]
+            conf[b, r] = 1.0 / np.sum(np.exp(z - m))
+            amax[b, r] = j
+            rest = np.concatenate([z[:j], z[j + 1:]])
+            margin[b, r] = m - np.max(rest)
+    return conf, amax, margin
+
+
+# --------------------------------------------------------------------------
+# KV cache update
+# --------------------------------------------------------------------------
+
+def kv_scatter(k_cache, v_cache, k_new, v_new, idx, count):
+    """Write the fresh K/V rows of the active positions into the full cache.
+
+    SureLock, technical summary section 2: K/V of locked positions are cached
+    and other tokens keep attending to them; only active rows get new K/V.
+    LSP, technical summary section 2 ("KV Cache"): contiguous appends.
+
+    Caches [B, L, H, d]; new rows [B, M_max, H, d]; row i < count[b] goes to
+    position idx[b, i].  Returns updated copies (inputs are left alone).
+    """
+    kc = np.array(k_cache, copy=True)
+    vc = np.array(v_cache, copy=True)
+    for b in range(kc.shape[0]):
+        for i in range(int(count[b])):
+            p = int(idx[b][i])
+            kc[b, p] = k_new[b, i]
+            vc[b, p] = v_new[b, i]
+    return kc, vc
+
+
+# --------------------------------------------------------------------------
+# Partial attention and attention column sums
+# --------------------------------------------------------------------------
+
+def partial_attention(q, k_cache, v_cache, count, scale: Optional[float] = None):
+    """Exact softmax attention of the active query rows over every cached key.
+
+    DyLLM, technical summary, Methodology 2 (salient path: the score rows of
+    salient queries are recomputed in full); SureLock, technical summary
+    section 2 (active tokens attend to all positions through the cached K/V;
+    cost O(M N d)); Attn-Sampler, technical summary, Methodology 2 (column sums
+    of the attention matrix).
+
+    q [B, M_max, H, d] (rows i < count[b] are the active queries), caches
+    [B, L, H, d].  Per (b, h): S = scale * Q K^T (no mask: the models are
+    bidirectional), P = row softmax of S, O = P V, lse = log sum_j exp S,
+    colsum[j] = sum over active rows of P[:, j].  Returns o [B, M_max, H, d]
+    (NaN on inactive rows), lse [B, H, M_max] (NaN on inactive rows),
+    colsum [B, H, L].
+    """
+    q = _f64(q)
+    k = _f64(k_cache)
+    v = _f64(v_cache)
+    B, M_max, H, d = q.shape
+    L = k.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    o = np.full((B, M_max, H, d), np.nan)
+    lse = np.full((B, H, M_max), np.nan)
+    colsum = np.zeros((B, H, L))
+    for b in range(B):
+        n = int(count[b])
+        if n == 0:
+            continue
+        for h in range(H):
+            Q = q[b, :n, h, :]
+            K = k[b, :, h, :]
+            Vv = v[b, :, h, :]
+            S = scale * (Q @ K.T)
+            m = np.max(S, axis=1, keepdims=True)
+            E = np.exp(S - m)
+            l = np.sum(E, axis=1, keepdims=True)
+            P = E / l
+            o[b, :n, h, :] = P @ Vv
+            lse[b, h, :n] = (m + np.log(l))[:, 0]
+            colsum[b, h, :] = np.sum(P, axis=0)
+    return o, lse, colsum
+
+
+# --------------------------------------------------------------------------
+# Longest stable prefix
+# --------------------------------------------------------------------------
+
+def stable_prefix(score, start, tau: float, min_commit: bool = True):
+    """Length of the longest run of stable positions starting at ``start``.
+
+    LSP, technical summary section 2: commit the longest contiguous stable
+    block at the head of the remaining active suffix (core principle), using a
+    per-position stability score (step 1); step 4 (fallback) commits at least
+    one token when none is stable.
+
+    ``score`` [B, L]; stable iff float32(score) >= float32(tau) (NaN is not).
+    Returns len [B] int32.
+    """
+    s32 = np.asarray(score).astype(np.float32)
+    t32 = np.float32(tau)
+    B, L = s32.shape
+    out = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        st = int(start[b])
+        k = 0
+        while st + k < L and s32[b, st + k] >= t32:
+            k += 1
+        if min_commit and k == 0 and st < L:
+            k = 1
+        out[b] = k
+    return out
+
+
+# --------------------------------------------------------------------------
+# One whole partial step
+# --------------------------------------------------------------------------
+
+def step(cur, prev, k_cache, v_cache, k_new, v_new, q, logits, *, tau: float,
+         win_start: int, score, start, tau_c: float, min_commit: bool = True,
+         scale: Optional[float] = None, locked=None):
+    """One partial denoising step, composed in the order the pages give.
+
+    Select the salient rows of the window (DyLLM), write their fresh K/V into
+    the cache (SureLock), attend from them over the whole cache with column
+    sums (DyLLM, Attn-Sampler), score the window's logit rows (SlowFast,
+    SureLock, LSP) and find the committable prefix (LSP).  ``logits`` holds one
+    row per window position; their confidence replaces ``score`` there.
+    """
+    cos, idx, count = saliency_select(cur[:, win_start:], prev[:, win_start:], tau,
+                                      locked, idx_base=win_start)
+    kc, vc = kv_scatter(k_cache, v_cache, k_new, v_new, idx, count)
+    o, lse, colsum = partial_attention(q, kc, vc, count, scale)
+    conf, amax, margin = confidence(logits)
+    new_score = np.array(score, dtype=np.float64, copy=True)
+    R = conf.shape[1]
+    new_score[:, win_start:win_start + R] = conf
+    length = stable_prefix(new_score, start, tau_c, min_commit)
+    return dict(cos=cos, idx=idx, count=count, k_cache=kc, v_cache=vc, o=o,
+                lse=lse, colsum=colsum, conf=conf, argmax=amax, margin=margin,
+                score=new_score, length=length)

@@ -1,0 +1,405 @@
+"""Pins of the float64 oracle to things other than itself.
+
+Each test ties one oracle output to a closed form, a hand-derived fixture
+(``tests/golden/closed_forms.json``), a library routine evaluating the same
+mathematics by another route, brute force on tiny inputs, or an invariant that
+characterises the output uniquely.  None of them needs a GPU.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+RNG = np.random.default_rng(1234)
+
+
+# ---------------------------------------------------------------- cosine
+
+def test_cos_golden(golden):
+    for case in golden["cosine"]:
+        c = oracle.saliency_cos(np.array([case["cur"]]), np.array([case["prev"]]))[0]
+        assert abs(c - case["cos"]) < 1e-15, case
+
+
+def test_cos_identity_negation_scale():
+    x = RNG.standard_normal((5, 7, 33))
+    assert np.allclose(oracle.saliency_cos(x, x), 1.0, atol=1e-15, rtol=0)
+    assert np.allclose(oracle.saliency_cos(x, -x), -1.0, atol=1e-15, rtol=0)
+    assert np.allclose(oracle.saliency_cos(x, 3.5 * x), 1.0, atol=1e-15, rtol=0)
+    y = RNG.standard_normal((5, 7, 33))
+    assert np.allclose(oracle.saliency_cos(2.0 * x, 0.25 * y), oracle.saliency_cos(x, y), atol=1e-14)
+    # symmetric in its arguments
+    assert np.allclose(oracle.saliency_cos(x, y), oracle.saliency_cos(y, x), atol=1e-15)
+
+
+def test_cos_orthogonal():
+    x = RNG.standard_normal((64, 40))
+    y = RNG.standard_normal((64, 40))
+    y -= (np.sum(x * y, -1) / np.sum(x * x, -1))[:, None] * x  # Gram-Schmidt
+    assert np.allclose(oracle.saliency_cos(x, y), 0.0, atol=1e-13)
+
+
+def test_cos_matches_torch_library():
+    x = RNG.standard_normal((3, 50, 128))
+    y = x + 0.3 * RNG.standard_normal((3, 50, 128))
+    ref = torch.nn.functional.cosine_similarity(torch.from_numpy(x), torch.from_numpy(y), dim=-1)
+    assert np.allclose(oracle.saliency_cos(x, y), ref.numpy(), atol=1e-14, rtol=0)
+
+
+def test_cos_zero_norm_readings():
+    z = np.zeros((1, 2, 4))
+    a = np.ones((1, 2, 4))
+    assert np.all(oracle.saliency_cos(z, z) == 1.0)
+    assert np.all(oracle.saliency_cos(z, a) == 0.0)
+    assert np.all(oracle.saliency_cos(a, z) == 0.0)
+
+
+def test_cos_value_on_planted_rows():
+    # cur = prev + N(0, 0.5) gives cos -> 1/sqrt(1.25) for large D; N(0, 1e-3) gives ~1 - 5e-7.
+    g = torch.Generator().manual_seed(7)
+    prev = torch.randn((200, 4096), generator=g, dtype=torch.float64)
+    big = prev + 0.5 * torch.randn((200, 4096), generator=g, dtype=torch.float64)
+    small = prev + 1e-3 * torch.randn((200, 4096), generator=g, dtype=torch.float64)
+    assert abs(oracle.saliency_cos(big, prev).mean() - 1 / math.sqrt(1.25)) < 2e-3
+    assert abs(oracle.saliency_cos(small, prev).mean() - (1 - 5e-7)) < 1e-7
+
+
+# ---------------------------------------------------------------- flags / compaction
+
+def test_flags_threshold_edges():
+    cos = np.array([[0.5, 0.99, 0.98999, np.nan, 1.0]], dtype=np.float32)
+    f = oracle.salient_flags(cos, 0.99)
+    assert f.tolist() == [[True, False, True, True, False]]
+    assert oracle.salient_flags(cos, 2.0).all()
+    assert oracle.salient_flags(cos, -2.0).tolist() == [[False, False, False, True, False]]
+    locked = np.array([[1, 0, 0, 1, 0]], dtype=np.uint8)
+    assert oracle.salient_flags(cos, 2.0, locked).tolist() == [[False, True, True, False, True]]
+
+
+@pytest.mark.parametrize("n", [1, 2, 5, 10])
+def test_compaction_brute_force(n):
+    # The invariants below (length = popcount, strictly increasing, each entry
+    # flagged, -1 padding) characterise the ordered compaction uniquely.
+    for bits in itertools.product([False, True], repeat=n):
+        flags = np.array([bits, bits[::-1]])
+        for base in (0, 7):
+            idx, count = oracle.compact(flags, base)
+            for b in range(2):
+                c = int(count[b])
+                assert c == int(flags[b].sum())
+                sel = idx[b, :c] - base
+                assert np.all(np.diff(sel) > 0)
+                assert np.all(flags[b][sel])
+                assert np.all(idx[b, c:] == -1)
+
+
+def test_select_recovers_planted_set_tiny():
+    s = workloads.TINY_F32
+    inp = workloads.make_step(s)
+    cos, idx, count = oracle.saliency_select(inp["cur"].double().numpy(),
+                                             inp["prev"].double().numpy(), s.tau)
+    assert int(count[0]) == s.n_salient
+    assert idx[0, : count[0]].tolist() == inp["planted"][0].tolist()
+
+
+def test_select_recovers_planted_set_1k_window():
+    s = workloads.STEP_1K
+    inp = workloads.make_step(s, with_logits=False)
+    w = s.win_start
+    cos, idx, count = oracle.saliency_select(inp["cur"][:, w:].double().numpy(),
+                                             inp["prev"][:, w:].double().numpy(), s.tau,
+                                             idx_base=w)
+    assert int(count[0]) == s.n_salient
+    assert idx[0, : count[0]].tolist() == inp["planted"][0].tolist()
+    assert cos[0].min() > 0.85 and cos[0].max() <= 1.0 + 1e-12
+
+
+def test_select_with_cluster_pattern_and_locks():
+    s = workloads.TINY_F32
+    inp = workloads.make_step(s, pattern="cluster", n_salient=40)
+    cur, prev = inp["cur"].double().numpy(), inp["prev"].double().numpy()
+    planted = inp["planted"][0].tolist()
+    locked = np.zeros((1, s.L), dtype=np.uint8)
+    locked[0, planted[:5]] = 1
+    _, idx, count = oracle.saliency_select(cur, prev, s.tau, locked)
+    assert idx[0, : count[0]].tolist() == planted[5:]
+
+
+# ---------------------------------------------------------------- confidence
+
+def test_confidence_golden(golden):
+    for case in golden["confidence"]:
+        conf, am, mg = oracle.confidence(np.array([[case["logits"]]]))
+        assert abs(conf[0, 0] - case["conf"]) < 1e-15
+        assert am[0, 0] == case["argmax"]
+        assert mg[0, 0] == case["margin"]
+
+
+@pytest.mark.parametrize("V", [2, 3, 17, 1000])
+@pytest.mark.parametrize("c", [0.5, 4.0, -3.0])
+def test_confidence_one_hot_closed_form(V, c):
+    z = np.zeros((1, 1, V))
+    z[0, 0, 0] = c
+    conf, am, mg = oracle.confidence(z)
+    if c > 0:
+        assert abs(conf[0, 0] - math.exp(c) / (math.exp(c) + V - 1)) < 1e-15
+        assert am[0, 0] == 0 and abs(mg[0, 0] - c) < 1e-15
+    else:  # the maximum 0 is first reached at index 1 (index 0 holds c < 0)
+        assert am[0, 0] == 1
+        if V > 2:
+            assert mg[0, 0] == 0.0
+        assert abs(conf[0, 0] - 1.0 / (math.exp(c) + V - 1)) < 1e-15
+
+
+def test_confidence_uniform():
+    conf, am, mg = oracle.confidence(np.full((1, 3, 50), 1.7))
+    assert np.allclose(conf, 1 / 50, atol=1e-16, rtol=0)
+    assert np.all(am == 0) and np.all(mg == 0)
+
+
+def test_confidence_matches_torch_library():
+    z = 2.0 * RNG.standard_normal((2, 6, 3001))
+    conf, am, mg = oracle.confidence(z)
+    t = torch.from_numpy(z)
+    p = torch.softmax(t, dim=-1)
+    assert np.allclose(conf, p.max(-1).values.numpy(), atol=1e-15, rtol=1e-12)
+    assert np.array_equal(am, torch.argmax(t, -1).numpy())
+    top2 = torch.topk(t, 2, dim=-1).values
+    assert np.allclose(mg, (top2[..., 0] - top2[..., 1]).numpy(), atol=0, rtol=0)
+
+
+def test_confidence_shift_invariance():
+    z = RNG.standard_normal((1, 4, 300))
+    a = oracle.confidence(z)
+    b = oracle.confidence(z + 123.25)
+    assert np.allclose(a[0], b[0], atol=1e-14)
+    assert np.array_equal(a[1], b[1])
+    assert np.allclose(a[2], b[2], atol=1e-12)
+
+
+def test_confidence_brute_force_small_V():
+    for V in range(2, 9):
+        z = np.round(RNG.standard_normal((1, 5, V)) * 2, 1)  # rounding makes ties likely
+        conf, am, mg = oracle.confidence(z)
+        for r in range(5):
+            row = [float(x) for x in z[0, r]]
+            best = 0
+            for j in range(1, V):
+                if row[j] > row[best]:
+                    best = j
+            total = 0.0
+            for j in range(V):
+                total += math.exp(row[j] - row[best])
+            second = max(row[j] for j in range(V) if j != best)
+            assert am[0, r] == best
+            assert abs(conf[0, r] - 1.0 / total) < 1e-15
+            assert mg[0, r] == row[best] - second
+
+
+def test_confidence_row_idx_and_count():
+    z = RNG.standard_normal((2, 10, 20))
+    row_idx = np.array([[3, 1, 9, 0], [2, 2, 5, 7]], dtype=np.int32)
+    count = np.array([3, 1])
+    conf, am, mg = oracle.confidence(z, count=count, row_idx=row_idx)
+    full_conf, full_am, _ = oracle.confidence(z)
+    for b in range(2):
+        for r in range(4):
+            if r < count[b]:
+                assert conf[b, r] == full_conf[b, row_idx[b, r]]
+                assert am[b, r] == full_am[b, row_idx[b, r]]
+            else:
+                assert np.isnan(conf[b, r]) and am[b, r] == -1
+
+
+# ---------------------------------------------------------------- scatter
+
+def test_scatter_properties():
+    B, L, H, d, M = 2, 40, 3, 8, 12
+    kc = RNG.standard_normal((B, L, H, d))
+    vc = RNG.standard_normal((B, L, H, d))
+    kn = RNG.standard_normal((B, M, H, d))
+    vn = RNG.standard_normal((B, M, H, d))
+    idx = np.full((B, M), -1, dtype=np.int32)
+    idx[0, :5] = [0, 3, 4, 5, 39]
+    idx[1, :0] = []
+    count = np.array([5, 0])
+    k2, v2 = oracle.kv_scatter(kc, vc, kn, vn, idx, count)
+    assert np.array_equal(k2[0, idx[0, :5]], kn[0, :5])
+    assert np.array_equal(v2[0, idx[0, :5]], vn[0, :5])
+    untouched = np.setdiff1d(np.arange(L), idx[0, :5])
+    assert np.array_equal(k2[0, untouched], kc[0, untouched])
+    assert np.array_equal(k2[1], kc[1]) and np.array_equal(v2[1], vc[1])
+    assert not np.shares_memory(k2, kc)
+
+
+# ---------------------------------------------------------------- attention
+
+def test_attention_golden(golden):
+    for case in golden["attention"]:
+        q = np.array(case["q"])[None, :, None, :]
+        k = np.array(case["k"])[None, :, None, :]
+        v = np.array(case["v"])[None, :, None, :]
+        o, lse, cs = oracle.partial_attention(q, k, v, [1])
+        assert np.allclose(o[0, 0, 0], case["o"], atol=1e-14, rtol=0)
+        assert abs(lse[0, 0, 0] - case["lse"]) < 1e-14
+        assert np.allclose(cs[0, 0], case["colsum"], atol=1e-15, rtol=0)
+
+
+def _rand_attn(B, M, L, H, d, seed=0):
+    r = np.random.default_rng(seed)
+    return (r.standard_normal((B, M, H, d)), r.standard_normal((B, L, H, d)),
+            r.standard_normal((B, L, H, d)))
+
+
+def test_attention_all_active_equals_torch_sdpa():
+    B, L, H, d = 2, 37, 3, 16
+    q, k, v = _rand_attn(B, L, L, H, d)
+    o, lse, cs = oracle.partial_attention(q, k, v, [L, L])
+    tq = torch.from_numpy(q).permute(0, 2, 1, 3)
+    tk = torch.from_numpy(k).permute(0, 2, 1, 3)
+    tv = torch.from_numpy(v).permute(0, 2, 1, 3)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv).permute(0, 2, 1, 3)
+    assert np.allclose(o, ref.numpy(), atol=1e-13, rtol=0)
+    s = torch.matmul(tq, tk.transpose(-1, -2)) / math.sqrt(d)
+    assert np.allclose(lse, torch.logsumexp(s, -1).numpy(), atol=1e-13, rtol=0)
+    # full-matrix column sums when every row is active
+    assert np.allclose(cs, torch.softmax(s, -1).sum(-2).numpy(), atol=1e-12, rtol=0)
+
+
+def test_attention_zero_query_gives_mean_and_uniform_colsum():
+    B, M, L, H, d = 1, 9, 23, 2, 8
+    q, k, v = _rand_attn(B, M, L, H, d, 3)
+    q[:] = 0
+    o, lse, cs = oracle.partial_attention(q, k, v, [7])
+    assert np.allclose(o[0, :7], np.broadcast_to(v[0].mean(0), (7, H, d)), atol=1e-14)
+    assert np.allclose(lse[0, :, :7], math.log(L), atol=1e-14)
+    assert np.allclose(cs, 7 / L, atol=1e-14, rtol=0)
+    assert np.all(np.isnan(o[0, 7:]))
+
+
+def test_attention_single_key():
+    q, k, v = _rand_attn(1, 4, 1, 2, 8, 5)
+    o, lse, cs = oracle.partial_attention(q, k, v, [4])
+    assert np.allclose(o[0], np.broadcast_to(v[0, 0], (4, 2, 8)), atol=1e-15)
+    s = np.einsum("mhd,hd->hm", q[0], k[0, 0]) / math.sqrt(8)
+    assert np.allclose(lse[0], s, atol=1e-14)
+    assert np.allclose(cs, 4.0, atol=1e-14)
+
+
+def test_attention_key_permutation_invariance():
+    q, k, v = _rand_attn(1, 6, 31, 2, 16, 9)
+    perm = RNG.permutation(31)
+    a = oracle.partial_attention(q, k, v, [6])
+    b = oracle.partial_attention(q, k[:, perm], v[:, perm], [6])
+    assert np.allclose(a[0], b[0], atol=1e-14)
+    assert np.allclose(a[1], b[1], atol=1e-14)
+    assert np.allclose(a[2][..., perm], b[2], atol=1e-15)
+
+
+def test_attention_brute_force_tiny():
+    for L in range(1, 9):
+        q, k, v = _rand_attn(1, 3, L, 2, 4, L)
+        scale = 0.37
+        o, lse, cs = oracle.partial_attention(q, k, v, [2], scale)
+        for h in range(2):
+            col = [0.0] * L
+            for i in range(2):
+                s = [scale * sum(q[0, i, h, t] * k[0, j, h, t] for t in range(4)) for j in range(L)]
+                mx = max(s)
+                w = [math.exp(x - mx) for x in s]
+                tot = sum(w)
+                for t in range(4):
+                    ref = sum(w[j] * v[0, j, h, t] for j in range(L)) / tot
+                    assert abs(o[0, i, h, t] - ref) < 1e-13
+                assert abs(lse[0, h, i] - (mx + math.log(tot))) < 1e-13
+                for j in range(L):
+                    col[j] += w[j] / tot
+            assert np.allclose(cs[0, h], col, atol=1e-14, rtol=0)
+
+
+def test_attention_colsum_sums_to_count_and_ignores_padding():
+    q, k, v = _rand_attn(2, 20, 45, 3, 8, 11)
+    a = oracle.partial_attention(q, k, v, [13, 0])
+    assert np.allclose(a[2][0].sum(-1), 13, atol=1e-12)
+    assert np.all(a[2][1] == 0)
+    q2 = q.copy()
+    q2[0, 13:] = 1e3  # garbage in padded rows must not matter
+    b = oracle.partial_attention(q2, k, v, [13, 0])
+    assert np.array_equal(a[0][0, :13], b[0][0, :13])
+    assert np.array_equal(a[2], b[2])
+
+
+# ---------------------------------------------------------------- stable prefix
+
+def test_prefix_golden(golden):
+    for case in golden["stable_prefix"]:
+        score = np.array([case["score"]], dtype=np.float32)
+        for c in case["cases"]:
+            got = oracle.stable_prefix(score, [c["start"]], case["tau"], c["min_commit"])
+            assert got[0] == c["len"], c
+
+
+@pytest.mark.parametrize("n", [1, 3, 6, 10])
+def test_prefix_brute_force(n):
+    # len is characterised by: every position in [start, start+len) stable and
+    # (start+len == L or position start+len unstable), then the fallback.
+    for bits in itertools.product([False, True], repeat=n):
+        score = np.where(np.array(bits), 0.95, 0.2).astype(np.float32)[None, :]
+        for start in range(n + 1):
+            for mc in (False, True):
+                got = int(oracle.stable_prefix(score, [start], 0.9, mc)[0])
+                k = got
+                if mc and start < n and not bits[start]:
+                    assert k == 1
+                    continue
+                assert all(bits[start:start + k])
+                assert start + k == n or not bits[start + k]
+
+
+def test_prefix_nan_and_equality():
+    s = np.array([[0.9, np.nan, 1.0], [np.inf, np.inf, 0.9]], dtype=np.float32)
+    got = oracle.stable_prefix(s, [0, 0], 0.9, False)
+    assert got.tolist() == [1, 3]
+
+
+# ---------------------------------------------------------------- whole step
+
+def _tiny_step_inputs():
+    s = workloads.TINY_F32
+    inp = workloads.make_step(s)
+    d = {k: inp[k].double().numpy() for k in ("cur", "prev", "k_cache", "v_cache",
+                                               "k_new", "v_new", "q", "logits")}
+    return s, inp, d
+
+
+def test_step_all_salient_is_dense_step():
+    s, inp, d = _tiny_step_inputs()
+    score = np.full((1, s.L), np.inf)
+    out = oracle.step(d["cur"], d["prev"], d["k_cache"], d["v_cache"], d["k_new"],
+                      d["v_new"], d["q"], d["logits"], tau=2.0, win_start=0,
+                      score=score, start=[0], tau_c=0.9)
+    assert int(out["count"][0]) == s.L
+    # every cache row replaced, and attention is dense attention over the new cache
+    assert np.array_equal(out["k_cache"], d["k_new"])
+    tq = torch.from_numpy(d["q"]).permute(0, 2, 1, 3)
+    tk = torch.from_numpy(d["k_new"]).permute(0, 2, 1, 3)
+    tv = torch.from_numpy(d["v_new"]).permute(0, 2, 1, 3)
+    ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv).permute(0, 2, 1, 3)
+    assert np.allclose(out["o"], ref.numpy(), atol=1e-13)
+
+
+def test_step_nothing_salient():
+    s, inp, d = _tiny_step_inputs()
+    score = np.full((1, s.L), np.inf)
+    out = oracle.step(d["cur"], d["prev"], d["k_cache"], d["v_cache"], d["k_new"],
+                      d["v_new"], d["q"], d["logits"], tau=-2.0, win_start=0,
+                      score=score, start=[0], tau_c=0.9)
+    assert int(out["count"][0]) == 0
+    assert np.array_equal(out["k_cache"], d["k_cache"])
+    assert np.all(out["colsum"] == 0)
+    assert np.all(np.isnan(out["o"]))
