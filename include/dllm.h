@@ -1,0 +1,236 @@
+/*
+ * dllm.h -- C ABI of the partial denoising step for masked-diffusion language
+ * models (one step that recomputes only a selected subset of token positions).
+ *
+ * The library (libdllm.so) runs every entry point as CUDA kernels for sm_103a
+ * (B300) on the caller's stream.  It never allocates device memory, never
+ * synchronises the stream and never reads device data back to the host: the
+ * active-row counts stay on the device, so a whole step can be captured in a
+ * CUDA graph.
+ *
+ * Common conventions
+ *   - Every data pointer is a DEVICE pointer owned by the caller.  Inputs are
+ *     read only; outputs are written only where stated.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *   - Element types: DLLM_F32 (IEEE float32) or DLLM_BF16 (bfloat16).  Scores,
+ *     log-sum-exps and column sums are always float32; indices int32.
+ *   - Sizes given on the host (M_max, R_max, ...) size the launch; the actual
+ *     per-batch counts are read on the device.
+ *   - Host-side validation failures return before any launch.  A failed launch
+ *     returns DLLM_ERR_CUDA.  dllm_last_error() then describes the failure
+ *     (thread-local string, valid until the next failing call on the thread).
+ *   - `dev_status` (may be NULL): an int32 in device memory that the caller
+ *     zeroes.  A kernel that detects bad device-side data (a count outside
+ *     [0, M_max], an index out of range or out of order, a bounded wait that
+ *     ran out) stores the first such code there (DLLM_ERR_DEVICE_CHECK or
+ *     DLLM_ERR_TIMEOUT), skips the offending row and carries on; it never
+ *     traps.  The caller reads the word back when it wants to check.
+ *
+ * Pages cited (title, then section):
+ *   DyLLM        "DyLLM: Efficient Diffusion LLM Inference via Saliency-based
+ *                 Token Selection and Partial Attention"
+ *   SlowFast     "Accelerating Diffusion Large Language Models with SlowFast
+ *                 Sampling: The Three Golden Principles"
+ *   Attn-Sampler "Attention-Based Sampler for Diffusion Language Models"
+ *   SureLock     "Stopping Computation for Converged Tokens in Masked
+ *                 Diffusion-LM Decoding"
+ *   LSP          "Beyond Scattered Acceptance: Fast and Coherent Inference for
+ *                 DLMs via Longest Stable Prefixes"
+ */
+#ifndef DLLM_H_
+#define DLLM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum dllm_status {
+  DLLM_OK = 0,
+  DLLM_ERR_INVALID_ARG = 1,  /* bad pointer, size, stride or alignment          */
+  DLLM_ERR_UNSUPPORTED = 2,  /* valid request this build does not implement     */
+  DLLM_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed     */
+  DLLM_ERR_DEVICE_CHECK = 4, /* (dev_status only) bad device-side count/index   */
+  DLLM_ERR_TIMEOUT = 5       /* (dev_status only) a bounded device wait expired */
+} dllm_status;
+
+typedef enum dllm_dtype { DLLM_F32 = 0, DLLM_BF16 = 1 } dllm_dtype;
+
+/* Library version string, e.g. "dllm 0.1.0 sm_103a". */
+const char* dllm_version(void);
+
+/* Message of the last failing call on this thread ("" if none). */
+const char* dllm_last_error(void);
+
+/*
+ * dllm_saliency_select -- temporal cosine saliency, threshold and ordered
+ * compaction of the active positions.
+ *
+ * DyLLM, technical summary, Methodology 1 (layer-adaptive saliency selection):
+ * the cosine similarity s of each token's vector at step t and its cached
+ * vector at step t-1; a cosine near 1 is stable, a low one is salient and is
+ * recomputed.  Methodology 3 (adaptive input): the window scored is the
+ * response rows on most steps and the whole sequence every few steps.
+ * SureLock, technical summary section 2: locked positions are never active.
+ *
+ *   cur, prev   [B, Lw, D] of `dtype`; row r of batch b starts at element
+ *               b*batch_stride + r*row_stride (row_stride >= D).  Pass the
+ *               window's first row as the base pointer.
+ *   locked      [B, Lw] uint8 (nonzero = locked), contiguous, or NULL.
+ *   tau         threshold: active iff !(cos >= tau) and not locked
+ *               (cos == tau is stable; a NaN cosine is salient).
+ *   idx_base    added to every emitted index (e.g. the prompt length, so
+ *               idx_out holds absolute sequence positions).
+ *   cos_out     [B, Lw] float32: cos = <cur,prev> / (|cur| |prev|); both norms
+ *               zero -> 1, exactly one zero -> 0.  Float32 accumulation.
+ *   idx_out     [B, Lw] int32: ascending active positions + idx_base in
+ *               [0, count), then -1.
+ *   count_out   [B] int32: number of active positions.
+ *
+ * Errors: INVALID_ARG for NULL required pointers, B/Lw/D < 1, row_stride < D,
+ * batch_stride < Lw*row_stride.  Never touches dev_status (may be NULL).
+ */
+dllm_status dllm_saliency_select(const void* cur, const void* prev, int dtype,
+                                 int B, int Lw, int D, int64_t row_stride,
+                                 int64_t batch_stride, const uint8_t* locked,
+                                 float tau, int32_t idx_base, float* cos_out,
+                                 int32_t* idx_out, int32_t* count_out,
+                                 int32_t* dev_status, void* stream);
+
+/*
+ * dllm_confidence -- max softmax probability, argmax and logit margin per row.
+ *
+ * SlowFast, section 2 (certainty principle; the fast phase unmasks tokens
+ * whose confidence exceeds a high threshold).  SureLock, technical summary
+ * section 2, locking criterion 2: the uncertainty 1 - max_v p(v) (here
+ * 1 - conf).  LSP, technical summary section 2 step 1: the logit margin, the
+ * highest minus the second-highest logit.
+ *
+ *   logits      [B, R_src, V] of `dtype`; row r of batch b starts at element
+ *               b*batch_stride + r*row_stride (row_stride >= V).
+ *   R_max       rows scored per batch row (launch size).
+ *   row_idx     [B, R_max] int32 or NULL: row r reads logits row row_idx[b,r]
+ *               (must be in [0, R_src)); NULL reads row r (R_max <= R_src).
+ *   count       [B] int32 or NULL: rows r < count[b] are scored (NULL: all
+ *               R_max).  Must lie in [0, R_max].
+ *   out_idx     [B, R_max] int32 or NULL: the results of row r land in column
+ *               out_idx[b,r] (in [0, out_cols)) of the outputs; NULL: column r
+ *               (R_max <= out_cols).
+ *   conf_out    [B, out_cols] float32 (batch stride out_cols): max_j softmax_j.
+ *   argmax_out  [B, out_cols] int32: lowest index of the maximum logit.
+ *   margin_out  [B, out_cols] float32 or NULL: top-1 minus top-2 logit (0 on a
+ *               tie for the maximum).
+ *   ws          device workspace of at least dllm_confidence_workspace_bytes()
+ *               bytes (256-byte aligned); its contents need no initialisation.
+ * Columns not written are left untouched.  Logits must be finite.
+ * Errors: INVALID_ARG (NULLs, V < 2, R_max < 1, strides, small workspace);
+ * dev_status gets DEVICE_CHECK for counts/indices out of range (row skipped).
+ */
+size_t dllm_confidence_workspace_bytes(int B, int R_max, int V, int dtype);
+
+dllm_status dllm_confidence(const void* logits, int dtype, int B, int R_src,
+                            int V, int64_t row_stride, int64_t batch_stride,
+                            int R_max, const int32_t* row_idx,
+                            const int32_t* count, const int32_t* out_idx,
+                            int out_cols, float* conf_out, int32_t* argmax_out,
+                            float* margin_out, void* ws, size_t ws_bytes,
+                            int32_t* dev_status, void* stream);
+
+/*
+ * dllm_kv_scatter -- write the fresh K/V rows of the active positions into
+ * the full-sequence cache.
+ *
+ * SureLock, technical summary section 2: the K/V of locked positions stay in
+ * the cache and active tokens keep attending to them; only active positions
+ * get new K/V.  LSP, technical summary section 2 ("KV Cache"): contiguous
+ * appends instead of fragmented updates (a run of consecutive indices is the
+ * same call).
+ *
+ *   k_cache, v_cache  [B, L, H, d] of `dtype`, contiguous (updated in place).
+ *   k_new, v_new      [B, M_max, H, d], contiguous: row i of batch b is the
+ *                     fresh row of position idx[b, i].
+ *   idx               [B, M_max] int32: for i < count[b], strictly increasing
+ *                     positions in [0, L).
+ *   count             [B] int32 in [0, M_max].
+ * Every other cache row is left bitwise unchanged.  A row whose index is out
+ * of range or not above its predecessor is skipped and dev_status gets
+ * DEVICE_CHECK.
+ */
+dllm_status dllm_kv_scatter(void* k_cache, void* v_cache, const void* k_new,
+                            const void* v_new, int dtype, int B, int L, int H,
+                            int d, int M_max, const int32_t* idx,
+                            const int32_t* count, int32_t* dev_status,
+                            void* stream);
+
+/*
+ * dllm_partial_attention -- bidirectional attention of the active query rows
+ * over the whole cached K/V, with optional per-key column sums.
+ *
+ * DyLLM, technical summary, Methodology 2 (salient path: score rows of the
+ * salient queries are recomputed in full).  SureLock, technical summary
+ * section 2: active tokens attend to every position through the cached K/V;
+ * cost O(M N d) for M active rows.  Attn-Sampler, technical summary,
+ * Methodology 2: column sums of the attention matrix, computed block-wise
+ * without materialising it.
+ *
+ *   q           [B, M_max, H, d] of `dtype`: rows i < count[b] are the active
+ *               queries (already projected); rows beyond are ignored.
+ *   k_cache, v_cache [B, L, H, d] of `dtype`.
+ *   count       [B] int32 in [0, M_max].
+ *   scale       score scale; <= 0 selects 1/sqrt(d).
+ *   o_out       [B, M_max, H, d] of `dtype`: o_i = sum_j softmax_j(s_i) v_j,
+ *               s_ij = scale <q_i, k_j>, no mask; written for rows < count.
+ *   lse_out     [B, H, M_max] float32 or NULL: log sum_j exp s_ij (rows <
+ *               count).  Required when colsum_out is given.
+ *   colsum_out  [B, H, L] float32 or NULL: colsum[b,h,j] = sum over active
+ *               rows i of exp(s_ij - lse_i) (written for every j; zero when
+ *               count[b] == 0).
+ *   ws          workspace of dllm_attention_workspace_bytes() bytes (may be 0).
+ * Supported: d in {32, 64, 128} (bf16 d == 128 runs on the tensor cores).
+ * Errors: INVALID_ARG, UNSUPPORTED (other d); dev_status gets DEVICE_CHECK for
+ * a count outside [0, M_max] (clamped) and TIMEOUT if a bounded pipeline wait
+ * expires (that tile's outputs are then not written).
+ */
+size_t dllm_attention_workspace_bytes(int B, int L, int H, int d, int M_max,
+                                      int dtype);
+
+dllm_status dllm_partial_attention(const void* q, const void* k_cache,
+                                   const void* v_cache, int dtype, int B, int L,
+                                   int H, int d, int M_max,
+                                   const int32_t* count, float scale,
+                                   void* o_out, float* lse_out,
+                                   float* colsum_out, void* ws, size_t ws_bytes,
+                                   int32_t* dev_status, void* stream);
+
+/*
+ * dllm_stable_prefix -- length of the longest stable block at the head of
+ * the remaining active suffix.
+ *
+ * LSP, technical summary section 2: commit the longest contiguous stable
+ * block at the start of the remaining active sequence in one step, judged by
+ * a per-position stability score (step 1); step 4 (fallback) commits at least
+ * one token when none is stable.
+ *
+ *   score       [B, L] float32, contiguous: position p is stable iff
+ *               score[b,p] >= tau (NaN is unstable).  Callers write +inf at
+ *               positions that must count as stable (already committed).
+ *   start       [B] int32 in [0, L]: first position of the remaining suffix.
+ *   min_commit  nonzero: a zero length becomes 1 when start < L.
+ *   advance_start nonzero: start[b] += len[b] after the scan (start is then
+ *               written).
+ *   len_out     [B] int32.
+ * Errors: INVALID_ARG; dev_status gets DEVICE_CHECK for start outside [0, L]
+ * (len 0, start unchanged).
+ */
+dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start,
+                               float tau, int min_commit, int advance_start,
+                               int32_t* len_out, int32_t* dev_status,
+                               void* stream);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif  /* DLLM_H_ */

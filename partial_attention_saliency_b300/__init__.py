@@ -1,0 +1,24 @@
+"""Partial denoising step for masked-diffusion language models on B300.
+
+One step recomputes only a selected subset of token positions: cosine saliency
+selection, KV-cache scatter, partial attention with column sums, confidence /
+argmax / margin, and the longest stable prefix.  Every operation runs in the
+hand-written sm_103a kernels of ``libdllm.so`` behind a C ABI
+(``include/dllm.h``); the functions below are its ctypes binding, with the
+same names.  PyTorch provides device memory and streams only.
+"""
+from ._lib import (  # noqa: F401
+    DllmError,
+    LIB_PATH,
+    SIGNATURES,
+    dllm_attention_workspace_bytes,
+    dllm_confidence,
+    dllm_confidence_workspace_bytes,
+    dllm_kv_scatter,
+    dllm_partial_attention,
+    dllm_saliency_select,
+    dllm_stable_prefix,
+    dllm_version,
+    load_library,
+)
+from .step import PartialStep  # noqa: F401

@@ -1,0 +1,265 @@
+"""ctypes binding of libdllm.so: argument marshalling only.
+
+Every wrapper takes torch CUDA tensors, checks dtypes/devices/strides, passes
+raw device pointers and the current CUDA stream to the C entry point of the
+same name, and raises ``DllmError`` on a non-zero status.  No computation of
+the step happens here: it all runs in the library's kernels.  If the library
+is missing the import fails loudly; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "libdllm.so")
+
+DLLM_OK = 0
+STATUS_NAMES = {0: "DLLM_OK", 1: "DLLM_ERR_INVALID_ARG", 2: "DLLM_ERR_UNSUPPORTED",
+                3: "DLLM_ERR_CUDA", 4: "DLLM_ERR_DEVICE_CHECK", 5: "DLLM_ERR_TIMEOUT"}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+
+# Every symbol include/dllm.h declares, with (restype, argtypes).
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+SIGNATURES = {
+    "dllm_version": (ctypes.c_char_p, []),
+    "dllm_last_error": (ctypes.c_char_p, []),
+    "dllm_saliency_select": (_I, [_P, _P, _I, _I, _I, _I, _I64, _I64, _P, _F, ctypes.c_int32,
+                                  _P, _P, _P, _P, _P]),
+    "dllm_confidence_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "dllm_confidence": (_I, [_P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P,
+                             _P, _SZ, _P, _P]),
+    "dllm_kv_scatter": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
+    "dllm_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
+    "dllm_partial_attention": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P,
+                                    _SZ, _P, _P]),
+    "dllm_stable_prefix": (_I, [_P, _I, _I, _P, _F, _I, _I, _P, _P, _P]),
+}
+
+
+class DllmError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+_LIB: Optional[ctypes.CDLL] = None
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libdllm.so (once) and declare every exported entry point."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    if not os.path.exists(path):
+        raise ImportError(
+            f"{path} is missing: build it with `python -m partial_attention_saliency_b300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _LIB = lib
+    return lib
+
+
+def _check(status: int):
+    if status != DLLM_OK:
+        raise DllmError(status, load_library().dllm_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _dtype(*ts: torch.Tensor) -> int:
+    dt = ts[0].dtype
+    for t in ts:
+        if t.dtype != dt:
+            raise TypeError(f"dtype mismatch: {t.dtype} vs {dt}")
+        if not t.is_cuda:
+            raise ValueError("tensors must live on a CUDA device")
+    if dt not in DTYPES:
+        raise TypeError(f"unsupported dtype {dt}; use float32 or bfloat16")
+    return DTYPES[dt]
+
+
+def _need(t: torch.Tensor, dtype, shape, name):
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name}: need contiguous CUDA {dtype} {tuple(shape)}, got "
+                         f"{t.dtype} {tuple(t.shape)} contiguous={t.is_contiguous()}")
+
+
+def dllm_version() -> str:
+    return load_library().dllm_version().decode()
+
+
+def dllm_confidence_workspace_bytes(B: int, R_max: int, V: int, dtype: torch.dtype) -> int:
+    return int(load_library().dllm_confidence_workspace_bytes(B, R_max, V, DTYPES[dtype]))
+
+
+def dllm_attention_workspace_bytes(B: int, L: int, H: int, d: int, M_max: int,
+                                   dtype: torch.dtype) -> int:
+    return int(load_library().dllm_attention_workspace_bytes(B, L, H, d, M_max, DTYPES[dtype]))
+
+
+def dllm_saliency_select(cur: torch.Tensor, prev: torch.Tensor, tau: float, *,
+                         locked: Optional[torch.Tensor] = None, idx_base: int = 0,
+                         cos_out=None, idx_out=None, count_out=None, dev_status=None,
+                         stream=None):
+    """Cosine saliency + ordered compaction over a [B, Lw, D] window.
+
+    ``cur``/``prev`` may be strided views (last dim contiguous).  Returns
+    (cos [B, Lw] f32, idx [B, Lw] i32, count [B] i32).
+    """
+    lib = load_library()
+    dt = _dtype(cur, prev)
+    if cur.dim() != 3 or cur.shape != prev.shape or cur.stride() != prev.stride():
+        raise ValueError("cur/prev must be [B, Lw, D] with identical strides")
+    if cur.stride(2) != 1:
+        raise ValueError("the hidden dim must be contiguous")
+    B, Lw, D = cur.shape
+    dev = cur.device
+    cos_out = torch.empty((B, Lw), dtype=torch.float32, device=dev) if cos_out is None else cos_out
+    idx_out = torch.empty((B, Lw), dtype=torch.int32, device=dev) if idx_out is None else idx_out
+    count_out = torch.empty((B,), dtype=torch.int32, device=dev) if count_out is None else count_out
+    _need(cos_out, torch.float32, (B, Lw), "cos_out")
+    _need(idx_out, torch.int32, (B, Lw), "idx_out")
+    _need(count_out, torch.int32, (B,), "count_out")
+    if locked is not None:
+        _need(locked, torch.uint8, (B, Lw), "locked")
+    _check(lib.dllm_saliency_select(_ptr(cur), _ptr(prev), dt, B, Lw, D, cur.stride(1),
+                                    cur.stride(0), _ptr(locked), float(tau), int(idx_base),
+                                    _ptr(cos_out), _ptr(idx_out), _ptr(count_out),
+                                    _ptr(dev_status), _stream(stream)))
+    return cos_out, idx_out, count_out
+
+
+def dllm_confidence(logits: torch.Tensor, *, R_max: Optional[int] = None, row_idx=None,
+                    count=None, out_idx=None, out_cols: Optional[int] = None, conf_out=None,
+                    argmax_out=None, margin_out=None, with_margin: bool = True, ws=None,
+                    dev_status=None, stream=None):
+    """Confidence, argmax and margin per logit row.
+
+    ``logits`` [B, R_src, V] (last dim contiguous, rows may be strided).
+    Outputs are [B, out_cols] (default out_cols = R_max).  Returns
+    (conf, argmax, margin-or-None).
+    """
+    lib = load_library()
+    dt = _dtype(logits)
+    if logits.dim() != 3 or logits.stride(2) != 1:
+        raise ValueError("logits must be [B, R_src, V] with a contiguous vocabulary dim")
+    B, R_src, V = logits.shape
+    R_max = R_src if R_max is None else int(R_max)
+    out_cols = R_max if out_cols is None else int(out_cols)
+    dev = logits.device
+    if conf_out is None:
+        conf_out = torch.empty((B, out_cols), dtype=torch.float32, device=dev)
+    if argmax_out is None:
+        argmax_out = torch.empty((B, out_cols), dtype=torch.int32, device=dev)
+    if margin_out is None and with_margin:
+        margin_out = torch.empty((B, out_cols), dtype=torch.float32, device=dev)
+    for t, n, ty in ((conf_out, "conf_out", torch.float32), (argmax_out, "argmax_out", torch.int32),
+                     (margin_out, "margin_out", torch.float32)):
+        if t is not None and (t.dtype != ty or not t.is_cuda or t.stride(-1) != 1
+                              or t.shape[0] != B or (B > 1 and t.stride(0) != out_cols)):
+            raise ValueError(f"{n}: need CUDA {ty} [B, out_cols] rows")
+    for t, n in ((row_idx, "row_idx"), (out_idx, "out_idx")):
+        if t is not None:
+            _need(t, torch.int32, (B, R_max), n)
+    if count is not None:
+        _need(count, torch.int32, (B,), "count")
+    need = lib.dllm_confidence_workspace_bytes(B, R_max, V, dt)
+    if ws is None:
+        ws = torch.empty((max(int(need), 16),), dtype=torch.uint8, device=dev)
+    _check(lib.dllm_confidence(_ptr(logits), dt, B, R_src, V, logits.stride(1), logits.stride(0),
+                               R_max, _ptr(row_idx), _ptr(count), _ptr(out_idx), out_cols,
+                               _ptr(conf_out), _ptr(argmax_out), _ptr(margin_out), _ptr(ws),
+                               ws.numel() * ws.element_size(), _ptr(dev_status),
+                               _stream(stream)))
+    return conf_out, argmax_out, margin_out
+
+
+def dllm_kv_scatter(k_cache, v_cache, k_new, v_new, idx, count, *, dev_status=None, stream=None):
+    """Write fresh K/V rows into the cache in place at idx[b, :count[b]]."""
+    lib = load_library()
+    dt = _dtype(k_cache, v_cache, k_new, v_new)
+    B, L, H, d = k_cache.shape
+    M_max = k_new.shape[1]
+    _need(k_cache, k_cache.dtype, (B, L, H, d), "k_cache")
+    _need(v_cache, k_cache.dtype, (B, L, H, d), "v_cache")
+    _need(k_new, k_cache.dtype, (B, M_max, H, d), "k_new")
+    _need(v_new, k_cache.dtype, (B, M_max, H, d), "v_new")
+    _need(idx, torch.int32, (B, M_max), "idx")
+    _need(count, torch.int32, (B,), "count")
+    _check(lib.dllm_kv_scatter(_ptr(k_cache), _ptr(v_cache), _ptr(k_new), _ptr(v_new), dt, B, L,
+                               H, d, M_max, _ptr(idx), _ptr(count), _ptr(dev_status),
+                               _stream(stream)))
+    return k_cache, v_cache
+
+
+def dllm_partial_attention(q, k_cache, v_cache, count, *, scale: float = 0.0, o_out=None,
+                           lse_out=None, colsum_out=None, with_lse: bool = True,
+                           with_colsum: bool = True, ws=None, dev_status=None, stream=None):
+    """Attention of the active query rows over the whole cache (+ column sums).
+
+    Returns (o [B, M_max, H, d], lse [B, H, M_max] or None, colsum [B, H, L] or None).
+    """
+    lib = load_library()
+    dt = _dtype(q, k_cache, v_cache)
+    B, M_max, H, d = q.shape
+    L = k_cache.shape[1]
+    _need(q, q.dtype, (B, M_max, H, d), "q")
+    _need(k_cache, q.dtype, (B, L, H, d), "k_cache")
+    _need(v_cache, q.dtype, (B, L, H, d), "v_cache")
+    _need(count, torch.int32, (B,), "count")
+    dev = q.device
+    o_out = torch.empty_like(q) if o_out is None else o_out
+    if lse_out is None and (with_lse or with_colsum):
+        lse_out = torch.empty((B, H, M_max), dtype=torch.float32, device=dev)
+    if colsum_out is None and with_colsum:
+        colsum_out = torch.empty((B, H, L), dtype=torch.float32, device=dev)
+    _need(o_out, q.dtype, (B, M_max, H, d), "o_out")
+    if lse_out is not None:
+        _need(lse_out, torch.float32, (B, H, M_max), "lse_out")
+    if colsum_out is not None:
+        _need(colsum_out, torch.float32, (B, H, L), "colsum_out")
+    need = int(lib.dllm_attention_workspace_bytes(B, L, H, d, M_max, dt))
+    if ws is None and need > 0:
+        ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(lib.dllm_partial_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), dt, B, L, H, d,
+                                      M_max, _ptr(count), float(scale), _ptr(o_out),
+                                      _ptr(lse_out), _ptr(colsum_out), _ptr(ws), ws_bytes,
+                                      _ptr(dev_status), _stream(stream)))
+    return o_out, lse_out, colsum_out
+
+
+def dllm_stable_prefix(score, start, tau: float, *, min_commit: bool = True,
+                       advance_start: bool = False, len_out=None, dev_status=None, stream=None):
+    """Longest stable prefix per batch row; optionally advances ``start`` in place."""
+    lib = load_library()
+    B, L = score.shape
+    _need(score, torch.float32, (B, L), "score")
+    _need(start, torch.int32, (B,), "start")
+    len_out = torch.empty((B,), dtype=torch.int32, device=score.device) if len_out is None else len_out
+    _need(len_out, torch.int32, (B,), "len_out")
+    _check(lib.dllm_stable_prefix(_ptr(score), B, L, _ptr(start), float(tau), int(min_commit),
+                                  int(advance_start), _ptr(len_out), _ptr(dev_status),
+                                  _stream(stream)))
+    return len_out

@@ -1,0 +1,190 @@
+// extern "C" entry points of libdllm: argument validation, launch, error text.
+//
+// Nothing here allocates device memory, synchronises a stream or reads device
+// data: counts stay on the device and the kernels read them there.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "dllm.h"
+#include "internal.h"
+
+namespace dllm {
+
+int num_sms() {
+  static thread_local int cached_dev = -1;
+  static thread_local int cached_sms = 148;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cached_sms;
+  if (dev != cached_dev) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+      cached_sms = sms;
+    cached_dev = dev;
+  }
+  return cached_sms;
+}
+
+}  // namespace dllm
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dllm_status fail(dllm_status code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return code;
+}
+
+dllm_status from_cuda(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return DLLM_OK;
+  return fail(DLLM_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool valid_dtype(int dt) { return dt == DLLM_F32 || dt == DLLM_BF16; }
+
+#define REQUIRE(cond, ...)                                   \
+  do {                                                       \
+    if (!(cond)) return fail(DLLM_ERR_INVALID_ARG, __VA_ARGS__); \
+  } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char* dllm_version(void) { return "dllm 0.1.0 sm_103a"; }
+
+const char* dllm_last_error(void) { return g_last_error.c_str(); }
+
+dllm_status dllm_saliency_select(const void* cur, const void* prev, int dtype, int B, int Lw,
+                                 int D, int64_t row_stride, int64_t batch_stride,
+                                 const uint8_t* locked, float tau, int32_t idx_base,
+                                 float* cos_out, int32_t* idx_out, int32_t* count_out,
+                                 int32_t* dev_status, void* stream) {
+  (void)dev_status;
+  REQUIRE(cur && prev && cos_out && idx_out && count_out,
+          "dllm_saliency_select: NULL input or output pointer");
+  REQUIRE(valid_dtype(dtype), "dllm_saliency_select: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && Lw >= 1 && D >= 1, "dllm_saliency_select: B=%d Lw=%d D=%d must be >= 1", B,
+          Lw, D);
+  REQUIRE(row_stride >= D, "dllm_saliency_select: row_stride %lld < D %d",
+          (long long)row_stride, D);
+  REQUIRE(B == 1 || batch_stride >= (int64_t)Lw * row_stride,
+          "dllm_saliency_select: batch_stride %lld < Lw*row_stride", (long long)batch_stride);
+  REQUIRE((int64_t)idx_base + Lw <= INT32_MAX && idx_base >= 0,
+          "dllm_saliency_select: idx_base %d out of range", idx_base);
+  return from_cuda(dllm::launch_saliency_select(cur, prev, dtype, B, Lw, D, row_stride,
+                                                batch_stride, locked, tau, idx_base, cos_out,
+                                                idx_out, count_out,
+                                                static_cast<cudaStream_t>(stream)),
+                   "dllm_saliency_select launch");
+}
+
+size_t dllm_confidence_workspace_bytes(int B, int R_max, int V, int dtype) {
+  if (B < 1 || R_max < 1 || V < 1 || !valid_dtype(dtype)) return 0;
+  return dllm::confidence_workspace_bytes(B, R_max, V, dtype);
+}
+
+dllm_status dllm_confidence(const void* logits, int dtype, int B, int R_src, int V,
+                            int64_t row_stride, int64_t batch_stride, int R_max,
+                            const int32_t* row_idx, const int32_t* count,
+                            const int32_t* out_idx, int out_cols, float* conf_out,
+                            int32_t* argmax_out, float* margin_out, void* ws, size_t ws_bytes,
+                            int32_t* dev_status, void* stream) {
+  REQUIRE(logits && conf_out && argmax_out, "dllm_confidence: NULL logits or output pointer");
+  REQUIRE(valid_dtype(dtype), "dllm_confidence: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && R_src >= 1 && R_max >= 1, "dllm_confidence: B=%d R_src=%d R_max=%d", B,
+          R_src, R_max);
+  REQUIRE(V >= 2, "dllm_confidence: V=%d must be >= 2", V);
+  REQUIRE(row_stride >= V, "dllm_confidence: row_stride %lld < V", (long long)row_stride);
+  REQUIRE(B == 1 || batch_stride >= (int64_t)R_src * row_stride,
+          "dllm_confidence: batch_stride too small");
+  REQUIRE(row_idx != nullptr || R_max <= R_src, "dllm_confidence: R_max > R_src without row_idx");
+  REQUIRE(out_cols >= 1 && (out_idx != nullptr || R_max <= out_cols),
+          "dllm_confidence: out_cols %d too small", out_cols);
+  const size_t need = dllm::confidence_workspace_bytes(B, R_max, V, dtype);
+  REQUIRE(ws != nullptr && ws_bytes >= need,
+          "dllm_confidence: workspace %zu bytes < %zu required", ws_bytes, need);
+  REQUIRE(reinterpret_cast<uintptr_t>(ws) % 16 == 0, "dllm_confidence: workspace misaligned");
+  REQUIRE((int64_t)B * R_max <= INT32_MAX, "dllm_confidence: B*R_max too large");
+  return from_cuda(dllm::launch_confidence(logits, dtype, B, R_src, V, row_stride, batch_stride,
+                                           R_max, row_idx, count, out_idx, out_cols, conf_out,
+                                           argmax_out, margin_out, ws, dev_status,
+                                           static_cast<cudaStream_t>(stream)),
+                   "dllm_confidence launch");
+}
+
+dllm_status dllm_kv_scatter(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                            int dtype, int B, int L, int H, int d, int M_max,
+                            const int32_t* idx, const int32_t* count, int32_t* dev_status,
+                            void* stream) {
+  REQUIRE(k_cache && v_cache && k_new && v_new && idx && count,
+          "dllm_kv_scatter: NULL pointer argument");
+  REQUIRE(valid_dtype(dtype), "dllm_kv_scatter: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && L >= 1 && H >= 1 && d >= 1 && M_max >= 1,
+          "dllm_kv_scatter: B=%d L=%d H=%d d=%d M_max=%d must be >= 1", B, L, H, d, M_max);
+  REQUIRE(B <= 65535, "dllm_kv_scatter: B=%d exceeds 65535", B);
+  return from_cuda(dllm::launch_kv_scatter(k_cache, v_cache, k_new, v_new, dtype, B, L, H, d,
+                                           M_max, idx, count, dev_status,
+                                           static_cast<cudaStream_t>(stream)),
+                   "dllm_kv_scatter launch");
+}
+
+size_t dllm_attention_workspace_bytes(int B, int L, int H, int d, int M_max, int dtype) {
+  if (B < 1 || L < 1 || H < 1 || d < 1 || M_max < 1 || !valid_dtype(dtype)) return 0;
+  return dllm::attention_workspace_bytes(B, L, H, d, M_max, dtype);
+}
+
+dllm_status dllm_partial_attention(const void* q, const void* k_cache, const void* v_cache,
+                                   int dtype, int B, int L, int H, int d, int M_max,
+                                   const int32_t* count, float scale, void* o_out,
+                                   float* lse_out, float* colsum_out, void* ws,
+                                   size_t ws_bytes, int32_t* dev_status, void* stream) {
+  REQUIRE(q && k_cache && v_cache && count && o_out,
+          "dllm_partial_attention: NULL pointer argument");
+  REQUIRE(valid_dtype(dtype), "dllm_partial_attention: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && L >= 1 && H >= 1 && M_max >= 1,
+          "dllm_partial_attention: B=%d L=%d H=%d M_max=%d must be >= 1", B, L, H, M_max);
+  REQUIRE(B <= 65535 && H <= 65535, "dllm_partial_attention: B or H above 65535");
+  REQUIRE(colsum_out == nullptr || lse_out != nullptr,
+          "dllm_partial_attention: colsum_out needs lse_out");
+  if (d != 32 && d != 64 && d != 128)
+    return fail(DLLM_ERR_UNSUPPORTED, "dllm_partial_attention: head dim %d not in {32,64,128}", d);
+  const size_t need = dllm::attention_workspace_bytes(B, L, H, d, M_max, dtype);
+  REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr),
+          "dllm_partial_attention: workspace %zu bytes < %zu required", ws_bytes, need);
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)d);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = dllm::launch_attention_simt(q, k_cache, v_cache, dtype, B, L, H, d, M_max,
+                                              count, scale, o_out, lse_out, dev_status, s);
+  if (e != cudaSuccess) return from_cuda(e, "dllm_partial_attention launch");
+  if (colsum_out != nullptr) {
+    e = dllm::launch_colsum_simt(q, k_cache, dtype, B, L, H, d, M_max, count, scale, lse_out,
+                                 colsum_out, dev_status, s);
+    if (e != cudaSuccess) return from_cuda(e, "dllm_partial_attention column-sum launch");
+  }
+  return DLLM_OK;
+}
+
+dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start, float tau,
+                               int min_commit, int advance_start, int32_t* len_out,
+                               int32_t* dev_status, void* stream) {
+  REQUIRE(score && start && len_out, "dllm_stable_prefix: NULL pointer argument");
+  REQUIRE(B >= 1 && L >= 1, "dllm_stable_prefix: B=%d L=%d must be >= 1", B, L);
+  return from_cuda(dllm::launch_stable_prefix(score, B, L, start, tau, min_commit, advance_start,
+                                              len_out, dev_status,
+                                              static_cast<cudaStream_t>(stream)),
+                   "dllm_stable_prefix launch");
+}
+
+}  // extern "C"
+
+namespace dllm {
+size_t attention_workspace_bytes(int, int, int, int, int, int) { return 0; }
+}  // namespace dllm

@@ -1,0 +1,364 @@
+// Confidence (max softmax probability), argmax and logit margin per row.
+//
+// SlowFast ("Accelerating Diffusion LLMs with SlowFast Sampling"), section 2:
+// certainty principle; SureLock, technical summary section 2, locking
+// criterion 2: uncertainty 1 - max_v p(v); LSP, technical summary section 2,
+// step 1: logit margin = top-1 minus top-2 logit.
+//
+// conf = 1 / sum_j exp(z_j - m) with m = max_j z_j; argmax = lowest j with
+// z_j = m; margin = m - max_{j != argmax} z_j.
+//
+// Split-row design (HBM bound, V * sizeof(T) bytes per row): a row of
+// V = 126464 bf16 logits is 253 KB, and a step scores only a few hundred rows,
+// so one CTA per row leaves SMs idle.  conf_partial_kernel gives each CTA one
+// 32 KB chunk of one row, loaded in a single burst of 16-byte vectors (8 per
+// thread in flight), reduces it to (max, second max, sum exp(z - max),
+// argmax) and stores that partial in the workspace; conf_merge_kernel folds
+// the partials of each row in a fixed order (deterministic) and writes the
+// outputs.
+#include <climits>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int kConfThreads = 256;
+constexpr int kConfU = 8;  // 16-byte vectors per thread per chunk
+
+struct ConfPartial {
+  float m1;   // maximum
+  float m2;   // second largest value (equal to m1 on a tie)
+  float l;    // sum of exp(z - m1)
+  int arg;    // lowest index reaching m1
+};
+
+template <typename T> constexpr int vec_elems() { return 16 / (int)sizeof(T); }
+
+template <typename T> __host__ __device__ inline int conf_chunk_elems() {
+  return kConfThreads * kConfU * vec_elems<T>();
+}
+
+__device__ __forceinline__ ConfPartial merge(const ConfPartial& a, const ConfPartial& b) {
+  if (b.m1 == -INFINITY) return a;
+  if (a.m1 == -INFINITY) return b;
+  ConfPartial r;
+  r.m1 = fmaxf(a.m1, b.m1);
+  r.l = a.l * ex2_approx((a.m1 - r.m1) * kLog2e) + b.l * ex2_approx((b.m1 - r.m1) * kLog2e);
+  if (a.m1 > b.m1) {
+    r.arg = a.arg;
+    r.m2 = fmaxf(a.m2, b.m1);
+  } else if (b.m1 > a.m1) {
+    r.arg = b.arg;
+    r.m2 = fmaxf(b.m2, a.m1);
+  } else {
+    r.arg = min(a.arg, b.arg);
+    r.m2 = a.m1;
+  }
+  return r;
+}
+
+// Element e of a 16-byte vector, as float32.
+template <typename T>
+__device__ __forceinline__ float elem_of(const uint4& v, int e) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (std::is_same<T, float>::value) {
+    return __uint_as_float(w[e]);
+  } else {
+    return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+  }
+}
+
+// Vector vi of a row: a 16-byte load when it lies inside [0, V) and VEC holds,
+// else element-wise loads with -inf past the end of the row.
+template <typename T, bool VEC>
+__device__ __forceinline__ uint4 load_vec(const T* row, int vi, int V) {
+  constexpr int E = vec_elems<T>();
+  if (VEC && (vi + 1) * E <= V) return ld_stream16(row + (int64_t)vi * E);
+  uint32_t w[4];
+  if constexpr (std::is_same<T, float>::value) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = vi * E + k;
+      w[k] = i < V ? __float_as_uint(row[i]) : 0xff800000u;
+    }
+  } else {
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i0 = vi * E + 2 * k, i1 = i0 + 1;
+      const uint32_t lo = i0 < V ? h[i0] : 0xff80u;
+      const uint32_t hi = i1 < V ? h[i1] : 0xff80u;
+      w[k] = lo | (hi << 16);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ bool row_valid(int b, int r, int R_max, int R_src,
+                                          const int32_t* row_idx, const int32_t* count,
+                                          int* row_out, bool* bad) {
+  int n = count ? count[b] : R_max;
+  *bad = false;
+  if (n < 0 || n > R_max) {
+    *bad = true;
+    n = n < 0 ? 0 : R_max;
+  }
+  if (r >= n) return false;
+  const int row = row_idx ? row_idx[(int64_t)b * R_max + r] : r;
+  if (row < 0 || row >= R_src) {
+    *bad = true;
+    return false;
+  }
+  *row_out = row;
+  return true;
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kConfThreads)
+conf_partial_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, int64_t bs,
+                    int R_max, const int32_t* __restrict__ row_idx,
+                    const int32_t* __restrict__ count, int nchunks,
+                    ConfPartial* __restrict__ ws) {
+  constexpr int E = vec_elems<T>();
+  const int br = blockIdx.x;
+  const int chunk = blockIdx.y;
+  const int b = br / R_max, r = br - b * R_max;
+  int row;
+  bool bad;
+  if (!row_valid(b, r, R_max, R_src, row_idx, count, &row, &bad)) return;
+  const T* p = logits + (int64_t)b * bs + (int64_t)row * rs;
+  const int tid = threadIdx.x;
+  const int vbase = chunk * (kConfThreads * kConfU);
+  const int nvec = (V + E - 1) / E;
+
+  uint4 v[kConfU];
+#pragma unroll
+  for (int u = 0; u < kConfU; ++u) {
+    const int vi = vbase + u * kConfThreads + tid;
+    v[u] = vi < nvec ? load_vec<T, VEC>(p, vi, V)
+                     : (std::is_same<T, float>::value
+                            ? make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u)
+                            : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u));
+  }
+
+  // -- thread-local top-2 (values only)
+  float t1, t2;
+  if constexpr (std::is_same<T, float>::value) {
+    t1 = -INFINITY;
+    t2 = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kConfU; ++u) {
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float x = elem_of<T>(v[u], e);
+        t2 = fmaxf(t2, fminf(t1, x));
+        t1 = fmaxf(t1, x);
+      }
+    }
+  } else {
+    // two independent packed (max, second) pairs for ILP
+    const __nv_bfloat162 ninf = __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
+    __nv_bfloat162 m1[2] = {ninf, ninf}, m2[2] = {ninf, ninf};
+#pragma unroll
+    for (int u = 0; u < kConfU; ++u) {
+      const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 x = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+        m2[k & 1] = __hmax2(m2[k & 1], __hmin2(m1[k & 1], x));
+        m1[k & 1] = __hmax2(m1[k & 1], x);
+      }
+    }
+    m2[0] = __hmax2(__hmax2(m2[0], m2[1]), __hmin2(m1[0], m1[1]));
+    m1[0] = __hmax2(m1[0], m1[1]);
+    const float a = __bfloat162float(m1[0].x), c = __bfloat162float(m1[0].y);
+    t1 = fmaxf(a, c);
+    t2 = fmaxf(fminf(a, c), fmaxf(__bfloat162float(m2[0].x), __bfloat162float(m2[0].y)));
+  }
+  // -- block top-2
+  __shared__ float s_t1[kConfThreads / 32], s_t2[kConfThreads / 32], s_l[kConfThreads / 32];
+  __shared__ int s_arg[kConfThreads / 32];
+  __shared__ float s_M;
+  const int lane = tid & 31, warp = tid >> 5;
+  const float own_max = t1;  // the thread's own maximum, for the argmax scan
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+    const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+    const float n2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+    t1 = fmaxf(t1, o1);
+    t2 = n2;
+  }
+  if (lane == 0) {
+    s_t1[warp] = t1;
+    s_t2[warp] = t2;
+  }
+  __syncthreads();
+  float M, S2;
+  if (tid == 0) {
+    M = s_t1[0];
+    S2 = s_t2[0];
+    for (int w = 1; w < kConfThreads / 32; ++w) {
+      const float o1 = s_t1[w], o2 = s_t2[w];
+      const float n2 = fmaxf(fminf(M, o1), fmaxf(S2, o2));
+      M = fmaxf(M, o1);
+      S2 = n2;
+    }
+    s_M = M;
+    s_t2[0] = S2;
+  }
+  __syncthreads();
+  M = s_M;
+  S2 = s_t2[0];
+
+  // -- sum of exp(z - M) and lowest index reaching M
+  const float negMl = -M * kLog2e;
+  float lacc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int u = 0; u < kConfU; ++u) {
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      const float x = elem_of<T>(v[u], e);
+      lacc[e & 3] += ex2_approx(fmaf(x, kLog2e, negMl));
+    }
+  }
+  float l = (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
+  // Only threads holding M look for its lowest position; the reverse scan
+  // leaves the smallest index (u, then e, ascend with the element index).
+  int arg = INT_MAX;
+  if (own_max == M) {
+#pragma unroll
+    for (int u = kConfU - 1; u >= 0; --u)
+#pragma unroll
+      for (int e = E - 1; e >= 0; --e)
+        if (elem_of<T>(v[u], e) == M) arg = (vbase + u * kConfThreads + tid) * E + e;
+  }
+  l = warp_sum(l);
+  arg = warp_min_int(arg);
+  if (lane == 0) {
+    s_l[warp] = l;
+    s_arg[warp] = arg;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float lt = 0.f;
+    int at = INT_MAX;
+    for (int w = 0; w < kConfThreads / 32; ++w) {
+      lt += s_l[w];
+      at = min(at, s_arg[w]);
+    }
+    ConfPartial out;
+    out.m1 = M;
+    out.m2 = S2;
+    out.l = lt;
+    out.arg = at;
+    ws[(int64_t)br * nchunks + chunk] = out;
+  }
+}
+
+__global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* __restrict__ row_idx,
+                                  const int32_t* __restrict__ count,
+                                  const int32_t* __restrict__ out_idx, int out_cols, int nchunks,
+                                  const ConfPartial* __restrict__ ws, float* __restrict__ conf_out,
+                                  int32_t* __restrict__ argmax_out, float* __restrict__ margin_out,
+                                  int32_t* dev_status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t br = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (br >= (int64_t)B * R_max) return;
+  const int b = (int)(br / R_max), r = (int)(br - (int64_t)b * R_max);
+  int row;
+  bool bad;
+  const bool ok = row_valid(b, r, R_max, R_src, row_idx, count, &row, &bad);
+  if (bad && lane == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
+  if (!ok) return;
+  int col = r;
+  if (out_idx != nullptr) {
+    col = out_idx[br];
+    if (col < 0 || col >= out_cols) {
+      if (lane == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
+      return;
+    }
+  }
+  ConfPartial acc;
+  acc.m1 = -INFINITY;
+  acc.m2 = -INFINITY;
+  acc.l = 0.f;
+  acc.arg = INT_MAX;
+  for (int c = lane; c < nchunks; c += 32) acc = merge(acc, ws[br * nchunks + c]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ConfPartial other;
+    other.m1 = __shfl_xor_sync(0xffffffffu, acc.m1, o);
+    other.m2 = __shfl_xor_sync(0xffffffffu, acc.m2, o);
+    other.l = __shfl_xor_sync(0xffffffffu, acc.l, o);
+    other.arg = __shfl_xor_sync(0xffffffffu, acc.arg, o);
+    acc = merge(acc, other);
+  }
+  if (lane == 0) {
+    const int64_t o = (int64_t)b * out_cols + col;
+    conf_out[o] = 1.0f / acc.l;
+    argmax_out[o] = acc.arg;
+    if (margin_out != nullptr) margin_out[o] = acc.m1 - acc.m2;
+  }
+}
+
+template <typename T>
+int conf_nchunks(int V) {
+  const int n = (V + conf_chunk_elems<T>() - 1) / conf_chunk_elems<T>();
+  return n < 1 ? 1 : n;
+}
+
+template <typename T>
+cudaError_t launch_typed(const T* logits, int B, int R_src, int V, int64_t rs, int64_t bs,
+                         int R_max, const int32_t* row_idx, const int32_t* count,
+                         const int32_t* out_idx, int out_cols, float* conf_out,
+                         int32_t* argmax_out, float* margin_out, void* ws, int32_t* dev_status,
+                         cudaStream_t stream) {
+  constexpr int E = vec_elems<T>();
+  const int nchunks = conf_nchunks<T>(V);
+  const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (rs % E == 0) &&
+                   (bs % E == 0);
+  dim3 grid(B * R_max, nchunks);
+  ConfPartial* part = static_cast<ConfPartial*>(ws);
+  if (vec)
+    conf_partial_kernel<T, true><<<grid, kConfThreads, 0, stream>>>(
+        logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
+  else
+    conf_partial_kernel<T, false><<<grid, kConfThreads, 0, stream>>>(
+        logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t rows = (int64_t)B * R_max;
+  const int warps = 8;
+  conf_merge_kernel<<<(unsigned)((rows + warps - 1) / warps), warps * 32, 0, stream>>>(
+      B, R_src, R_max, row_idx, count, out_idx, out_cols, nchunks, part, conf_out, argmax_out,
+      margin_out, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t confidence_workspace_bytes(int B, int R_max, int V, int dtype) {
+  const int nchunks = dtype == DLLM_BF16 ? conf_nchunks<__nv_bfloat16>(V) : conf_nchunks<float>(V);
+  return (size_t)B * (size_t)R_max * (size_t)nchunks * sizeof(ConfPartial);
+}
+
+cudaError_t launch_confidence(const void* logits, int dtype, int B, int R_src, int V,
+                              int64_t row_stride, int64_t batch_stride, int R_max,
+                              const int32_t* row_idx, const int32_t* count,
+                              const int32_t* out_idx, int out_cols, float* conf_out,
+                              int32_t* argmax_out, float* margin_out, void* ws,
+                              int32_t* dev_status, cudaStream_t stream) {
+  if (dtype == DLLM_BF16)
+    return launch_typed(static_cast<const __nv_bfloat16*>(logits), B, R_src, V, row_stride,
+                        batch_stride, R_max, row_idx, count, out_idx, out_cols, conf_out,
+                        argmax_out, margin_out, ws, dev_status, stream);
+  return launch_typed(static_cast<const float*>(logits), B, R_src, V, row_stride, batch_stride,
+                      R_max, row_idx, count, out_idx, out_cols, conf_out, argmax_out,
+                      margin_out, ws, dev_status, stream);
+}
+
+}  // namespace dllm

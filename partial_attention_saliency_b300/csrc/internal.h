@@ -1,0 +1,49 @@
+// Launchers behind the C ABI.  Each returns the cudaError_t of its launches;
+// arguments were validated by the entry points in api.cu.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dllm {
+
+cudaError_t launch_saliency_select(const void* cur, const void* prev, int dtype, int B,
+                                   int Lw, int D, int64_t row_stride, int64_t batch_stride,
+                                   const uint8_t* locked, float tau, int32_t idx_base,
+                                   float* cos_out, int32_t* idx_out, int32_t* count_out,
+                                   cudaStream_t stream);
+
+size_t confidence_workspace_bytes(int B, int R_max, int V, int dtype);
+
+cudaError_t launch_confidence(const void* logits, int dtype, int B, int R_src, int V,
+                              int64_t row_stride, int64_t batch_stride, int R_max,
+                              const int32_t* row_idx, const int32_t* count,
+                              const int32_t* out_idx, int out_cols, float* conf_out,
+                              int32_t* argmax_out, float* margin_out, void* ws,
+                              int32_t* dev_status, cudaStream_t stream);
+
+cudaError_t launch_kv_scatter(void* k_cache, void* v_cache, const void* k_new,
+                              const void* v_new, int dtype, int B, int L, int H, int d,
+                              int M_max, const int32_t* idx, const int32_t* count,
+                              int32_t* dev_status, cudaStream_t stream);
+
+size_t attention_workspace_bytes(int B, int L, int H, int d, int M_max, int dtype);
+
+cudaError_t launch_attention_simt(const void* q, const void* k, const void* v, int dtype,
+                                  int B, int L, int H, int d, int M_max, const int32_t* count,
+                                  float scale, void* o, float* lse, int32_t* dev_status,
+                                  cudaStream_t stream);
+
+cudaError_t launch_colsum_simt(const void* q, const void* k, int dtype, int B, int L, int H,
+                               int d, int M_max, const int32_t* count, float scale,
+                               const float* lse, float* colsum, int32_t* dev_status,
+                               cudaStream_t stream);
+
+cudaError_t launch_stable_prefix(const float* score, int B, int L, int32_t* start, float tau,
+                                 int min_commit, int advance_start, int32_t* len_out,
+                                 int32_t* dev_status, cudaStream_t stream);
+
+int num_sms();
+
+}  // namespace dllm

@@ -1,0 +1,94 @@
+"""The C-ABI library loads and exports what include/dllm.h declares.
+
+No GPU needed: only host-side entry points run (version, workspace queries and
+argument validation, which returns before any CUDA call).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    with open(os.path.join(ROOT, "include", "dllm.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dllm_[a-z_0-9]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from partial_attention_saliency_b300 import build
+    path = build.build_library()
+    from partial_attention_saliency_b300 import _lib
+    return _lib.load_library(path)
+
+
+def test_header_declares_the_five_entry_points():
+    names = _declared_functions()
+    for n in ("dllm_saliency_select", "dllm_confidence", "dllm_kv_scatter",
+              "dllm_partial_attention", "dllm_stable_prefix"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    from partial_attention_saliency_b300 import _lib
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, f"binding lacks {name}"
+    assert set(_lib.SIGNATURES) <= set(_declared_functions())
+
+
+def test_version_and_no_error(lib):
+    assert lib.dllm_version().decode().startswith("dllm ")
+    assert "sm_103a" in lib.dllm_version().decode()
+
+
+def test_workspace_queries_host_only(lib):
+    assert lib.dllm_confidence_workspace_bytes(1, 512, 126464, 1) > 0
+    assert lib.dllm_confidence_workspace_bytes(0, 512, 126464, 1) == 0
+    assert lib.dllm_confidence_workspace_bytes(1, 512, 126464, 7) == 0
+    # grows with rows
+    a = lib.dllm_confidence_workspace_bytes(1, 100, 126464, 1)
+    b = lib.dllm_confidence_workspace_bytes(2, 100, 126464, 1)
+    assert b == 2 * a
+
+
+def test_invalid_arguments_rejected_before_launch(lib):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    st = lib.dllm_saliency_select(None, p, 1, 1, 8, 8, 8, 64, None, 0.99, 0, p, p, p, None, None)
+    assert st == 1 and b"NULL" in lib.dllm_last_error()
+    st = lib.dllm_saliency_select(p, p, 1, 1, 8, 8, 4, 64, None, 0.99, 0, p, p, p, None, None)
+    assert st == 1 and b"row_stride" in lib.dllm_last_error()
+    st = lib.dllm_saliency_select(p, p, 9, 1, 8, 8, 8, 64, None, 0.99, 0, p, p, p, None, None)
+    assert st == 1 and b"dtype" in lib.dllm_last_error()
+    st = lib.dllm_confidence(p, 1, 1, 4, 1, 1, 4, 4, None, None, None, 4, p, p, None, p, 1 << 20,
+                             None, None)
+    assert st == 1 and b"V=1" in lib.dllm_last_error()
+    st = lib.dllm_confidence(p, 1, 1, 4, 64, 64, 256, 4, None, None, None, 4, p, p, None, p, 0,
+                             None, None)
+    assert st == 1 and b"workspace" in lib.dllm_last_error()
+    st = lib.dllm_partial_attention(p, p, p, 1, 1, 16, 2, 48, 8, p, 0.0, p, p, None, None, 0,
+                                    None, None)
+    assert st == 2 and b"head dim" in lib.dllm_last_error()
+    st = lib.dllm_partial_attention(p, p, p, 1, 1, 16, 2, 128, 8, p, 0.0, p, None, p, None, 0,
+                                    None, None)
+    assert st == 1 and b"lse" in lib.dllm_last_error()
+    st = lib.dllm_kv_scatter(p, p, p, None, 1, 1, 16, 2, 128, 8, p, p, None, None)
+    assert st == 1
+    st = lib.dllm_stable_prefix(p, 0, 16, p, 0.9, 1, 0, p, None, None)
+    assert st == 1
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    from partial_attention_saliency_b300 import _lib
+    with pytest.raises(ImportError):
+        saved = _lib._LIB
+        _lib._LIB = None
+        try:
+            _lib.load_library(str(tmp_path / "missing.so"))
+        finally:
+            _lib._LIB = saved
