@@ -139,6 +139,45 @@ dllm_status dllm_confidence(const void* logits, int dtype, int B, int R_src,
                             int32_t* dev_status, void* stream);
 
 /*
+ * dllm_confidence_static_ws -- dllm_confidence for callers that cannot
+ * allocate device memory.
+ *
+ * The pages have no counterpart to this entry point: it exists for callers
+ * that only receive their input and output buffers (for instance a plugin
+ * that a host framework hands raw device pointers, with no allocator of its
+ * own) and for latency-critical callers that cannot afford cudaMalloc, which
+ * may synchronise the whole device.  Instead of a caller workspace it uses a
+ * scratch array of DLLM_CONFIDENCE_STATIC_WS_BYTES bytes that the library
+ * defines in device memory; every GPU that loads the library holds that array
+ * until the process exits.
+ *
+ * Arguments, outputs and device-side checks are those of dllm_confidence,
+ * minus ws/ws_bytes.  Rejects (DLLM_ERR_INVALID_ARG, nothing launched) any
+ * shape whose scratch need, dllm_confidence_workspace_bytes(B, R_max, V,
+ * dtype), exceeds DLLM_CONFIDENCE_STATIC_WS_BYTES.  Allocates nothing: no
+ * cudaMalloc, no cudaFree, no allocating library routine.
+ *
+ * The first call on a device (made with that device current) looks up the
+ * array's device address once; make that first call before any stream
+ * capture.  All calls on a device share the one array and it keeps the last
+ * call's contents: calls whose kernels overlap on the GPU (e.g. on two
+ * streams without ordering between them) race on it and must be serialised
+ * by the caller.  Nothing in it needs to start at zero: each call writes
+ * every partial result it later reads.
+ */
+#define DLLM_CONFIDENCE_STATIC_WS_BYTES ((size_t)4 << 20) /* 4 MiB */
+
+dllm_status dllm_confidence_static_ws(const void* logits, int dtype, int B,
+                                      int R_src, int V, int64_t row_stride,
+                                      int64_t batch_stride, int R_max,
+                                      const int32_t* row_idx,
+                                      const int32_t* count,
+                                      const int32_t* out_idx, int out_cols,
+                                      float* conf_out, int32_t* argmax_out,
+                                      float* margin_out, int32_t* dev_status,
+                                      void* stream);
+
+/*
  * dllm_kv_scatter -- write the fresh K/V rows of the active positions into
  * the full-sequence cache.
  *

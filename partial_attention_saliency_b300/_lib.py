@@ -36,6 +36,8 @@ SIGNATURES = {
     "dllm_confidence_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "dllm_confidence": (_I, [_P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P,
                              _P, _SZ, _P, _P]),
+    "dllm_confidence_static_ws": (_I, [_P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _P,
+                                       _P, _P, _P, _P]),
     "dllm_kv_scatter": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P]),
     "dllm_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "dllm_partial_attention": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P,

@@ -187,4 +187,9 @@ dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start,
 
 namespace dllm {
 size_t attention_workspace_bytes(int, int, int, int, int, int) { return 0; }
+
+int set_last_error(int code, const char* message) {
+  g_last_error = message;
+  return code;
+}
 }  // namespace dllm

@@ -46,4 +46,7 @@ cudaError_t launch_stable_prefix(const float* score, int B, int L, int32_t* star
 
 int num_sms();
 
+// Records `message` as the thread's dllm_last_error() text and returns `code`.
+int set_last_error(int code, const char* message);
+
 }  // namespace dllm
