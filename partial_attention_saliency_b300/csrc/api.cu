@@ -161,6 +161,18 @@ dllm_status dllm_partial_attention(const void* q, const void* k_cache, const voi
           "dllm_partial_attention: workspace %zu bytes < %zu required", ws_bytes, need);
   if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)d);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dllm::attention_tc_supported(dtype, d, q, k_cache, v_cache, o_out) &&
+      (colsum_out == nullptr || lse_out != nullptr)) {
+    float* lse = lse_out;
+    if (lse == nullptr) {  // the tensor-core epilogue can skip the lse
+      return from_cuda(dllm::launch_attention_tc(q, k_cache, v_cache, B, L, H, M_max, count,
+                                                 scale, o_out, nullptr, nullptr, dev_status, s),
+                       "dllm_partial_attention launch");
+    }
+    return from_cuda(dllm::launch_attention_tc(q, k_cache, v_cache, B, L, H, M_max, count, scale,
+                                               o_out, lse, colsum_out, dev_status, s),
+                     "dllm_partial_attention launch");
+  }
   cudaError_t e = dllm::launch_attention_simt(q, k_cache, v_cache, dtype, B, L, H, d, M_max,
                                               count, scale, o_out, lse_out, dev_status, s);
   if (e != cudaSuccess) return from_cuda(e, "dllm_partial_attention launch");

@@ -35,6 +35,13 @@ cudaError_t launch_attention_simt(const void* q, const void* k, const void* v, i
                                   float scale, void* o, float* lse, int32_t* dev_status,
                                   cudaStream_t stream);
 
+bool attention_tc_supported(int dtype, int d, const void* q, const void* k, const void* v,
+                            const void* o);
+
+cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int B, int L, int H,
+                                int M_max, const int32_t* count, float scale, void* o, float* lse,
+                                float* colsum, int32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_colsum_simt(const void* q, const void* k, int dtype, int B, int L, int H,
                                int d, int M_max, const int32_t* count, float scale,
                                const float* lse, float* colsum, int32_t* dev_status,
