@@ -42,7 +42,7 @@ N_SETS = 4  # rotating input sets: 4 x ~175 MB keeps every step's inputs out of 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -90,7 +90,7 @@ class ClockSampler:
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
             self.ok = True
         except Exception as e:  # noqa: BLE001
-            self.err = repr(e)
+            self.err = repr(e)[:200]
         self._stop = threading.Event()
         self._t = None
 
@@ -118,7 +118,8 @@ class ClockSampler:
     def summary(self):
         if not self.ok or not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "samples": 0, "source": "nvml unavailable" if not self.ok else "nvml"}
+                    "samples": 0, "source": "nvml unavailable" if not self.ok else "nvml",
+                    "error": getattr(self, "err", None)}
         mhz = [m for m, _ in self.samples]
         seen = 0
         for _, r in self.samples:
@@ -314,24 +315,36 @@ def main():
     assert int(step.dev_status[0]) == 0, "device-side check failed"
 
     # ---------------------------------------------------------------- device-timed
-    for i in range(args.warmup):
-        run_step(dl, step, sets[i % N_SETS], stream)
+    # W warm-up steps and the K timed steps are each captured as one CUDA graph
+    # (no host launch gaps inside the timed region); external timing events
+    # between the entry points of every timed step give the per-kernel times.
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    cap = torch.cuda.Stream(device)
+    g_warm = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_warm, stream=cap):
+        for i in range(args.warmup):
+            run_step(dl, step, sets[i % N_SETS], torch.cuda.current_stream())
+    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
+          for _ in range(K)]
+    g_timed = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_timed, stream=cap):
+        for i in range(K):
+            run_step(dl, step, sets[i % N_SETS], torch.cuda.current_stream(), ev[i])
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
+    g_warm.replay()
     torch.cuda.synchronize()
     if pg: pg.barrier()
     torch.cuda.synchronize()
     clocks.start()
     t_start.record(stream)
-    for i in range(K):
-        run_step(dl, step, sets[i % N_SETS], stream, ev[i])
+    g_timed.replay()
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.stop()
     if pg: pg.barrier()
+    assert int(step.dev_status[0]) == 0, "device-side check failed"
     elapsed_ms = t_start.elapsed_time(t_end)
     per_entry = {n: 0.0 for n in ENTRY_ORDER}
     for i in range(K):
@@ -383,7 +396,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": workload_desc(s, sum(counts_per_set[0])),
             "roofline": roof, "kernels": kernels, "clocks": clocks.summary(),
-            "gpu_launches": LAUNCHES_PER_STEP * K, "e2e": e2e}
+            "gpu_launches": LAUNCHES_PER_STEP * K, "timing": "K steps replayed as one CUDA graph", "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cb, _, _ = cpu_baseline(s, args.cpu_seconds)
         cb.pop("s_per_step", None)
