@@ -242,7 +242,7 @@ def dllm_partial_attention(q, k_cache, v_cache, count, *, scale: float = 0.0, o_
     if colsum_out is not None:
         _need(colsum_out, torch.float32, (B, H, L), "colsum_out")
     need = int(lib.dllm_attention_workspace_bytes(B, L, H, d, M_max, dt))
-    if ws is None and need > 0:
+    if ws is None and need > 0:  # the workspace is optional: without it no key-range split
         ws = torch.empty((need,), dtype=torch.uint8, device=dev)
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib.dllm_partial_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), dt, B, L, H, d,

@@ -5,7 +5,10 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
+#include <set>
 #include <string>
+#include <utility>
 
 #include "dllm.h"
 #include "internal.h"
@@ -24,6 +27,19 @@ int num_sms() {
     cached_dev = dev;
   }
   return cached_sms;
+}
+
+cudaError_t ensure_smem_limit(const void* func, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({func, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({func, dev});
+  return e;
 }
 
 }  // namespace dllm
@@ -156,21 +172,14 @@ dllm_status dllm_partial_attention(const void* q, const void* k_cache, const voi
           "dllm_partial_attention: colsum_out needs lse_out");
   if (d != 32 && d != 64 && d != 128)
     return fail(DLLM_ERR_UNSUPPORTED, "dllm_partial_attention: head dim %d not in {32,64,128}", d);
-  const size_t need = dllm::attention_workspace_bytes(B, L, H, d, M_max, dtype);
-  REQUIRE(ws_bytes >= need && (need == 0 || ws != nullptr),
-          "dllm_partial_attention: workspace %zu bytes < %zu required", ws_bytes, need);
+  if (ws_bytes > 0 && ws == nullptr)
+    return fail(DLLM_ERR_INVALID_ARG, "dllm_partial_attention: ws_bytes > 0 with a NULL workspace");
   if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)d);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dllm::attention_tc_supported(dtype, d, q, k_cache, v_cache, o_out) &&
-      (colsum_out == nullptr || lse_out != nullptr)) {
-    float* lse = lse_out;
-    if (lse == nullptr) {  // the tensor-core epilogue can skip the lse
-      return from_cuda(dllm::launch_attention_tc(q, k_cache, v_cache, B, L, H, M_max, count,
-                                                 scale, o_out, nullptr, nullptr, dev_status, s),
-                       "dllm_partial_attention launch");
-    }
+  if (dllm::attention_tc_supported(dtype, d, q, k_cache, v_cache, o_out)) {
     return from_cuda(dllm::launch_attention_tc(q, k_cache, v_cache, B, L, H, M_max, count, scale,
-                                               o_out, lse, colsum_out, dev_status, s),
+                                               o_out, lse_out, colsum_out, ws, ws_bytes,
+                                               dev_status, s),
                      "dllm_partial_attention launch");
   }
   cudaError_t e = dllm::launch_attention_simt(q, k_cache, v_cache, dtype, B, L, H, d, M_max,
@@ -198,7 +207,10 @@ dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start,
 }  // extern "C"
 
 namespace dllm {
-size_t attention_workspace_bytes(int, int, int, int, int, int) { return 0; }
+size_t attention_workspace_bytes(int, int, int, int d, int, int dtype) {
+  // only the tensor-core path uses a workspace (key-range split partials)
+  return (dtype == DLLM_BF16 && d == 128) ? attention_tc_workspace_bytes(num_sms()) : 0;
+}
 
 int set_last_error(int code, const char* message) {
   g_last_error = message;

@@ -7,7 +7,10 @@
 // cost O(M N d).  Attn-Sampler, technical summary, Methodology 2: column sums
 // of the attention matrix, computed block by block without materialising it.
 //
-// attn_fwd_tc_kernel -- one CTA per (128 active query rows, head, batch row):
+// attn_fwd_tc_kernel -- persistent, one CTA per SM; work items are (128 active
+//   query rows, head, batch row), each optionally limited to a slice of the
+//   key range when there are fewer query tiles than SMs (attn_split_merge_kernel
+//   then combines the slices):
 //   warp 0     TMA producer: the Q tile once, then K/V tiles of 128 keys into
 //              a two-stage ring (128-byte swizzle, 16 KB boxes of 64 dims).
 //   warp 1     one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
@@ -52,7 +55,10 @@ struct FwdParams {
   const int32_t* count;
   __nv_bfloat16* o;
   float* lse;
-  int L, H, M_max;
+  float* ws_o;   // split partials: [item][128 rows][128 dims] unnormalised O
+  float* ws_ml;  // split partials: [item][128 rows][2] = (running max (log2 units), sum)
+  int B, L, H, M_max;
+  int max_split_items;  // capacity of the workspace in items (0: never split)
   float scale_log2;
   int32_t* dev_status;
 };
@@ -104,18 +110,71 @@ __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+// Work plan shared by the forward and merge kernels, computed on the device
+// from the active counts: query tiles of 128 active rows per (batch, head);
+// when there are fewer tiles than CTAs the key range of each tile is split
+// so that every SM gets work.
+struct FwdPlan {
+  int total_qt;  // query tiles over all (b, h)
+  int nsplit;    // key-range splits per query tile
+  int tps;       // key tiles per split
+  int nkt;       // key tiles of the sequence
+};
+
+__device__ __forceinline__ int clamp_count(const int32_t* count, int b, int M_max) {
+  const int n = count[b];
+  return n < 0 ? 0 : (n > M_max ? M_max : n);
+}
+
+__device__ FwdPlan make_plan(const FwdParams& p, int n_ctas) {
+  FwdPlan pl;
+  pl.nkt = (p.L + kBN - 1) / kBN;
+  int qt = 0;
+  for (int b = 0; b < p.B; ++b) qt += p.H * ((clamp_count(p.count, b, p.M_max) + kBM - 1) / kBM);
+  pl.total_qt = qt;
+  int ns = 1;
+  if (qt > 0 && qt < n_ctas && p.max_split_items > 0) {
+    ns = (n_ctas + qt - 1) / qt;
+    const int max_by_tiles = pl.nkt / 2 > 1 ? pl.nkt / 2 : 1;  // at least two key tiles each
+    ns = ns < max_by_tiles ? ns : max_by_tiles;
+    const int max_by_ws = p.max_split_items / qt;
+    ns = ns < max_by_ws ? ns : max_by_ws;
+    if (ns < 1) ns = 1;
+  }
+  pl.tps = (pl.nkt + ns - 1) / ns;
+  pl.nsplit = (pl.nkt + pl.tps - 1) / pl.tps;  // no empty split
+  return pl;
+}
+
+// Query tile index qi -> (b, h, tile) in batch-major, head-major order.
+__device__ __forceinline__ void decode_qtile(const FwdParams& p, int qi, int* b, int* h, int* t) {
+  for (int bb = 0; bb < p.B; ++bb) {
+    const int per_head = (clamp_count(p.count, bb, p.M_max) + kBM - 1) / kBM;
+    const int n = per_head * p.H;
+    if (qi < n) {
+      *b = bb;
+      *h = qi / per_head;
+      *t = qi - *h * per_head;
+      return;
+    }
+    qi -= n;
+  }
+  *b = *h = *t = 0;
+}
+
+// Persistent forward kernel: one CTA per SM walks the work items (query tile,
+// key-range split) round-robin; the TMA, MMA and softmax roles keep their
+// pipeline phases across items.
 __global__ void __launch_bounds__(kThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, FwdParams p) {
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  int n = p.count[b];
-  if (n < 0 || n > p.M_max) {
-    if (qt == 0 && h == 0 && threadIdx.x == 0) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
-    n = n < 0 ? 0 : p.M_max;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int b = 0; b < p.B; ++b)
+      if (p.count[b] < 0 || p.count[b] > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
   }
-  const int row0 = qt * kBM;
-  if (row0 >= n) return;
-  const int nkt = (p.L + kBN - 1) / kBN;
+  const FwdPlan plan = make_plan(p, gridDim.x);
+  const int n_items = plan.total_qt * plan.nsplit;
+  if ((int)blockIdx.x >= n_items) return;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -124,19 +183,22 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   const uint32_t sQ = base + kFwdQ, sP = base + kFwdP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kFwdBar);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [kStages]
-  uint64_t* kv_empty = bars + 3;  // [kStages]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_free = bars + 7;    // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_ready = bars + 10;
-  uint64_t* mma_done = bars + 11;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-  int* abort_flag = reinterpret_cast<int*>(bars + 13);
+  uint64_t* q_empty = bars + 1;
+  uint64_t* kv_full = bars + 2;   // [kStages]
+  uint64_t* kv_empty = bars + 4;  // [kStages]
+  uint64_t* s_full = bars + 6;    // [2]
+  uint64_t* s_free = bars + 8;    // [2]
+  uint64_t* p_full = bars + 10;
+  uint64_t* o_ready = bars + 11;
+  uint64_t* o_free = bars + 12;
+  uint64_t* mma_done = bars + 13;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  int* abort_flag = reinterpret_cast<int*>(bars + 15);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
@@ -147,6 +209,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
     mbar_init(p_full, 4);
     mbar_init(o_ready, 1);
+    mbar_init(o_free, 4);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -159,42 +222,54 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   volatile int* abort = abort_flag;
 
   if (warp == 0) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      mbar_expect_tx(q_full, kTile);
-      tma_load_4d(gbase + kFwdQ, &tq, q_full, 0, h, row0, b);
-      tma_load_4d(gbase + kFwdQ + kBox, &tq, q_full, 64, h, row0, b);
-      int issued = 0;
-      for (int it = 0; it < nkt; ++it) {
-        const int s = it % kStages;
-        if (it >= kStages && !mbar_wait(&kv_empty[s], ((it / kStages) - 1) & 1, abort)) break;
-        uint8_t* kdst = gbase + kFwdK + s * 2 * kTile;
-        uint8_t* vdst = kdst + kTile;
-        const int key0 = it * kBN;
-        mbar_expect_tx(&kv_full[s], 2 * kTile);
-        tma_load_4d(kdst, &tk, &kv_full[s], 0, h, key0, b);
-        tma_load_4d(kdst + kBox, &tk, &kv_full[s], 64, h, key0, b);
-        tma_load_4d(vdst, &tv, &kv_full[s], 0, h, key0, b);
-        tma_load_4d(vdst + kBox, &tv, &kv_full[s], 64, h, key0, b);
-        issued = it + 1;
+      int j = 0, g = 0;
+      bool ok = true;
+      for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
+        int b, h, qt;
+        decode_qtile(p, v / plan.nsplit, &b, &h, &qt);
+        const int split = v % plan.nsplit;
+        const int kt0 = split * plan.tps;
+        const int nt = min(plan.tps, plan.nkt - kt0);
+        if (j > 0 && !mbar_wait(q_empty, (j - 1) & 1, abort)) break;
+        mbar_expect_tx(q_full, kTile);
+        tma_load_4d(gbase + kFwdQ, &tq, q_full, 0, h, qt * kBM, b);
+        tma_load_4d(gbase + kFwdQ + kBox, &tq, q_full, 64, h, qt * kBM, b);
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int s = g % kStages;
+          if (g >= kStages && !mbar_wait(&kv_empty[s], ((g / kStages) - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* kdst = gbase + kFwdK + s * 2 * kTile;
+          uint8_t* vdst = kdst + kTile;
+          const int key0 = (kt0 + t) * kBN;
+          mbar_expect_tx(&kv_full[s], 2 * kTile);
+          tma_load_4d(kdst, &tk, &kv_full[s], 0, h, key0, b);
+          tma_load_4d(kdst + kBox, &tk, &kv_full[s], 64, h, key0, b);
+          tma_load_4d(vdst, &tv, &kv_full[s], 0, h, key0, b);
+          tma_load_4d(vdst + kBox, &tv, &kv_full[s], 64, h, key0, b);
+        }
       }
       // Drain: never leave with copies in flight into this CTA's shared memory.
       int none = 0;
-      mbar_wait(q_full, 0, &none);
-      for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
-        mbar_wait(&kv_full[it % kStages], (it / kStages) & 1, &none);
+      if (j > 0) mbar_wait(q_full, (j - 1) & 1, &none);
+      for (int k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
+        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &none);
     }
   } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       const uint32_t id_pv = idesc_bf16_f32(kBM, kHD, false, true);
-      bool ok = mbar_wait(q_full, 0, abort);
-      auto issue_qk = [&](int it) -> bool {
-        const int s = it % kStages, sb = it & 1;
-        if (!mbar_wait(&kv_full[s], (it / kStages) & 1, abort)) return false;
-        if (it >= 2 && !mbar_wait(&s_free[sb], ((it >> 1) - 1) & 1, abort)) return false;
+      auto issue_qk = [&](int g) -> bool {
+        const int s = g % kStages, sb = g & 1;
+        if (!mbar_wait(&kv_full[s], (g / kStages) & 1, abort)) return false;
+        if (g >= 2 && !mbar_wait(&s_free[sb], ((g >> 1) - 1) & 1, abort)) return false;
         tc_fence_after();
         const uint32_t sK = base + kFwdK + s * 2 * kTile;
 #pragma unroll
@@ -206,22 +281,46 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         mma_commit(&s_full[sb]);
         return true;
       };
-      if (ok) ok = issue_qk(0);
-      for (int it = 0; ok && it < nkt; ++it) {
-        if (it + 1 < nkt && !issue_qk(it + 1)) break;
-        if (!mbar_wait(p_full, it & 1, abort)) break;
-        tc_fence_after();
-        const int s = it % kStages;
-        const uint32_t sV = base + kFwdK + s * 2 * kTile + kTile;
+      int j = 0, g = 0;
+      bool ok = true;
+      for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
+        const int split = v % plan.nsplit;
+        const int nt = min(plan.tps, plan.nkt - split * plan.tps);
+        if (!mbar_wait(q_full, j & 1, abort)) break;
+        const int g0 = g;
+        if (!issue_qk(g0)) break;
+        for (int t = 0; t < nt; ++t) {
+          const int gg = g0 + t;
+          if (t + 1 < nt) {
+            if (!issue_qk(gg + 1)) {
+              ok = false;
+              break;
+            }
+          } else {
+            mma_commit(q_empty);  // the last QK^T of the item is issued: Q may be replaced
+          }
+          if (!mbar_wait(p_full, gg & 1, abort)) {
+            ok = false;
+            break;
+          }
+          if (t == 0 && j > 0 && !mbar_wait(o_free, (j - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int s = gg % kStages;
+          const uint32_t sV = base + kFwdK + s * 2 * kTile + kTile;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + 2 * kBN, smem_desc_sw128(sP + aoff, 16, 1024),
-                      smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), id_pv,
-                      (it > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kBN / 16; ++kk) {
+            const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_bf16_ss(tmem + 2 * kBN, smem_desc_sw128(sP + aoff, 16, 1024),
+                        smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), id_pv,
+                        (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(o_ready);
+          mma_commit(&kv_empty[s]);
         }
-        mma_commit(o_ready);
-        mma_commit(&kv_empty[s]);
+        g = g0 + nt;
       }
       // Every MMA issued above completes before the tensor memory is freed.
       mma_commit(mma_done);
@@ -229,111 +328,144 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_wait(mma_done, 0, &none);
     }
   } else {
-    // ---------------------------------------------------------- softmax warps
+    // ------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY, l = 0.f;
+    int j = 0, g = 0;
     bool ok = true;
-    for (int it = 0; it < nkt; ++it) {
-      const int sb = it & 1;
-      if (!warp_wait(&s_full[sb], (it >> 1) & 1, abort)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t raw[kBN];
+    for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
+      int b, h, qt;
+      decode_qtile(p, v / plan.nsplit, &b, &h, &qt);
+      const int split = v % plan.nsplit;
+      const int kt0 = split * plan.tps;
+      const int nt = min(plan.tps, plan.nkt - kt0);
+      float m = -INFINITY, l = 0.f;
+      for (int t = 0; t < nt; ++t) {
+        const int gg = g + t;
+        const int sb = gg & 1;
+        if (!warp_wait(&s_full[sb], (gg >> 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t raw[kBN];
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c)
-        tmem_ld_32x32b_x32(tmem + lane_base + sb * kBN + c * 32,
-                           *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld_32x32b_x32(tmem + lane_base + sb * kBN + c * 32,
+                             *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[sb]);
 
-      const int kvalid = min(kBN, p.L - it * kBN);
-      float sv[kBN];
-      float mx = -INFINITY;
+        const int kvalid = min(kBN, p.L - (kt0 + t) * kBN);
+        float sv[kBN];
+        float mx = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < kBN; ++j) {
-        const float s = (j < kvalid) ? __uint_as_float(raw[j]) * sl2 : -INFINITY;
-        sv[j] = s;
-        mx = fmaxf(mx, s);
+        for (int jj = 0; jj < kBN; ++jj) {
+          const float sc = (jj < kvalid) ? __uint_as_float(raw[jj]) * sl2 : -INFINITY;
+          sv[jj] = sc;
+          mx = fmaxf(mx, sc);
+        }
+        const float m_new = fmaxf(m, mx);
+        const bool grow = m_new > m + kRescaleThreshold;
+        const float m_use = grow ? m_new : m;
+        // P V of the previous tile must be done: the P buffer is reused and O
+        // may be rescaled below.
+        if (t > 0 && !warp_wait(o_ready, (gg - 1) & 1, abort)) {
+          ok = false;
+          break;
+        }
+        if (grow) {
+          const float alpha = ex2_approx(m - m_use);
+          l *= alpha;
+          if (t > 0) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < kHD / 32; ++c) {
+              uint32_t ov[32];
+              tmem_ld_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
+              tmem_ld_wait();
+#pragma unroll
+              for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha);
+              tmem_st_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
+            }
+            tmem_st_wait();
+          }
+        }
+        float sum = 0.f;
+#pragma unroll
+        for (int c = 0; c < kBN / 8; ++c) {
+          float e[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            e[k] = ex2_approx(sv[c * 8 + k] - m_use);
+            sum += e[k];
+          }
+          const uint32_t addr = sP + (c >> 3) * kBox + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+          st_shared_v4(addr, pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
+                       pack_bf16(e[6], e[7]));
+        }
+        l += sum;
+        m = m_use;
+        fence_proxy_async_smem();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(p_full);
       }
-      const float m_new = fmaxf(m, mx);
-      const bool grow = m_new > m + kRescaleThreshold;
-      const float m_use = grow ? m_new : m;
-      // P V of the previous tile must be done: the P buffer is reused and O
-      // may be rescaled below.
-      if (it > 0 && !warp_wait(o_ready, (it - 1) & 1, abort)) {
+      if (!ok || !warp_wait(o_ready, (g + nt - 1) & 1, abort)) {
         ok = false;
         break;
       }
-      if (grow) {
-        const float alpha = ex2_approx(m - m_use);
-        l *= alpha;
-        if (it > 0) {
-          tc_fence_after();
-#pragma unroll 1
-          for (int c = 0; c < kHD / 32; ++c) {
-            uint32_t ov[32];
-            tmem_ld_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
-            tmem_ld_wait();
-#pragma unroll
-            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
-            tmem_st_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
-          }
-          tmem_st_wait();
-        }
-      }
-      float sum = 0.f;
-#pragma unroll
-      for (int c = 0; c < kBN / 8; ++c) {
-        float e[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          e[k] = ex2_approx(sv[c * 8 + k] - m_use);
-          sum += e[k];
-        }
-        const uint32_t addr = sP + (c >> 3) * kBox + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
-        st_shared_v4(addr, pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
-                     pack_bf16(e[6], e[7]));
-      }
-      l += sum;
-      m = m_use;
-      fence_proxy_async_smem();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
-    }
-    if (ok && warp_wait(o_ready, (nkt - 1) & 1, abort)) {
+      g += nt;
+      // ---------------------------------------------------------- epilogue
       tc_fence_after();
-      const int i = row0 + r;
-      const float inv = 1.0f / l;
+      const int n = clamp_count(p.count, b, p.M_max);
+      const int i = qt * kBM + r;
       const bool store = i < n;
-      __nv_bfloat16* orow = p.o + ((int64_t)b * p.M_max + i) * ((int64_t)p.H * kHD) + (int64_t)h * kHD;
+      const bool partial = plan.nsplit > 1;
+      const float inv = partial ? 1.0f : 1.0f / l;
+      __nv_bfloat16* orow =
+          p.o + ((int64_t)b * p.M_max + i) * ((int64_t)p.H * kHD) + (int64_t)h * kHD;
+      float* prow = p.ws_o + ((int64_t)v * kBM + r) * kHD;
 #pragma unroll 1
       for (int c = 0; c < kHD / 32; ++c) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
         tmem_ld_wait();
-        if (store) {
+        if (store && partial) {
+          float4* dst = reinterpret_cast<float4*>(prow + c * 32);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            dst[q] = make_float4(__uint_as_float(ov[q * 4 + 0]), __uint_as_float(ov[q * 4 + 1]),
+                                 __uint_as_float(ov[q * 4 + 2]), __uint_as_float(ov[q * 4 + 3]));
+        } else if (store) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
+          for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(ov[v * 8 + 0]) * inv, __uint_as_float(ov[v * 8 + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(ov[v * 8 + 2]) * inv, __uint_as_float(ov[v * 8 + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(ov[v * 8 + 4]) * inv, __uint_as_float(ov[v * 8 + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(ov[v * 8 + 6]) * inv, __uint_as_float(ov[v * 8 + 7]) * inv);
-            dst[v] = w;
+            w.x = pack_bf16(__uint_as_float(ov[q * 8 + 0]) * inv, __uint_as_float(ov[q * 8 + 1]) * inv);
+            w.y = pack_bf16(__uint_as_float(ov[q * 8 + 2]) * inv, __uint_as_float(ov[q * 8 + 3]) * inv);
+            w.z = pack_bf16(__uint_as_float(ov[q * 8 + 4]) * inv, __uint_as_float(ov[q * 8 + 5]) * inv);
+            w.w = pack_bf16(__uint_as_float(ov[q * 8 + 6]) * inv, __uint_as_float(ov[q * 8 + 7]) * inv);
+            dst[q] = w;
           }
         }
       }
-      if (store && p.lse != nullptr)
-        p.lse[((int64_t)b * p.H + h) * p.M_max + i] = (m + log2f(l)) * 0.69314718055994531f;
+      // O is read: the next item's first P V may overwrite it.
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(o_free);
+      if (store) {
+        if (partial) {
+          p.ws_ml[((int64_t)v * kBM + r) * 2 + 0] = m;
+          p.ws_ml[((int64_t)v * kBM + r) * 2 + 1] = l;
+        } else if (p.lse != nullptr) {
+          p.lse[((int64_t)b * p.H + h) * p.M_max + i] = (m + log2f(l)) * 0.69314718055994531f;
+        }
+      }
     }
   }
 
@@ -344,6 +476,70 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     tmem_dealloc(tmem, 512);
   }
   if (threadIdx.x == 0 && *abort) report(p.dev_status, DLLM_ERR_TIMEOUT);
+}
+
+// Combines the key-range splits of each active row: O = sum_s 2^(m_s - M) O_s
+// / sum_s 2^(m_s - M) l_s, lse = (M + log2 l) ln 2.  Grid-stride over the
+// active rows only (one warp per (b, row, h)); does nothing when the plan did
+// not split.
+__global__ void __launch_bounds__(256)
+attn_split_merge_kernel(FwdParams p, int n_ctas) {
+  __shared__ FwdPlan s_plan;
+  __shared__ int s_rows;  // active rows summed over batch rows
+  if (threadIdx.x == 0) {
+    s_plan = make_plan(p, n_ctas);
+    int rows = 0;
+    for (int b = 0; b < p.B; ++b) rows += clamp_count(p.count, b, p.M_max);
+    s_rows = rows;
+  }
+  __syncthreads();
+  const FwdPlan plan = s_plan;
+  if (plan.nsplit <= 1) return;
+  const int lane = threadIdx.x & 31;
+  const int64_t total = (int64_t)s_rows * p.H;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
+       w += (int64_t)gridDim.x * (blockDim.x >> 5)) {
+    int rem = (int)(w / p.H);
+    const int h = (int)(w - (int64_t)rem * p.H);
+    int b = 0, qi = 0;
+    for (; b < p.B; ++b) {
+      const int nb = clamp_count(p.count, b, p.M_max);
+      if (rem < nb) break;
+      rem -= nb;
+      qi += p.H * ((nb + kBM - 1) / kBM);
+    }
+    const int i = rem;
+    const int n = clamp_count(p.count, b, p.M_max);
+    const int per_head = (n + kBM - 1) / kBM;
+    qi += h * per_head + i / kBM;
+    const int r = i % kBM;
+    float M = -INFINITY;
+    for (int s = 0; s < plan.nsplit; ++s)
+      M = fmaxf(M, p.ws_ml[(((int64_t)qi * plan.nsplit + s) * kBM + r) * 2]);
+    float l = 0.f;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int s = 0; s < plan.nsplit; ++s) {
+      const int64_t item = (int64_t)qi * plan.nsplit + s;
+      const float ms = p.ws_ml[(item * kBM + r) * 2];
+      const float ls = p.ws_ml[(item * kBM + r) * 2 + 1];
+      const float wgt = ex2_approx(ms - M);
+      l += wgt * ls;
+      const float4 o4 = reinterpret_cast<const float4*>(p.ws_o + (item * kBM + r) * kHD)[lane];
+      acc[0] = fmaf(wgt, o4.x, acc[0]);
+      acc[1] = fmaf(wgt, o4.y, acc[1]);
+      acc[2] = fmaf(wgt, o4.z, acc[2]);
+      acc[3] = fmaf(wgt, o4.w, acc[3]);
+    }
+    const float inv = 1.0f / l;
+    __nv_bfloat16* orow =
+        p.o + ((int64_t)b * p.M_max + i) * ((int64_t)p.H * kHD) + (int64_t)h * kHD;
+    uint2 w2;
+    w2.x = pack_bf16(acc[0] * inv, acc[1] * inv);
+    w2.y = pack_bf16(acc[2] * inv, acc[3] * inv);
+    reinterpret_cast<uint2*>(orow)[lane] = w2;
+    if (lane == 0 && p.lse != nullptr)
+      p.lse[((int64_t)b * p.H + h) * p.M_max + i] = (M + log2f(l)) * 0.69314718055994531f;
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -535,28 +731,51 @@ bool attention_tc_supported(int dtype, int d, const void* q, const void* k, cons
          reinterpret_cast<uintptr_t>(o) % 16 == 0 && encode_fn() != nullptr;
 }
 
+size_t attention_tc_workspace_bytes(int n_ctas) {
+  // 2 x n_ctas split items of 128 rows: unnormalised O (128 floats) + (max, sum)
+  return (size_t)2 * n_ctas * kBM * (kHD + 2) * sizeof(float);
+}
+
 cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int B, int L, int H,
                                 int M_max, const int32_t* count, float scale, void* o, float* lse,
-                                float* colsum, int32_t* dev_status, cudaStream_t stream) {
-  static std::once_flag attr_once;
-  static cudaError_t attr_err = cudaSuccess;
-  std::call_once(attr_once, [] {
-    attr_err = cudaFuncSetAttribute(attn_fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                float* colsum, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                cudaStream_t stream) {
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_tc_kernel),
                                     (int)kFwdSmem);
-    if (attr_err == cudaSuccess)
-      attr_err = cudaFuncSetAttribute(attn_colsum_tc_kernel,
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kCsSmem);
-  });
-  if (attr_err != cudaSuccess) return attr_err;
+  if (e == cudaSuccess)
+    e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel), (int)kCsSmem);
+  if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv;
   if (!make_rows_map(&tq, q, B, M_max, H) || !make_rows_map(&tk, k, B, L, H) ||
       !make_rows_map(&tv, v, B, L, H))
     return cudaErrorInvalidValue;
-  FwdParams fp{count, static_cast<__nv_bfloat16*>(o), lse, L, H, M_max, scale * kLog2e, dev_status};
-  dim3 grid((M_max + kBM - 1) / kBM, H, B);
-  attn_fwd_tc_kernel<<<grid, kThreads, kFwdSmem, stream>>>(tq, tk, tv, fp);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || colsum == nullptr) return e;
+  const int n_ctas = num_sms();
+  const size_t need = attention_tc_workspace_bytes(n_ctas);
+  const bool can_split =
+      ws != nullptr && ws_bytes >= need && reinterpret_cast<uintptr_t>(ws) % 16 == 0;
+  FwdParams fp;
+  fp.count = count;
+  fp.o = static_cast<__nv_bfloat16*>(o);
+  fp.lse = lse;
+  fp.ws_o = can_split ? static_cast<float*>(ws) : nullptr;
+  fp.ws_ml = can_split ? static_cast<float*>(ws) + (size_t)2 * n_ctas * kBM * kHD : nullptr;
+  fp.B = B;
+  fp.L = L;
+  fp.H = H;
+  fp.M_max = M_max;
+  fp.max_split_items = can_split ? 2 * n_ctas : 0;
+  fp.scale_log2 = scale * kLog2e;
+  fp.dev_status = dev_status;
+  attn_fwd_tc_kernel<<<n_ctas, kThreads, kFwdSmem, stream>>>(tq, tk, tv, fp);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (can_split) {
+    // at most 2 * n_ctas split items of 128 rows exist: size the grid for them
+    attn_split_merge_kernel<<<2 * n_ctas, 256, 0, stream>>>(fp, n_ctas);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  if (colsum == nullptr) return cudaSuccess;
   ColsumParams cp{count, lse, colsum, L, H, M_max, scale * kLog2e, dev_status};
   dim3 cgrid((L + kBN - 1) / kBN, H, B);
   attn_colsum_tc_kernel<<<cgrid, kThreads, kCsSmem, stream>>>(tq, tk, cp);

@@ -15,12 +15,14 @@
 // thread in flight), reduces it to (max, second max, sum exp(z - max),
 // argmax) and stores that partial in the workspace; conf_merge_kernel folds
 // the partials of each row in a fixed order (deterministic) and writes the
-// outputs.
+// outputs.  Aligned rows take the streaming kernel below instead of
+// conf_partial_kernel.
 #include <climits>
 #include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace dllm {
 namespace {
@@ -35,7 +37,7 @@ struct ConfPartial {
   int arg;    // lowest index reaching m1
 };
 
-template <typename T> constexpr int vec_elems() { return 16 / (int)sizeof(T); }
+template <typename T> __host__ __device__ constexpr int vec_elems() { return 16 / (int)sizeof(T); }
 
 template <typename T> __host__ __device__ inline int conf_chunk_elems() {
   return kConfThreads * kConfU * vec_elems<T>();
@@ -305,6 +307,241 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* __
   }
 }
 
+// ---------------------------------------------------------------------------
+// Streaming variant (rows 16-byte aligned, V * sizeof(T) a multiple of 16):
+// one persistent CTA per SM.  A producer warp copies 64 KB row chunks with
+// cp.async.bulk into a 3-stage shared-memory ring (up to 192 KB of HBM reads
+// in flight per SM).  Each of the 8 consumer warps reduces its own 8 KB slice
+// of every staged chunk (128 elements per lane) with warp shuffles only, no
+// block barrier, and writes one ConfPartial per slice; the merge kernel folds
+// the 8 slices x chunks of a row.  The exponentials run on packed f32x2
+// FMA/add with MUFU ex2.  Work items are (row, chunk) pairs dealt round-robin
+// to the CTAs.
+constexpr int kStreamWarps = 8;                          // consumer warps
+constexpr int kStreamThreads = (kStreamWarps + 1) * 32;
+constexpr int kStreamStages = 3;
+constexpr uint32_t kStreamChunkBytes = 65536;
+constexpr uint32_t kStreamSliceBytes = kStreamChunkBytes / kStreamWarps;  // 8 KB per warp
+constexpr int kStreamVPL = kStreamSliceBytes / 16 / 32;                   // 16-byte vectors per lane
+constexpr uint32_t kStreamSmem = kStreamStages * kStreamChunkBytes + 256 + 1024;
+
+__host__ __device__ inline int stream_nchunks(int V, int elem_bytes) {
+  const int64_t bytes = (int64_t)V * elem_bytes;
+  const int n = (int)((bytes + kStreamChunkBytes - 1) / kStreamChunkBytes);
+  return n < 1 ? 1 : n;
+}
+
+__device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
+  uint4 r;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "r"(addr));
+  return r;
+}
+
+struct Top2Sum {
+  float m1, m2, l;
+};
+
+__device__ __forceinline__ Top2Sum merge_t2s(const Top2Sum& a, const Top2Sum& b) {
+  Top2Sum r;
+  r.m1 = fmaxf(a.m1, b.m1);
+  r.m2 = fmaxf(fminf(a.m1, b.m1), fmaxf(a.m2, b.m2));
+  if (r.m1 == -INFINITY) {
+    r.l = 0.f;
+  } else {
+    r.l = a.l * ex2_approx((a.m1 - r.m1) * kLog2e) + b.l * ex2_approx((b.m1 - r.m1) * kLog2e);
+  }
+  return r;
+}
+
+// Lane-local top-2 and sum of exp(z - own max) over the lane's vectors.
+template <typename T>
+__device__ __forceinline__ Top2Sum lane_reduce(const uint4 (&x)[kStreamVPL]) {
+  constexpr int E = vec_elems<T>();
+  Top2Sum t;
+  if constexpr (std::is_same<T, float>::value) {
+    t.m1 = -INFINITY;
+    t.m2 = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < kStreamVPL; ++u)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float z = elem_of<T>(x[u], e);
+        t.m2 = fmaxf(t.m2, fminf(t.m1, z));
+        t.m1 = fmaxf(t.m1, z);
+      }
+    float lacc[4] = {0.f, 0.f, 0.f, 0.f};
+    if (t.m1 != -INFINITY) {
+      const float neg = -t.m1 * kLog2e;
+#pragma unroll
+      for (int u = 0; u < kStreamVPL; ++u)
+#pragma unroll
+        for (int e = 0; e < E; ++e)
+          lacc[e & 3] += ex2_approx(fmaf(elem_of<T>(x[u], e), kLog2e, neg));
+    }
+    t.l = (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
+  } else {
+    // packed bf16x2 (max, second) in four independent chains
+    const __nv_bfloat162 ninf =
+        __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
+    __nv_bfloat162 m1[4] = {ninf, ninf, ninf, ninf}, m2[4] = {ninf, ninf, ninf, ninf};
+#pragma unroll
+    for (int u = 0; u < kStreamVPL; ++u) {
+      const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+        m2[k] = __hmax2(m2[k], __hmin2(m1[k], z));
+        m1[k] = __hmax2(m1[k], z);
+      }
+    }
+#pragma unroll
+    for (int k = 1; k < 4; ++k) {
+      m2[0] = __hmax2(__hmax2(m2[0], m2[k]), __hmin2(m1[0], m1[k]));
+      m1[0] = __hmax2(m1[0], m1[k]);
+    }
+    const float a = __bfloat162float(m1[0].x), c = __bfloat162float(m1[0].y);
+    t.m1 = fmaxf(a, c);
+    t.m2 = fmaxf(fminf(a, c), fmaxf(__bfloat162float(m2[0].x), __bfloat162float(m2[0].y)));
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    if (t.m1 != -INFINITY) {
+      const float2 l2e = make_float2(kLog2e, kLog2e);
+      const float2 neg = make_float2(-t.m1 * kLog2e, -t.m1 * kLog2e);
+#pragma unroll
+      for (int u = 0; u < kStreamVPL; ++u) {
+        const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const float2 z = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
+          const float2 arg = __ffma2_rn(z, l2e, neg);
+          const float2 e = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+          if (k & 1)
+            acc1 = __fadd2_rn(acc1, e);
+          else
+            acc0 = __fadd2_rn(acc0, e);
+        }
+      }
+    }
+    t.l = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+  }
+  return t;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(kStreamThreads, 1)
+conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, int64_t bs,
+                   int B, int R_max, const int32_t* __restrict__ row_idx,
+                   const int32_t* __restrict__ count, int nchunks,
+                   ConfPartial* __restrict__ ws, int32_t* dev_status) {
+  using namespace sm100;
+  constexpr int E = vec_elems<T>();
+  constexpr int CE = kStreamChunkBytes / sizeof(T);  // elements per chunk
+  constexpr int SE = kStreamSliceBytes / sizeof(T);  // elements per warp slice
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_addr);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gbase + kStreamStages * kStreamChunkBytes);
+  uint64_t* empty = full + kStreamStages;
+  int* abort_flag = reinterpret_cast<int*>(empty + kStreamStages);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) {
+    for (int s = 0; s < kStreamStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kStreamWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  volatile int* abort = abort_flag;
+  const int total = B * R_max * nchunks;  // < 2^31 (checked on the host)
+
+  if (warp == kStreamWarps) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int j = 0;
+      for (int v = blockIdx.x; v < total; v += gridDim.x) {
+        const int br = v / nchunks, c = v - br * nchunks;
+        const int b = br / R_max, r = br - b * R_max;
+        int row;
+        bool bad;
+        if (!row_valid(b, r, R_max, R_src, row_idx, count, &row, &bad)) continue;
+        const int stage = j % kStreamStages;
+        if (j >= kStreamStages &&
+            !mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort))
+          break;
+        const int e0 = c * CE;
+        const uint32_t bytes = (uint32_t)min(CE, V - e0) * (uint32_t)sizeof(T);
+        mbar_expect_tx(&full[stage], bytes);
+        bulk_load(gbase + stage * kStreamChunkBytes,
+                  logits + (int64_t)b * bs + (int64_t)row * rs + e0, bytes, &full[stage]);
+        ++j;
+      }
+      int none = 0;  // never leave with copies in flight into shared memory
+      for (int k = j - kStreamStages < 0 ? 0 : j - kStreamStages; k < j; ++k)
+        mbar_wait(&full[k % kStreamStages], (k / kStreamStages) & 1, &none);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const uint32_t sent = std::is_same<T, float>::value ? 0xff800000u : 0xff80ff80u;
+  int j = 0;
+  for (int v = blockIdx.x; v < total; v += gridDim.x) {
+    const int br = v / nchunks, c = v - br * nchunks;
+    const int b = br / R_max, r = br - b * R_max;
+    int row;
+    bool bad;
+    if (!row_valid(b, r, R_max, R_src, row_idx, count, &row, &bad)) continue;
+    const int stage = j % kStreamStages;
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStreamStages) & 1, abort));
+    const int s0 = c * CE + warp * SE;  // first element of this warp's slice
+    const int nvec = ok ? max(0, min(SE, V - s0)) / E : 0;
+    const uint32_t sbase = base + stage * kStreamChunkBytes + warp * kStreamSliceBytes;
+    uint4 x[kStreamVPL];
+#pragma unroll
+    for (int u = 0; u < kStreamVPL; ++u) {
+      const int vi = u * 32 + lane;
+      x[u] = vi < nvec ? ld_shared16(sbase + vi * 16) : make_uint4(sent, sent, sent, sent);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[stage]);  // this warp's slice is in registers
+    Top2Sum t = lane_reduce<T>(x);
+    const float own_max = t.m1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      Top2Sum q;
+      q.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
+      q.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
+      q.l = __shfl_xor_sync(0xffffffffu, t.l, o);
+      t = merge_t2s(t, q);
+    }
+    int arg = INT_MAX;
+    if (own_max == t.m1 && own_max != -INFINITY) {
+      // the reverse scan leaves the lowest index (u, then e, ascend with it)
+#pragma unroll
+      for (int u = kStreamVPL - 1; u >= 0; --u)
+#pragma unroll
+        for (int e = E - 1; e >= 0; --e)
+          if (elem_of<T>(x[u], e) == t.m1) arg = s0 + (u * 32 + lane) * E + e;
+    }
+    arg = __reduce_min_sync(0xffffffffu, arg);
+    if (lane == 0) {
+      ConfPartial out;
+      out.m1 = t.m1;
+      out.m2 = t.m2;
+      out.l = t.l;
+      out.arg = arg;
+      ws[((int64_t)br * nchunks + c) * kStreamWarps + warp] = out;
+    }
+    ++j;
+  }
+  if (lane == 0 && *abort) report(dev_status, DLLM_ERR_TIMEOUT);
+}
+
 template <typename T>
 int conf_nchunks(int V) {
   const int n = (V + conf_chunk_elems<T>() - 1) / conf_chunk_elems<T>();
@@ -321,20 +558,33 @@ cudaError_t launch_typed(const T* logits, int B, int R_src, int V, int64_t rs, i
   const int nchunks = conf_nchunks<T>(V);
   const bool vec = (reinterpret_cast<uintptr_t>(logits) % 16 == 0) && (rs % E == 0) &&
                    (bs % E == 0);
-  dim3 grid(B * R_max, nchunks);
   ConfPartial* part = static_cast<ConfPartial*>(ws);
-  if (vec)
-    conf_partial_kernel<T, true><<<grid, kConfThreads, 0, stream>>>(
-        logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
-  else
-    conf_partial_kernel<T, false><<<grid, kConfThreads, 0, stream>>>(
-        logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
+  int parts = nchunks;  // partials per row handed to the merge
+  const bool stream_ok = vec && ((int64_t)V * (int64_t)sizeof(T)) % 16 == 0 &&
+                         (int64_t)B * R_max * stream_nchunks(V, (int)sizeof(T)) < INT32_MAX;
+  if (stream_ok) {
+    const cudaError_t ea =
+        ensure_smem_limit(reinterpret_cast<const void*>(conf_stream_kernel<T>), (int)kStreamSmem);
+    if (ea != cudaSuccess) return ea;
+    const int snc = stream_nchunks(V, (int)sizeof(T));
+    conf_stream_kernel<T><<<num_sms(), kStreamThreads, kStreamSmem, stream>>>(
+        logits, R_src, V, rs, bs, B, R_max, row_idx, count, snc, part, dev_status);
+    parts = snc * kStreamWarps;
+  } else {
+    dim3 grid(B * R_max, nchunks);
+    if (vec)
+      conf_partial_kernel<T, true><<<grid, kConfThreads, 0, stream>>>(
+          logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
+    else
+      conf_partial_kernel<T, false><<<grid, kConfThreads, 0, stream>>>(
+          logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)B * R_max;
   const int warps = 8;
   conf_merge_kernel<<<(unsigned)((rows + warps - 1) / warps), warps * 32, 0, stream>>>(
-      B, R_src, R_max, row_idx, count, out_idx, out_cols, nchunks, part, conf_out, argmax_out,
+      B, R_src, R_max, row_idx, count, out_idx, out_cols, parts, part, conf_out, argmax_out,
       margin_out, dev_status);
   return cudaGetLastError();
 }
@@ -342,8 +592,12 @@ cudaError_t launch_typed(const T* logits, int B, int R_src, int V, int64_t rs, i
 }  // namespace
 
 size_t confidence_workspace_bytes(int B, int R_max, int V, int dtype) {
-  const int nchunks = dtype == DLLM_BF16 ? conf_nchunks<__nv_bfloat16>(V) : conf_nchunks<float>(V);
-  return (size_t)B * (size_t)R_max * (size_t)nchunks * sizeof(ConfPartial);
+  // partials per row: one per 32 KB chunk (chunked kernel) or one per 8 KB
+  // slice (streaming kernel); size for the larger
+  const int eb = dtype == DLLM_BF16 ? 2 : 4;
+  const int a = dtype == DLLM_BF16 ? conf_nchunks<__nv_bfloat16>(V) : conf_nchunks<float>(V);
+  const int s = stream_nchunks(V, eb) * kStreamWarps;
+  return (size_t)B * (size_t)R_max * (size_t)(a > s ? a : s) * sizeof(ConfPartial);
 }
 
 cudaError_t launch_confidence(const void* logits, int dtype, int B, int R_src, int V,

@@ -38,9 +38,12 @@ cudaError_t launch_attention_simt(const void* q, const void* k, const void* v, i
 bool attention_tc_supported(int dtype, int d, const void* q, const void* k, const void* v,
                             const void* o);
 
+size_t attention_tc_workspace_bytes(int n_ctas);
+
 cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int B, int L, int H,
                                 int M_max, const int32_t* count, float scale, void* o, float* lse,
-                                float* colsum, int32_t* dev_status, cudaStream_t stream);
+                                float* colsum, void* ws, size_t ws_bytes, int32_t* dev_status,
+                                cudaStream_t stream);
 
 cudaError_t launch_colsum_simt(const void* q, const void* k, int dtype, int B, int L, int H,
                                int d, int M_max, const int32_t* count, float scale,
@@ -52,6 +55,10 @@ cudaError_t launch_stable_prefix(const float* score, int B, int L, int32_t* star
                                  int32_t* dev_status, cudaStream_t stream);
 
 int num_sms();
+
+// Raises the dynamic shared-memory limit of `func` to `bytes` on the current
+// device (once per function and device).
+cudaError_t ensure_smem_limit(const void* func, int bytes);
 
 // Records `message` as the thread's dllm_last_error() text and returns `code`.
 int set_last_error(int code, const char* message);

@@ -7,8 +7,9 @@
 // SureLock, technical summary section 2: locked positions are never active.
 //
 // Two launches:
-//   cos_rows_kernel  one warp per row, 16-byte streaming loads, three float32
-//                    accumulators (<a,b>, |a|^2, |b|^2) reduced by shuffles.
+//   cos_rows_kernel  32 to 256 threads per row (more when rows are few),
+//                    16-byte streaming loads, three float32 accumulators
+//                    (<a,b>, |a|^2, |b|^2) reduced by shuffles.
 //                    HBM bound: 2 * D * sizeof(T) bytes per row.
 //   compact_kernel   one CTA per batch row: threshold + lock mask, block-wide
 //                    exclusive scan, ascending idx, -1 padding, count.
@@ -64,55 +65,85 @@ __device__ __forceinline__ float cosine_from_sums(float dot, float na, float nb)
   return dot / (sqrtf(na) * sqrtf(nb));
 }
 
-// VEC: rows are 16-byte aligned and D is a multiple of the vector width.
-template <typename T, bool VEC>
+// One group of TPR threads (TPR in {32, 64, 128, 256}) per row, 256 threads
+// per CTA.  Few rows (a 512-row window) take 256 threads each so that every
+// SM streams; many rows take one warp each.  VEC: rows are 16-byte aligned and
+// D is a multiple of the vector width.
+template <typename T, bool VEC, int TPR>
 __global__ void __launch_bounds__(kCosWarps * 32)
 cos_rows_kernel(const T* __restrict__ cur, const T* __restrict__ prev, int B, int Lw, int D,
                 int64_t rs, int64_t bs, float* __restrict__ cos_out) {
-  const int lane = threadIdx.x & 31;
+  constexpr int kRowsPerCta = kCosWarps * 32 / TPR;
+  constexpr int kWarpsPerRow = TPR / 32;
+  __shared__ float red[kCosWarps][3];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gi = threadIdx.x / TPR;  // row slot in the CTA
+  const int li = threadIdx.x % TPR;  // thread within the row group
   const int64_t total = (int64_t)B * Lw;
-  const int64_t stride = (int64_t)gridDim.x * kCosWarps;
-  for (int64_t row = (int64_t)blockIdx.x * kCosWarps + (threadIdx.x >> 5); row < total;
-       row += stride) {
-    const int b = (int)(row / Lw);
-    const int r = (int)(row - (int64_t)b * Lw);
-    const T* pc = cur + b * bs + r * rs;
-    const T* pp = prev + b * bs + r * rs;
+  for (int64_t row0 = (int64_t)blockIdx.x * kRowsPerCta; row0 < total;
+       row0 += (int64_t)gridDim.x * kRowsPerCta) {
+    const int64_t row = row0 + gi;
     float dot = 0.f, na = 0.f, nb = 0.f;
-    if constexpr (VEC) {
-      constexpr int E = Vec16<T>::kElems;
-      const int nvec = D / E;
-      const uint4* vc = reinterpret_cast<const uint4*>(pc);
-      const uint4* vp = reinterpret_cast<const uint4*>(pp);
-      for (int base = 0; base < nvec; base += 32 * kCosUnroll) {
-        uint4 a[kCosUnroll], c[kCosUnroll];
+    if (row < total) {
+      const int b = (int)(row / Lw);
+      const int r = (int)(row - (int64_t)b * Lw);
+      const T* pc = cur + b * bs + r * rs;
+      const T* pp = prev + b * bs + r * rs;
+      if constexpr (VEC) {
+        constexpr int E = Vec16<T>::kElems;
+        const int nvec = D / E;
+        const uint4* vc = reinterpret_cast<const uint4*>(pc);
+        const uint4* vp = reinterpret_cast<const uint4*>(pp);
+        for (int base = 0; base < nvec; base += TPR * kCosUnroll) {
+          uint4 a[kCosUnroll], c[kCosUnroll];
 #pragma unroll
-        for (int u = 0; u < kCosUnroll; ++u) {
-          const int v = base + u * 32 + lane;
-          if (v < nvec) {
-            a[u] = ld_stream16(vc + v);
-            c[u] = ld_stream16(vp + v);
-          } else {
-            a[u] = make_uint4(0, 0, 0, 0);
-            c[u] = make_uint4(0, 0, 0, 0);
+          for (int u = 0; u < kCosUnroll; ++u) {
+            const int v = base + u * TPR + li;
+            if (v < nvec) {
+              a[u] = ld_stream16(vc + v);
+              c[u] = ld_stream16(vp + v);
+            } else {
+              a[u] = make_uint4(0, 0, 0, 0);
+              c[u] = make_uint4(0, 0, 0, 0);
+            }
           }
-        }
 #pragma unroll
-        for (int u = 0; u < kCosUnroll; ++u) Vec16<T>::acc(a[u], c[u], dot, na, nb);
-      }
-    } else {
-      for (int k = lane; k < D; k += 32) {
-        const float x = Elem<T>::to_f32(pc[k]);
-        const float y = Elem<T>::to_f32(pp[k]);
-        dot = fmaf(x, y, dot);
-        na = fmaf(x, x, na);
-        nb = fmaf(y, y, nb);
+          for (int u = 0; u < kCosUnroll; ++u) Vec16<T>::acc(a[u], c[u], dot, na, nb);
+        }
+      } else {
+        for (int k = li; k < D; k += TPR) {
+          const float x = Elem<T>::to_f32(pc[k]);
+          const float y = Elem<T>::to_f32(pp[k]);
+          dot = fmaf(x, y, dot);
+          na = fmaf(x, x, na);
+          nb = fmaf(y, y, nb);
+        }
       }
     }
     dot = warp_sum(dot);
     na = warp_sum(na);
     nb = warp_sum(nb);
-    if (lane == 0) cos_out[row] = cosine_from_sums(dot, na, nb);
+    if constexpr (kWarpsPerRow == 1) {
+      if (lane == 0 && row < total) cos_out[row] = cosine_from_sums(dot, na, nb);
+    } else {
+      if (lane == 0) {
+        red[warp][0] = dot;
+        red[warp][1] = na;
+        red[warp][2] = nb;
+      }
+      __syncthreads();
+      if (li == 0 && row < total) {
+        float sd = 0.f, sa = 0.f, sb = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarpsPerRow; ++w) {  // fixed order: run-to-run identical
+          sd += red[gi * kWarpsPerRow + w][0];
+          sa += red[gi * kWarpsPerRow + w][1];
+          sb += red[gi * kWarpsPerRow + w][2];
+        }
+        cos_out[row] = cosine_from_sums(sd, sa, sb);
+      }
+      __syncthreads();
+    }
   }
 }
 
@@ -178,22 +209,43 @@ compact_kernel(const float* __restrict__ cos, const uint8_t* __restrict__ locked
   if (tid == 0) count_out[b] = running;
 }
 
+template <typename T, bool VEC, int TPR>
+void launch_cos(const T* cur, const T* prev, int B, int Lw, int D, int64_t rs, int64_t bs,
+                float* cos_out, cudaStream_t stream) {
+  constexpr int kRowsPerCta = kCosWarps * 32 / TPR;
+  const int64_t rows = (int64_t)B * Lw;
+  const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
+  const int64_t cap = (int64_t)num_sms() * 16;
+  const int grid = (int)(want < cap ? want : cap);
+  cos_rows_kernel<T, VEC, TPR><<<grid, kCosWarps * 32, 0, stream>>>(cur, prev, B, Lw, D, rs, bs,
+                                                                    cos_out);
+}
+
+template <typename T, bool VEC>
+void launch_cos_tpr(const T* cur, const T* prev, int B, int Lw, int D, int64_t rs, int64_t bs,
+                    float* cos_out, cudaStream_t stream) {
+  // enough row groups for ~16 resident warps per SM on every SM
+  const int64_t rows = (int64_t)B * Lw;
+  const int64_t target_threads = (int64_t)num_sms() * 16 * 32;
+  int tpr = 32;
+  while (tpr < 256 && rows * tpr < target_threads) tpr *= 2;
+  if (tpr == 32) launch_cos<T, VEC, 32>(cur, prev, B, Lw, D, rs, bs, cos_out, stream);
+  else if (tpr == 64) launch_cos<T, VEC, 64>(cur, prev, B, Lw, D, rs, bs, cos_out, stream);
+  else if (tpr == 128) launch_cos<T, VEC, 128>(cur, prev, B, Lw, D, rs, bs, cos_out, stream);
+  else launch_cos<T, VEC, 256>(cur, prev, B, Lw, D, rs, bs, cos_out, stream);
+}
+
 template <typename T>
 cudaError_t launch_typed(const T* cur, const T* prev, int B, int Lw, int D, int64_t rs,
                          int64_t bs, float* cos_out, cudaStream_t stream) {
-  const int64_t rows = (int64_t)B * Lw;
-  const int64_t want = (rows + kCosWarps - 1) / kCosWarps;
-  const int grid = (int)(want < (int64_t)num_sms() * 16 ? want : (int64_t)num_sms() * 16);
   constexpr int E = 16 / sizeof(T);
   const bool vec = (reinterpret_cast<uintptr_t>(cur) % 16 == 0) &&
                    (reinterpret_cast<uintptr_t>(prev) % 16 == 0) && (D % E == 0) &&
                    (rs % E == 0) && (bs % E == 0);
   if (vec)
-    cos_rows_kernel<T, true><<<grid, kCosWarps * 32, 0, stream>>>(cur, prev, B, Lw, D, rs, bs,
-                                                                  cos_out);
+    launch_cos_tpr<T, true>(cur, prev, B, Lw, D, rs, bs, cos_out, stream);
   else
-    cos_rows_kernel<T, false><<<grid, kCosWarps * 32, 0, stream>>>(cur, prev, B, Lw, D, rs, bs,
-                                                                   cos_out);
+    launch_cos_tpr<T, false>(cur, prev, B, Lw, D, rs, bs, cos_out, stream);
   return cudaGetLastError();
 }
 

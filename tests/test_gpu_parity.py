@@ -402,3 +402,52 @@ def test_step_1k_against_oracle_step(dl):
     assert np.array_equal(i32(step.argmax)[:, w:], ref["argmax"])
     # prefix decision on the GPU's own score array
     assert np.array_equal(i32(step.length), oracle.stable_prefix(gs.astype(np.float32), [w], 0.9, True))
+
+
+@pytest.mark.parametrize("L,counts", [(1500, [130, 7]), (2100, [1, 260]), (4096, [37])])
+def test_attention_split_key_range_ragged(dl, L, counts):
+    # few query tiles -> the key range is split across CTAs, then merged
+    _attn_case(dl, len(counts), 300, counts, L, 4, 128, torch.bfloat16, seed=L)
+
+
+def test_attention_without_workspace_matches_split(dl):
+    B, M_max, L, H, d = 1, 200, 2048, 8, 128
+    g = torch.Generator().manual_seed(77)
+    q = dev(workloads.normal(g, (B, M_max, H, d), 1.0, torch.bfloat16))
+    k = dev(workloads.normal(g, (B, L, H, d), 1.0, torch.bfloat16))
+    v = dev(workloads.normal(g, (B, L, H, d), 1.0, torch.bfloat16))
+    count = dev(torch.tensor([150], dtype=torch.int32))
+    o1, l1, c1 = dl.dllm_partial_attention(q, k, v, count)  # workspace: split allowed
+    no_ws = torch.empty((0,), dtype=torch.uint8, device="cuda")
+    o2, l2, c2 = dl.dllm_partial_attention(q, k, v, count, ws=no_ws)  # never split
+    torch.cuda.synchronize()
+    ro, rl, rc = oracle.partial_attention(f64(q), f64(k), f64(v), [150])
+    for o, lse, cs in ((o1, l1, c1), (o2, l2, c2)):
+        check_attn(o[:, :150], ro[:, :150], torch.bfloat16)
+        assert np.max(np.abs(f64(lse)[:, :, :150] - rl[:, :, :150])) <= SCORE_TOL
+        assert np.max(np.abs(f64(cs) - rc)) <= SCORE_TOL
+
+
+def test_attention_repeatable_run_to_run(dl):
+    s = workloads.STEP_1K
+    g = torch.Generator().manual_seed(9)
+    q = dev(workloads.normal(g, (1, s.Lw, s.H, s.d), 1.0, s.dtype))
+    k = dev(workloads.normal(g, (1, s.L, s.H, s.d), 1.0, s.dtype))
+    v = dev(workloads.normal(g, (1, s.L, s.H, s.d), 1.0, s.dtype))
+    count = dev(torch.tensor([102], dtype=torch.int32))
+    a = [t.clone() for t in dl.dllm_partial_attention(q, k, v, count)]
+    b = dl.dllm_partial_attention(q, k, v, count)
+    torch.cuda.synchronize()
+    assert torch.equal(a[0][:, :102], b[0][:, :102])
+    assert torch.equal(a[1][:, :, :102], b[1][:, :, :102])
+    assert torch.equal(a[2], b[2])
+
+
+def test_confidence_repeatable_run_to_run(dl):
+    g = torch.Generator().manual_seed(19)
+    z = dev(workloads.normal(g, (2, 300, 126464), 2.0, torch.bfloat16))
+    a = [t.clone() for t in dl.dllm_confidence(z)]
+    b = dl.dllm_confidence(z)
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
