@@ -2,10 +2,13 @@
 """Benchmark of the partial denoising step on B300.
 
 One step = one pass of the whole hot path over one batch: saliency select,
-KV scatter, partial attention with column sums, confidence over the window's
-logit rows, longest stable prefix.  Default workload: batch 1, L = 1024
-(512 prompt + 512 generated), 32 heads x 128, hidden 4096, vocabulary 126464
-logits over the generated rows, ~10% of positions salient, bf16.
+KV scatter, partial attention, the column-sum pass, confidence over the logit
+rows, longest stable prefix.  Default workload (``--workload step_1k``):
+batch 1, L = 1024 (512 prompt + 512 generated), 32 heads x 128, hidden 4096,
+vocabulary 126464 logits over the generated rows, ~10% of positions salient,
+bf16.  The other workloads are the larger step shapes (``batch8_2k`` with an
+active fraction and pattern, ``long_4k`` with a locked fraction, ``loop_b4_2k``)
+and print the same line for their own shape.
 
 Metric: active query tokens per second (sum over batch rows of the active
 count / step time); the line also carries the step latency, a per-entry-point
@@ -14,15 +17,21 @@ the timed region, the end-to-end figure (host buffers, copies inside the
 timed region) and the float64 oracle timed on the host cores.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--workload NAME] [--frac F] [--pattern random|cluster] [--locked F]
 Under torchrun (N > 1) every rank runs an independent replica (weak scaling);
 the timed region is bracketed by barriers and the max over ranks is reported.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
+import hashlib
 import json
+import math
 import os
+import shutil
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -36,15 +45,43 @@ import workloads  # noqa: E402
 
 METRIC = "partial-step latency (µs) & active query tokens/s; % of B300 HBM/TC roofline"
 UNIT = "active query tokens/s"
-N_SETS = 4  # rotating input sets: 4 x ~175 MB keeps every step's inputs out of L2 (126 MB)
+CSRC = os.path.join(ROOT, "partial_attention_saliency_b300", "csrc")
+
+ENTRY_ORDER = ["dllm_saliency_select", "dllm_kv_scatter", "dllm_partial_attention",
+               "dllm_attention_colsum", "dllm_confidence", "dllm_stable_prefix"]
+KERNELS = {  # kernels each entry point launches, and the source they come from
+    "dllm_saliency_select": (["cos_rows_kernel", "compact_kernel"], "select.cu"),
+    "dllm_kv_scatter": (["kv_scatter_kernel"], "kv_scatter.cu"),
+    "dllm_partial_attention": (["attn_fwd_tc_kernel", "attn_split_merge_kernel"],
+                               "attention_tc.cu"),
+    "dllm_attention_colsum": (["attn_colsum_tc_kernel"], "attention_tc.cu"),
+    "dllm_confidence": (["conf_stream_kernel", "conf_merge_kernel"], "confidence.cu"),
+    "dllm_stable_prefix": (["stable_prefix_kernel"], "stable_prefix.cu"),
+}
+
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of an
+# entry point's main kernel, from one ncu capture of the named workload.  The
+# figure is reported only while the kernel's source file still has the digest
+# it was captured with; otherwise traffic is null.
+TRAFFIC = {
+    # (workload, entry point): {"bytes": ..., "src_sha": first 16 hex of sha256}
+}
 
 
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: about one second of steps)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["step_1k", "batch8_2k", "long_4k", "loop_b4_2k"],
+                    default="step_1k")
+    ap.add_argument("--frac", type=float, default=0.25,
+                    help="batch8_2k: active fraction of the 2048 positions")
+    ap.add_argument("--pattern", choices=["random", "cluster"], default="random")
+    ap.add_argument("--locked", type=float, default=0.0,
+                    help="long_4k: locked fraction (0 = first step of the schedule)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time spent on the oracle baseline sample")
@@ -69,181 +106,337 @@ def peaks():
             "source": "fallback"}
 
 
+def src_sha(fname: str) -> str:
+    with open(os.path.join(CSRC, fname), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- clocks
+
 class ClockSampler:
-    """Polls NVML (SM clock, clock-event reasons) from a thread while running."""
+    """Samples the SM clock and the clock-event reasons while running: NVML
+    when the Python module is present, else an ``nvidia-smi -lms`` child."""
 
     REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
                0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown",
                0x100: "display_clock_setting"}
 
-    def __init__(self, index: int, period_s: float = 0.002):
+    def __init__(self, device_index: int, period_s: float = 0.005):
         self.samples = []
         self.period = period_s
-        self.ok = False
         self.max_mhz = None
+        self.mode = None
+        self.err = None
+        props = torch.cuda.get_device_properties(device_index)
+        self.uuid = "GPU-" + str(props.uuid)
+        self._stop = threading.Event()
+        self._t = None
+        self._proc = None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
-            self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
+            self.h = pynvml.nvmlDeviceGetHandleByUUID(self.uuid.encode())
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
+            self.mode = "nvml"
         except Exception as e:  # noqa: BLE001
-            self.err = repr(e)[:200]
-        self._stop = threading.Event()
-        self._t = None
+            self.err = repr(e)[:160]
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
                 mhz = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
                 reasons = nv.nvmlDeviceGetCurrentClocksEventReasons(self.h)
-                self.samples.append((mhz, reasons))
+                self.samples.append((mhz, int(reasons)))
             except Exception:  # noqa: BLE001
                 pass
             time.sleep(self.period)
 
     def start(self):
-        if self.ok:
-            self._t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self._t = threading.Thread(target=self._run_nvml, daemon=True)
             self._t.start()
+        elif self.mode == "nvidia-smi":
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.uuid,
+                 "--query-gpu=timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.5)  # the child is sampling before the timed region begins
+        self.t0 = time.time()
 
     def stop(self):
+        self.t1 = time.time()
         if self._t is not None:
             self._stop.set()
             self._t.join()
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                out, _ = self._proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+                out, _ = self._proc.communicate()
+            from datetime import datetime
+            for line in out.splitlines():
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) != 4:
+                    continue
+                try:
+                    ts = datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    mhz, mx = float(parts[1]), float(parts[2])
+                    reasons = int(parts[3], 16)
+                except ValueError:
+                    continue
+                self.max_mhz = mx
+                if self.t0 <= ts <= self.t1:  # samples taken inside the timed region only
+                    self.samples.append((mhz, reasons))
 
     def summary(self):
-        if not self.ok or not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [],
-                    "samples": 0, "source": "nvml unavailable" if not self.ok else "nvml",
-                    "error": getattr(self, "err", None)}
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "source": self.mode or "unavailable", "error": self.err}
         mhz = [m for m, _ in self.samples]
         seen = 0
         for _, r in self.samples:
             seen |= int(r)
         names = [n for bit, n in self.REASONS.items() if seen & bit and n != "gpu_idle"]
         return {"sm_mhz": statistics.median(mhz), "sm_max_mhz": self.max_mhz, "reasons": names,
-                "samples": len(mhz), "source": "nvml"}
+                "samples": len(mhz), "source": self.mode}
 
 
-# ----------------------------------------------------------------------------- workload
+# ----------------------------------------------------------------------------- workloads
 
-def workload_desc(s, n_active):
-    return {"workload": f"partial step B{s.B} L{s.L} ({s.win_start} prompt + {s.Lw} gen) "
-                        f"{s.H}x{s.d} heads, hidden {s.D}, vocab {s.V} over {s.logit_rows} gen rows, "
-                        f"~{round(100 * n_active / s.L)}% salient",
-            "batch": s.B, "seq_len": s.L, "heads": s.H, "head_dim": s.d, "hidden": s.D,
-            "vocab": s.V, "logit_rows": s.logit_rows, "active_rows": n_active,
-            "l2": f"{N_SETS} rotating input sets (~{N_SETS * 175} MB) > 126 MB L2",
-            "parallelism": "replicas (one independent step per GPU)"}
+@dataclasses.dataclass
+class Workload:
+    """One benchmarked step shape.
+
+    ``conf``: how the confidence pass reads its logit rows -- "window" (one
+    logit row per window position, row r -> position win_start + r), "gather"
+    (a full [B, L, V] logits buffer read through row_idx = the active
+    positions), "compact" (one logit row per active row, in compaction order)
+    or None (no confidence pass).
+    """
+
+    name: str
+    shape: workloads.StepShape
+    n_active: int
+    pattern: str
+    locked: float
+    conf: str
+    logit_rows: int
+    default_steps: int
+    desc: str
 
 
-def algorithmic_work(s, counts):
+def make_workload(args) -> Workload:
+    if args.workload == "step_1k":
+        s = workloads.STEP_1K
+        return Workload("step_1k", s, s.n_salient, "random", 0.0, "window", s.logit_rows, 10000,
+                        f"partial step B{s.B} L{s.L} ({s.win_start} prompt + {s.Lw} gen) "
+                        f"{s.H}x{s.d} heads, hidden {s.D}, vocab {s.V} over {s.logit_rows} "
+                        f"gen rows, ~10% salient")
+    if args.workload == "batch8_2k":
+        s = workloads.BATCH8_2K
+        n = round(args.frac * s.L)
+        return Workload(f"batch8_2k_f{round(100 * args.frac):02d}_{args.pattern}", s, n,
+                        args.pattern, 0.0, None, 0, 400,
+                        f"partial step B{s.B} L{s.L} {s.H}x{s.d} heads, hidden {s.D}, "
+                        f"{round(100 * args.frac)}% active ({args.pattern}), no logits")
+    if args.workload == "long_4k":
+        s = workloads.LONG_4K
+        n_locked = round(args.locked * s.L)
+        return Workload(f"long_4k_locked{round(100 * args.locked):02d}", s, s.L - n_locked,
+                        "random", args.locked, "gather", s.L, 200,
+                        f"partial step B{s.B} L{s.L} {s.H}x{s.d} heads, vocab {s.V}, "
+                        f"{round(100 * args.locked)}% locked, logits of the active rows "
+                        f"gathered from a [{s.L}, {s.V}] buffer")
+    s = workloads.LOOP_B4_2K
+    n = 134
+    return Workload("loop_b4_2k", s, n, "random", 0.0, "compact", 160, 2000,
+                    f"partial step B{s.B} L{s.L} ({s.win_start} prompt + {s.Lw} gen) "
+                    f"{s.H}x{s.d} heads, hidden {s.D}, vocab {s.V}, {n} active per batch row, "
+                    f"logits of the active rows only")
+
+
+def build_set(wl: Workload, seed: int, device):
+    """Inputs of one step on the device (and the host copies for e2e)."""
+    s = wl.shape
+    inp = workloads.make_step(dataclasses.replace(s, logit_rows=0) if wl.conf != "window" else s,
+                              n_salient=0 if wl.conf == "gather" else wl.n_active,
+                              pattern=wl.pattern, seed=seed, with_logits=wl.conf == "window")
+    g = torch.Generator().manual_seed(seed + 7)
+    if wl.conf == "gather":
+        inp["logits"] = workloads.normal(g, (s.B, s.L, s.V), 2.0, s.dtype)
+    elif wl.conf == "compact":
+        inp["logits"] = workloads.normal(g, (s.B, wl.logit_rows, s.V), 2.0, s.dtype)
+    locked = None
+    if wl.locked > 0:
+        n_locked = round(wl.locked * s.Lw)
+        locked = torch.zeros((s.B, s.Lw), dtype=torch.uint8)
+        for b in range(s.B):
+            locked[b, torch.randperm(s.Lw, generator=g)[:n_locked]] = 1
+    inp["locked"] = locked
+    d = {k: inp[k].to(device) for k in ("cur", "prev", "k_cache", "v_cache", "k_new", "v_new", "q")}
+    d["locked"] = None if locked is None else locked.to(device)
+    if wl.conf == "compact":
+        # R_max = M_max logit rows; only rows < count are ever read
+        buf = torch.zeros((s.B, s.Lw, s.V), dtype=s.dtype, device=device)
+        buf[:, :wl.logit_rows] = inp["logits"].to(device)
+        d["logits"] = buf
+    elif wl.conf is not None:
+        d["logits"] = inp["logits"].to(device)
+    d["score"] = torch.full((s.B, s.L), float("inf"), device=device)
+    d["start"] = torch.full((s.B,), s.win_start, dtype=torch.int32, device=device)
+    d["host"] = inp
+    return d
+
+
+def set_bytes(d) -> int:
+    return sum(t.numel() * t.element_size() for k, t in d.items()
+               if isinstance(t, torch.Tensor) and t.is_cuda)
+
+
+class Buffers:
+    """Outputs and workspaces of the step, allocated once."""
+
+    def __init__(self, dl, wl: Workload, device):
+        s = wl.shape
+        f32, i32 = torch.float32, torch.int32
+        self.M_max = s.Lw
+        self.cos = torch.empty((s.B, s.Lw), dtype=f32, device=device)
+        self.idx = torch.empty((s.B, s.Lw), dtype=i32, device=device)
+        self.count = torch.empty((s.B,), dtype=i32, device=device)
+        self.o = torch.empty((s.B, self.M_max, s.H, s.d), dtype=s.dtype, device=device)
+        self.lse = torch.empty((s.B, s.H, self.M_max), dtype=f32, device=device)
+        self.colsum = torch.empty((s.B, s.H, s.L), dtype=f32, device=device)
+        self.argmax = torch.zeros((s.B, s.L), dtype=i32, device=device)
+        self.margin = torch.zeros((s.B, s.L), dtype=f32, device=device)
+        self.length = torch.empty((s.B,), dtype=i32, device=device)
+        self.dev_status = torch.zeros((1,), dtype=i32, device=device)
+        r_max = s.logit_rows if wl.conf == "window" else s.Lw
+        cw = dl.dllm_confidence_workspace_bytes(s.B, max(r_max, 1), s.V, s.dtype)
+        self.conf_ws = torch.empty((max(cw, 16),), dtype=torch.uint8, device=device)
+        aw = dl.dllm_attention_workspace_bytes(s.B, s.L, s.H, s.d, self.M_max, s.dtype)
+        self.attn_ws = torch.empty((max(aw, 16),), dtype=torch.uint8, device=device)
+        self.attn_split = aw > 0
+
+
+def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None):
+    """The six calls in order; optional events bracket each call."""
+    s = wl.shape
+    w = s.win_start
+    ev = events
+    if ev: ev[0].record(stream)
+    dl.dllm_saliency_select(d["cur"][:, w:], d["prev"][:, w:], s.tau, locked=d["locked"],
+                            idx_base=w, cos_out=bf.cos, idx_out=bf.idx, count_out=bf.count,
+                            dev_status=bf.dev_status, stream=stream)
+    if ev: ev[1].record(stream)
+    dl.dllm_kv_scatter(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], bf.idx, bf.count,
+                       dev_status=bf.dev_status, stream=stream)
+    if ev: ev[2].record(stream)
+    dl.dllm_partial_attention(d["q"], d["k_cache"], d["v_cache"], bf.count, o_out=bf.o,
+                              lse_out=bf.lse, with_colsum=False, ws=bf.attn_ws,
+                              dev_status=bf.dev_status, stream=stream)
+    if ev: ev[3].record(stream)
+    dl.dllm_attention_colsum(d["q"], d["k_cache"], bf.count, bf.lse, colsum_out=bf.colsum,
+                             dev_status=bf.dev_status, stream=stream)
+    if ev: ev[4].record(stream)
+    if wl.conf == "window":
+        dl.dllm_confidence(d["logits"], out_cols=s.L, conf_out=d["score"][:, w:],
+                           argmax_out=bf.argmax[:, w:], margin_out=bf.margin[:, w:],
+                           ws=bf.conf_ws, dev_status=bf.dev_status, stream=stream)
+    elif wl.conf == "gather":
+        dl.dllm_confidence(d["logits"], R_max=s.Lw, row_idx=bf.idx, count=bf.count,
+                           out_idx=bf.idx, out_cols=s.L, conf_out=d["score"],
+                           argmax_out=bf.argmax, margin_out=bf.margin, ws=bf.conf_ws,
+                           dev_status=bf.dev_status, stream=stream)
+    elif wl.conf == "compact":
+        dl.dllm_confidence(d["logits"], R_max=s.Lw, count=bf.count, out_idx=bf.idx,
+                           out_cols=s.L, conf_out=d["score"], argmax_out=bf.argmax,
+                           margin_out=bf.margin, ws=bf.conf_ws, dev_status=bf.dev_status,
+                           stream=stream)
+    if ev: ev[5].record(stream)
+    dl.dllm_stable_prefix(d["score"], d["start"], 0.9, min_commit=True, advance_start=False,
+                          len_out=bf.length, dev_status=bf.dev_status, stream=stream)
+    if ev: ev[6].record(stream)
+
+
+def launches_per_step(wl: Workload, bf: Buffers) -> int:
+    n = 2 + 1 + (2 if bf.attn_split else 1) + 1 + 1
+    if wl.conf is not None:
+        n += 2
+    return n
+
+
+def algorithmic_work(wl: Workload, counts):
     """Algorithmic bytes / flops of each entry point for one step."""
+    s = wl.shape
     M = int(sum(counts))
     el = 2 if s.dtype == torch.bfloat16 else 4
     hd = s.H * s.d
     select_b = 2 * s.B * s.Lw * s.D * el + s.B * s.Lw * 8
     scatter_b = M * 2 * 2 * hd * el
-    attn_b = 2 * s.B * s.L * hd * el + 2 * M * hd * el + M * s.H * 4 + s.B * s.H * s.L * 4
+    # K and V once per batch row, Q in and O out per active row, lse out
+    attn_b = 2 * s.B * s.L * hd * el + 2 * M * hd * el + M * s.H * 4
     attn_f = 4.0 * M * s.L * s.d * s.H
-    conf_b = s.B * s.logit_rows * (s.V * el + 12)
+    # K once per batch row, Q and lse per active row, colsum out
+    colsum_b = s.B * s.L * hd * el + M * hd * el + M * s.H * 4 + s.B * s.H * s.L * 4
+    if wl.conf == "window":
+        conf_rows = s.B * s.logit_rows
+    elif wl.conf is None:
+        conf_rows = 0
+    else:
+        conf_rows = M
+    conf_b = conf_rows * (s.V * el + 12)
     prefix_b = s.B * s.Lw * 4
     return {
         "dllm_saliency_select": {"bytes": select_b, "flops": 6.0 * s.B * s.Lw * s.D},
         "dllm_kv_scatter": {"bytes": scatter_b, "flops": 0.0},
-        "dllm_partial_attention": {"bytes": attn_b, "flops": attn_f,
-                                   "colsum_executed_flops": 2.0 * M * s.L * s.d * s.H},
+        "dllm_partial_attention": {"bytes": attn_b, "flops": attn_f},
+        # algorithmically the pass only adds L terms per active row; the
+        # executed work recomputes Q K^T (2 M L d H flops)
+        "dllm_attention_colsum": {"bytes": colsum_b, "flops": 2.0 * M * s.L * s.d * s.H,
+                                  "alg_adds": float(M * s.L * s.H)},
         "dllm_confidence": {"bytes": conf_b, "flops": 0.0},
         "dllm_stable_prefix": {"bytes": prefix_b, "flops": 0.0},
     }
 
 
-KERNELS = {  # kernels each entry point launches (for the ncu launch-list summary)
-    "dllm_saliency_select": ["cos_rows_kernel", "compact_kernel"],
-    "dllm_kv_scatter": ["kv_scatter_kernel"],
-    "dllm_partial_attention": ["attention kernels (forward + column sums)"],
-    "dllm_confidence": ["conf_partial_kernel", "conf_merge_kernel"],
-    "dllm_stable_prefix": ["stable_prefix_kernel"],
-}
+# ----------------------------------------------------------------------------- CPU oracle
 
-
-def build_sets(s, device):
-    sets = []
-    for i in range(N_SETS):
-        inp = workloads.make_step(s, seed=s.seed + 1000 * i)
-        d = {k: inp[k].to(device) for k in ("cur", "prev", "k_cache", "v_cache", "k_new", "v_new",
-                                            "q", "logits")}
-        d["score"] = torch.full((s.B, s.L), float("inf"), device=device)
-        d["start"] = torch.full((s.B,), s.win_start, dtype=torch.int32, device=device)
-        d["host"] = inp
-        sets.append(d)
-    return sets
-
-
-def run_step(dl, step, d, stream, events=None):
-    """The five entry points in order; optional events bracket each call."""
-    w = step.win_start
-    ev = events
-    if ev: ev[0].record(stream)
-    dl.dllm_saliency_select(d["cur"][:, w:], d["prev"][:, w:], step.tau, idx_base=w,
-                            cos_out=step.cos, idx_out=step.idx, count_out=step.count,
-                            dev_status=step.dev_status, stream=stream)
-    if ev: ev[1].record(stream)
-    dl.dllm_kv_scatter(d["k_cache"], d["v_cache"], d["k_new"], d["v_new"], step.idx, step.count,
-                       dev_status=step.dev_status, stream=stream)
-    if ev: ev[2].record(stream)
-    dl.dllm_partial_attention(d["q"], d["k_cache"], d["v_cache"], step.count, o_out=step.o,
-                              lse_out=step.lse, colsum_out=step.colsum, ws=step.attn_ws,
-                              dev_status=step.dev_status, stream=stream)
-    if ev: ev[3].record(stream)
-    dl.dllm_confidence(d["logits"], out_cols=step.L, conf_out=d["score"][:, w:],
-                       argmax_out=step.argmax[:, w:], margin_out=step.margin[:, w:],
-                       ws=step.conf_ws, dev_status=step.dev_status, stream=stream)
-    if ev: ev[4].record(stream)
-    dl.dllm_stable_prefix(d["score"], d["start"], step.tau_c, min_commit=True,
-                          advance_start=False, len_out=step.length, dev_status=step.dev_status,
-                          stream=stream)
-    if ev: ev[5].record(stream)
-
-
-ENTRY_ORDER = ["dllm_saliency_select", "dllm_kv_scatter", "dllm_partial_attention",
-               "dllm_confidence", "dllm_stable_prefix"]
-LAUNCHES_PER_STEP = 2 + 1 + 2 + 2 + 1
-
-
-def cpu_baseline(s, seconds, steps_cap=None):
-    """The float64 oracle, as it stands, on the host cores over full steps."""
+def oracle_step(wl: Workload, h, b: int):
+    """The float64 oracle over batch row ``b`` of one step (what the GPU step
+    computes for that row).  Returns the row's active count."""
     import numpy as np
     import oracle
-    inp = workloads.make_step(s)
-    d = {k: inp[k].double().numpy() for k in ("cur", "prev", "k_cache", "v_cache", "k_new",
-                                               "v_new", "q", "logits")}
-    times, active = [], 0
-    t_begin = time.perf_counter()
-    cpu_begin = time.process_time()
-    while True:
-        t0 = time.perf_counter()
-        out = oracle.step(d["cur"], d["prev"], d["k_cache"], d["v_cache"], d["k_new"],
-                          d["v_new"], d["q"], d["logits"], tau=s.tau, win_start=s.win_start,
-                          score=np.full((s.B, s.L), np.inf), start=[s.win_start] * s.B,
-                          tau_c=0.9)
-        times.append(time.perf_counter() - t0)
-        active = int(out["count"].sum())
-        if steps_cap is not None and len(times) >= steps_cap:
-            break
-        if steps_cap is None and time.perf_counter() - t_begin >= seconds:
-            break
-    util = (time.process_time() - cpu_begin) / max(time.perf_counter() - t_begin, 1e-9)
-    per_step = sum(times) / len(times)
-    return {"value": active / per_step, "unit": UNIT, "cores": blas_threads(),
-            "cpu_utilisation": round(util, 2), "kind": "oracle",
-            "sample": f"{len(times)} full float64 oracle steps of the same workload "
-                      f"({active} active rows each), {sum(times):.1f} s on the host",
-            "s_per_step": per_step}, times, active
+    s = wl.shape
+    w = s.win_start
+    sl = slice(b, b + 1)
+    f = lambda k: h[k][sl].double().numpy()  # noqa: E731
+    locked = None if h["locked"] is None else h["locked"][sl].numpy()
+    cur, prev = f("cur"), f("prev")
+    cos, idx, count = oracle.saliency_select(cur[:, w:], prev[:, w:], s.tau, locked, idx_base=w)
+    kc, vc = oracle.kv_scatter(f("k_cache"), f("v_cache"), f("k_new"), f("v_new"), idx, count)
+    o, lse, colsum = oracle.partial_attention(f("q"), kc, vc, count)
+    score = np.full((1, s.L), np.inf)
+    if wl.conf == "window":
+        conf, _, _ = oracle.confidence(f("logits"))
+        score[:, w:w + conf.shape[1]] = conf
+    elif wl.conf == "gather":
+        conf, _, _ = oracle.confidence(f("logits"), count=count, row_idx=idx)
+        n = int(count[0])
+        score[0, idx[0, :n]] = conf[0, :n]
+    elif wl.conf == "compact":
+        n = min(int(count[0]), wl.logit_rows)
+        conf, _, _ = oracle.confidence(f("logits"), count=[n])
+        score[0, idx[0, :n]] = conf[0, :n]
+    oracle.stable_prefix(score, [w], 0.9, True)
+    return int(count[0])
 
 
 def blas_threads():
@@ -258,29 +451,62 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
+def cpu_baseline(wl: Workload, host, seconds, steps_cap=None):
+    """The float64 oracle, as it stands, on the host cores: batch rows of the
+    same step taken in turn until ``seconds`` have passed (or ``steps_cap``
+    batch rows), at least one."""
+    times, rows, units = [], 0, 0
+    t_begin = time.perf_counter()
+    cpu_begin = time.process_time()
+    while True:
+        t0 = time.perf_counter()
+        units += oracle_step(wl, host, rows % wl.shape.B)
+        rows += 1
+        times.append(time.perf_counter() - t0)
+        if steps_cap is not None and rows >= steps_cap:
+            break
+        if steps_cap is None and time.perf_counter() - t_begin >= seconds:
+            break
+    elapsed = sum(times)
+    util = (time.process_time() - cpu_begin) / max(time.perf_counter() - t_begin, 1e-9)
+    return {"value": units / elapsed, "unit": UNIT, "cores": blas_threads(),
+            "cpu_utilisation": round(util, 2), "kind": "oracle",
+            "sample": f"{rows} batch row(s) of the {wl.name} step through the float64 oracle "
+                      f"({units} active rows in all), {elapsed:.1f} s on the host"}, times, units
+
+
 def reference_arm(args, rank):
     """`--impl reference`: the float64 oracle timed as the reference arm."""
-    s = workloads.STEP_1K
     if rank != 0:
         return 0
-    res, times, active = cpu_baseline(s, 0, steps_cap=args.warmup + args.steps)
-    timed = times[args.warmup:]
-    per = sum(timed) / len(timed)
-    value = active / per
+    wl = make_workload(args)
+    host = build_set(wl, wl.shape.seed, torch.device("cpu"))["host"]
+    # warm-up rows (at most 3), then as many of the K timed rows as fit in
+    # about 90 s of oracle time, at least 3: the run stays within minutes
+    _, wt, _ = cpu_baseline(wl, host, 0, steps_cap=max(1, min(args.warmup, 3)))
+    per_row = sum(wt) / len(wt)
+    k = args.steps if args.steps is not None else 10
+    res, times, units = cpu_baseline(wl, host, 0,
+                                     steps_cap=max(3, min(k, int(90.0 / max(per_row, 1e-6)))))
+    timed = sum(times)
+    value = units / timed
+    rows_per_step = wl.shape.B
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": per * 1e3, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_desc(s, active),
+            "n_gpus": args.gpus, "steps": len(times), "warmup": args.warmup,
+            "ms_per_step": timed / len(times) * rows_per_step * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.desc, "name": wl.name},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": res["cores"],
                              "kind": "oracle",
-                             "sample": f"{len(timed)} timed full float64 oracle steps after "
-                                       f"{args.warmup} warm-up steps"},
+                             "sample": f"{len(times)} timed batch row(s) of the step through the "
+                                       f"float64 oracle after {len(wt)} warm-up row(s)"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
 
+
+# ----------------------------------------------------------------------------- main
 
 def main():
     args = parse()
@@ -302,34 +528,42 @@ def main():
     import partial_attention_saliency_b300 as dl
     dl.load_library()
 
-    s = workloads.STEP_1K
-    sets = build_sets(s, device)
-    step = dl.PartialStep(s.B, s.L, s.H, s.d, s.D, s.V, s.dtype, s.win_start, s.logit_rows,
-                          s.tau, device=device)
+    wl = make_workload(args)
+    s = wl.shape
+    sets = [build_set(wl, s.seed + 1000 * (rank * 16 + 0), device)]
+    # rotate input sets so that every step's inputs come from HBM, not L2
+    n_sets = min(4, max(2, math.ceil(512e6 / set_bytes(sets[0]))))
+    for i in range(1, n_sets):
+        sets.append(build_set(wl, s.seed + 1000 * (rank * 16 + i), device))
+    bf = Buffers(dl, wl, device)
     stream = torch.cuda.current_stream(device)
     counts_per_set = []
     for d in sets:
-        run_step(dl, step, d, stream)
+        run_step(dl, wl, bf, d, stream)
         torch.cuda.synchronize()
-        counts_per_set.append(step.count.cpu().tolist())
-    assert int(step.dev_status[0]) == 0, "device-side check failed"
+        counts_per_set.append(bf.count.cpu().tolist())
+    assert int(bf.dev_status[0]) == 0, "device-side check failed"
 
     # ---------------------------------------------------------------- device-timed
-    # W warm-up steps and the K timed steps are each captured as one CUDA graph
-    # (no host launch gaps inside the timed region); external timing events
-    # between the entry points of every timed step give the per-kernel times.
-    K = args.steps
+    # A graph of S steps (with external timing events between the calls of
+    # every step) is replayed K / S times back to back: no host launch gaps in
+    # the timed region.  The per-call times come from the events of the last
+    # replay, which lies inside the timed region.
+    K = args.steps if args.steps is not None else wl.default_steps
+    S = min(K, 250)
+    K = max(S, (K // S) * S)
     cap = torch.cuda.Stream(device)
     g_warm = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_warm, stream=cap):
         for i in range(args.warmup):
-            run_step(dl, step, sets[i % N_SETS], torch.cuda.current_stream())
-    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(6)]
-          for _ in range(K)]
+            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream())
+    nev = len(ENTRY_ORDER) + 1
+    ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)]
+          for _ in range(S)]
     g_timed = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_timed, stream=cap):
-        for i in range(K):
-            run_step(dl, step, sets[i % N_SETS], torch.cuda.current_stream(), ev[i])
+        for i in range(S):
+            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream(), ev[i])
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
@@ -339,18 +573,19 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     t_start.record(stream)
-    g_timed.replay()
+    for _ in range(K // S):
+        g_timed.replay()
     t_end.record(stream)
     torch.cuda.synchronize()
     clocks.stop()
     if pg: pg.barrier()
-    assert int(step.dev_status[0]) == 0, "device-side check failed"
+    assert int(bf.dev_status[0]) == 0, "device-side check failed"
     elapsed_ms = t_start.elapsed_time(t_end)
     per_entry = {n: 0.0 for n in ENTRY_ORDER}
-    for i in range(K):
+    for i in range(S):
         for j, n in enumerate(ENTRY_ORDER):
             per_entry[n] += ev[i][j].elapsed_time(ev[i][j + 1])
-    active_total = sum(sum(counts_per_set[i % N_SETS]) for i in range(K))
+    active_total = sum(sum(counts_per_set[i % n_sets]) for i in range(S)) * (K // S)
     if pg:
         t = torch.tensor([elapsed_ms], device=device)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -363,43 +598,63 @@ def main():
 
     # ---------------------------------------------------------------- per entry point
     pk = peaks()
-    work = algorithmic_work(s, counts_per_set[0])
+    work = algorithmic_work(wl, counts_per_set[0])
+    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     kernels = {}
     for n in ENTRY_ORDER:
-        avg_ms = per_entry[n] / K
+        if n == "dllm_confidence" and wl.conf is None:
+            continue
+        avg_ms = per_entry[n] / S
         w = work[n]
         gbs = w["bytes"] / (avg_ms / 1e3) / 1e9
         tfs = w["flops"] / (avg_ms / 1e3) / 1e12
+        ai = w["flops"] / max(w["bytes"], 1)
+        bound = "tensor" if w["flops"] > 0 and ai > ridge and n == "dllm_partial_attention" \
+            else "hbm"
         kernels[n] = {"us": avg_ms * 1e3, "share": per_entry[n] / sum(per_entry.values()),
                       "alg_bytes": w["bytes"], "alg_flops": w["flops"], "GB/s": gbs,
-                      "TFLOP/s": tfs, "hbm_frac": gbs / pk["hbm_gbs"],
-                      "kernels": KERNELS[n]}
-    dom = max(ENTRY_ORDER, key=lambda n: per_entry[n])
+                      "TFLOP/s": tfs, "bound": bound,
+                      "frac": (tfs / pk["bf16_tflops"]) if bound == "tensor"
+                      else gbs / pk["hbm_gbs"],
+                      "kernels": KERNELS[n][0]}
+    dom = max(kernels, key=lambda n: kernels[n]["us"])
     dk = kernels[dom]
-    ai = work[dom]["flops"] / max(work[dom]["bytes"], 1)
-    ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
-    if work[dom]["flops"] > 0 and ai > ridge:
+    if dk["bound"] == "tensor":
         roof = {"bound": "tensor", "achieved": dk["TFLOP/s"], "peak": pk["bf16_tflops"],
-                "unit": "TFLOP/s", "frac": dk["TFLOP/s"] / pk["bf16_tflops"]}
+                "unit": "TFLOP/s", "frac": dk["TFLOP/s"] / pk["bf16_tflops"],
+                "frac_of_sustained": dk["TFLOP/s"] / pk["bf16_tflops_sustained"]}
     else:
         roof = {"bound": "hbm", "achieved": dk["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": dk["GB/s"] / pk["hbm_gbs"]}
-    roof.update({"traffic": None, "kernel": dom, "peak_source": pk["source"] + " (burst)",
-                 "alg_per_launch": work[dom]["bytes"] if roof["unit"] == "GB/s" else work[dom]["flops"]})
+    tr = TRAFFIC.get((wl.name, dom))
+    traffic = None
+    if tr is not None and tr["src_sha"] == src_sha(KERNELS[dom][1]):
+        traffic = tr["bytes"]
+    roof.update({"traffic": traffic, "kernel": dom, "kernels": KERNELS[dom][0],
+                 "peak_source": pk["source"] + " (burst)",
+                 "alg_per_launch": work[dom]["flops"] if roof["unit"] == "TFLOP/s"
+                 else work[dom]["bytes"],
+                 "timing": "CUDA events around the call on the launching stream, averaged "
+                           f"over the {S} steps of the last graph replay"})
 
     # ---------------------------------------------------------------- end to end
-    e2e = e2e_run(dl, s, step, sets, stream, args, pg, device)
+    e2e = e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step,
             "latency_us_per_step": ms_per_step * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_desc(s, sum(counts_per_set[0])),
+            "config": {"workload": wl.desc, "name": wl.name, "batch": s.B, "seq_len": s.L,
+                       "heads": s.H, "head_dim": s.d, "hidden": s.D, "vocab": s.V,
+                       "active_rows_per_step": sum(counts_per_set[0]),
+                       "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 1e6:.0f} MB "
+                             f"each (> 126 MB L2)",
+                       "parallelism": "replicas (one independent step per GPU)"},
             "roofline": roof, "kernels": kernels, "clocks": clocks.summary(),
-            "gpu_launches": LAUNCHES_PER_STEP * K, "timing": "K steps replayed as one CUDA graph", "e2e": e2e}
+            "gpu_launches": launches_per_step(wl, bf) * K,
+            "timing": f"{K} steps as {K // S} replays of a {S}-step CUDA graph", "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb, _, _ = cpu_baseline(s, args.cpu_seconds)
-        cb.pop("s_per_step", None)
+        cb, _, _ = cpu_baseline(wl, sets[0]["host"], args.cpu_seconds)
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -408,37 +663,38 @@ def main():
     return 0
 
 
-def e2e_run(dl, s, step, sets, stream, args, pg, device):
+def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev):
     """Same metric through the public API with pinned host buffers: H2D of the
     step's fresh inputs and D2H of its results inside the timed region."""
-    host_in = ["cur", "k_new", "v_new", "q", "logits"]
-    pinned = [{k: sets[i]["host"][k].pin_memory() for k in host_in} for i in range(N_SETS)]
+    host_in = ["cur", "k_new", "v_new", "q"] + (["logits"] if wl.conf is not None else [])
+    pinned = [{k: sets[i]["host"][k].pin_memory() for k in host_in} for i in range(n_sets)]
     out_host = {
-        "idx": torch.empty_like(step.idx, device="cpu").pin_memory(),
-        "count": torch.empty_like(step.count, device="cpu").pin_memory(),
-        "o": torch.empty_like(step.o, device="cpu").pin_memory(),
-        "lse": torch.empty_like(step.lse, device="cpu").pin_memory(),
-        "colsum": torch.empty_like(step.colsum, device="cpu").pin_memory(),
-        "score": torch.empty((s.B, s.L), dtype=torch.float32).pin_memory(),
-        "argmax": torch.empty_like(step.argmax, device="cpu").pin_memory(),
-        "length": torch.empty_like(step.length, device="cpu").pin_memory(),
+        "idx": torch.empty_like(bf.idx, device="cpu").pin_memory(),
+        "count": torch.empty_like(bf.count, device="cpu").pin_memory(),
+        "o": torch.empty_like(bf.o, device="cpu").pin_memory(),
+        "lse": torch.empty_like(bf.lse, device="cpu").pin_memory(),
+        "colsum": torch.empty_like(bf.colsum, device="cpu").pin_memory(),
+        "score": torch.empty((wl.shape.B, wl.shape.L), dtype=torch.float32).pin_memory(),
+        "argmax": torch.empty_like(bf.argmax, device="cpu").pin_memory(),
+        "length": torch.empty_like(bf.length, device="cpu").pin_memory(),
     }
     h2d = sum(t.numel() * t.element_size() for t in pinned[0].values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
     def one(i):
-        d = sets[i % N_SETS]
+        d = sets[i % n_sets]
         for k in host_in:
-            d[k].copy_(pinned[i % N_SETS][k], non_blocking=True)
-        run_step(dl, step, d, stream)
-        for k, src in (("idx", step.idx), ("count", step.count), ("o", step.o),
-                       ("lse", step.lse), ("colsum", step.colsum), ("score", d["score"]),
-                       ("argmax", step.argmax), ("length", step.length)):
+            dst = d[k][:, :pinned[i % n_sets][k].shape[1]] if k == "logits" else d[k]
+            dst.copy_(pinned[i % n_sets][k], non_blocking=True)
+        run_step(dl, wl, bf, d, stream)
+        for k, src in (("idx", bf.idx), ("count", bf.count), ("o", bf.o), ("lse", bf.lse),
+                       ("colsum", bf.colsum), ("score", d["score"]), ("argmax", bf.argmax),
+                       ("length", bf.length)):
             out_host[k].copy_(src, non_blocking=True)
 
     for i in range(max(args.warmup, 3)):
         one(i)
-    K = max(args.steps // 4, 10)
+    K = max(min(K_dev // 40, 500), 10)
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
@@ -453,7 +709,7 @@ def e2e_run(dl, s, step, sets, stream, args, pg, device):
         t = torch.tensor([ms], device=device)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
-    active = int(step.count.sum().item()) * (pg.get_world_size() if pg else 1)
+    active = int(bf.count.sum().item()) * (pg.get_world_size() if pg else 1)
     return {"value": active * K / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": ms / K}
 

@@ -244,6 +244,29 @@ dllm_status dllm_partial_attention(const void* q, const void* k_cache,
                                    int32_t* dev_status, void* stream);
 
 /*
+ * dllm_attention_colsum -- the per-key column sums alone, from a log-sum-exp
+ * computed earlier (the second normalised pass as a call of its own).
+ *
+ * Attn-Sampler, technical summary, Methodology 2: the column sums of the
+ * attention matrix over the active query rows, computed block by block
+ * without materialising the matrix.  colsum[b,h,j] = sum over i < count[b] of
+ * exp(scale <q_i, k_j> - lse[b,h,i]); with the lse that
+ * dllm_partial_attention wrote for the same q, k_cache and scale, this is
+ * exactly the colsum_out that call computes.
+ *
+ *   q, k_cache, count, scale, B, L, H, d, M_max  as in dllm_partial_attention.
+ *   lse         [B, H, M_max] float32 (rows < count[b] are read).
+ *   colsum_out  [B, H, L] float32, written for every j (zero when
+ *               count[b] == 0).
+ * Errors as dllm_partial_attention.
+ */
+dllm_status dllm_attention_colsum(const void* q, const void* k_cache, int dtype,
+                                  int B, int L, int H, int d, int M_max,
+                                  const int32_t* count, float scale,
+                                  const float* lse, float* colsum_out,
+                                  int32_t* dev_status, void* stream);
+
+/*
  * dllm_stable_prefix -- length of the longest stable block at the head of
  * the remaining active suffix.
  *

@@ -11,15 +11,14 @@ matmul / sum / exp / argmax as the only library steps.
 Pages cited (title, then section):
 
 * DyLLM -- "DyLLM: Efficient Diffusion LLM Inference via Saliency-based Token
-  Selection and Partial Attention" (gist.science/nl/paper/2603.08026).
+  Selection and Partial Attention".
 * SlowFast -- "Accelerating Diffusion Large Language Models with SlowFast
-  Sampling: The Three Golden Principles" (gist.science/it/paper/2506.10848).
-* Attn-Sampler -- "Attention-Based Sampler for Diffusion Language Models"
-  (gist.science/nl/paper/2604.08564).
+  Sampling: The Three Golden Principles".
+* Attn-Sampler -- "Attention-Based Sampler for Diffusion Language Models".
 * SureLock -- "Stopping Computation for Converged Tokens in Masked
-  Diffusion-LM Decoding" (gist.science/de/paper/2602.06412).
+  Diffusion-LM Decoding".
 * LSP -- "Beyond Scattered Acceptance: Fast and Coherent Inference for DLMs via
-  Longest Stable Prefixes" (gist.science/nl/paper/2603.05454).
+  Longest Stable Prefixes".
 
 Readings taken where the pages are silent (each is pinned or listed as
 unpinned in the tests): salient iff cos < tau, so cos == tau is stable and a

@@ -11,6 +11,7 @@ from ._lib import (  # noqa: F401
     DllmError,
     LIB_PATH,
     SIGNATURES,
+    dllm_attention_colsum,
     dllm_attention_workspace_bytes,
     dllm_confidence,
     dllm_confidence_workspace_bytes,

@@ -42,6 +42,7 @@ SIGNATURES = {
     "dllm_attention_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "dllm_partial_attention": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P,
                                     _SZ, _P, _P]),
+    "dllm_attention_colsum": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P]),
     "dllm_stable_prefix": (_I, [_P, _I, _I, _P, _F, _I, _I, _P, _P, _P]),
 }
 
@@ -250,6 +251,29 @@ def dllm_partial_attention(q, k_cache, v_cache, count, *, scale: float = 0.0, o_
                                       _ptr(lse_out), _ptr(colsum_out), _ptr(ws), ws_bytes,
                                       _ptr(dev_status), _stream(stream)))
     return o_out, lse_out, colsum_out
+
+
+def dllm_attention_colsum(q, k_cache, count, lse, *, scale: float = 0.0, colsum_out=None,
+                          dev_status=None, stream=None):
+    """Per-key column sums over the active rows from a given lse.
+
+    Returns colsum [B, H, L] f32.
+    """
+    lib = load_library()
+    dt = _dtype(q, k_cache)
+    B, M_max, H, d = q.shape
+    L = k_cache.shape[1]
+    _need(q, q.dtype, (B, M_max, H, d), "q")
+    _need(k_cache, q.dtype, (B, L, H, d), "k_cache")
+    _need(count, torch.int32, (B,), "count")
+    _need(lse, torch.float32, (B, H, M_max), "lse")
+    if colsum_out is None:
+        colsum_out = torch.empty((B, H, L), dtype=torch.float32, device=q.device)
+    _need(colsum_out, torch.float32, (B, H, L), "colsum_out")
+    _check(lib.dllm_attention_colsum(_ptr(q), _ptr(k_cache), dt, B, L, H, d, M_max, _ptr(count),
+                                     float(scale), _ptr(lse), _ptr(colsum_out), _ptr(dev_status),
+                                     _stream(stream)))
+    return colsum_out
 
 
 def dllm_stable_prefix(score, start, tau: float, *, min_commit: bool = True,

@@ -193,6 +193,29 @@ dllm_status dllm_partial_attention(const void* q, const void* k_cache, const voi
   return DLLM_OK;
 }
 
+dllm_status dllm_attention_colsum(const void* q, const void* k_cache, int dtype, int B, int L,
+                                  int H, int d, int M_max, const int32_t* count, float scale,
+                                  const float* lse, float* colsum_out, int32_t* dev_status,
+                                  void* stream) {
+  REQUIRE(q && k_cache && count && lse && colsum_out,
+          "dllm_attention_colsum: NULL pointer argument");
+  REQUIRE(valid_dtype(dtype), "dllm_attention_colsum: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && L >= 1 && H >= 1 && M_max >= 1,
+          "dllm_attention_colsum: B=%d L=%d H=%d M_max=%d must be >= 1", B, L, H, M_max);
+  REQUIRE(B <= 65535 && H <= 65535, "dllm_attention_colsum: B or H above 65535");
+  if (d != 32 && d != 64 && d != 128)
+    return fail(DLLM_ERR_UNSUPPORTED, "dllm_attention_colsum: head dim %d not in {32,64,128}", d);
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)d);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dllm::attention_tc_supported(dtype, d, q, k_cache, k_cache, q))
+    return from_cuda(dllm::launch_colsum_tc(q, k_cache, B, L, H, M_max, count, scale, lse,
+                                            colsum_out, dev_status, s),
+                     "dllm_attention_colsum launch");
+  return from_cuda(dllm::launch_colsum_simt(q, k_cache, dtype, B, L, H, d, M_max, count, scale,
+                                            lse, colsum_out, dev_status, s),
+                   "dllm_attention_colsum launch");
+}
+
 dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start, float tau,
                                int min_commit, int advance_start, int32_t* len_out,
                                int32_t* dev_status, void* stream) {

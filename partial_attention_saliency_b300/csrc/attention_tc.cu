@@ -742,8 +742,6 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
                                 cudaStream_t stream) {
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_fwd_tc_kernel),
                                     (int)kFwdSmem);
-  if (e == cudaSuccess)
-    e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel), (int)kCsSmem);
   if (e != cudaSuccess) return e;
   CUtensorMap tq, tk, tv;
   if (!make_rows_map(&tq, q, B, M_max, H) || !make_rows_map(&tk, k, B, L, H) ||
@@ -776,6 +774,18 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
     if (e != cudaSuccess) return e;
   }
   if (colsum == nullptr) return cudaSuccess;
+  return launch_colsum_tc(q, k, B, L, H, M_max, count, scale, lse, colsum, dev_status, stream);
+}
+
+cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, int M_max,
+                             const int32_t* count, float scale, const float* lse, float* colsum,
+                             int32_t* dev_status, cudaStream_t stream) {
+  cudaError_t e =
+      ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel), (int)kCsSmem);
+  if (e != cudaSuccess) return e;
+  CUtensorMap tq, tk;
+  if (!make_rows_map(&tq, q, B, M_max, H) || !make_rows_map(&tk, k, B, L, H))
+    return cudaErrorInvalidValue;
   ColsumParams cp{count, lse, colsum, L, H, M_max, scale * kLog2e, dev_status};
   dim3 cgrid((L + kBN - 1) / kBN, H, B);
   attn_colsum_tc_kernel<<<cgrid, kThreads, kCsSmem, stream>>>(tq, tk, cp);

@@ -45,6 +45,10 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
                                 float* colsum, void* ws, size_t ws_bytes, int32_t* dev_status,
                                 cudaStream_t stream);
 
+cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, int M_max,
+                             const int32_t* count, float scale, const float* lse, float* colsum,
+                             int32_t* dev_status, cudaStream_t stream);
+
 cudaError_t launch_colsum_simt(const void* q, const void* k, int dtype, int B, int L, int H,
                                int d, int M_max, const int32_t* count, float scale,
                                const float* lse, float* colsum, int32_t* dev_status,

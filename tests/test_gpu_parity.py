@@ -338,6 +338,25 @@ def test_attention_batch8_sampled_heads(dl):
         assert np.max(np.abs(gc[b, h] - rc[0, 0])) <= SCORE_TOL
 
 
+@pytest.mark.parametrize("dtype,d", [(torch.bfloat16, 128), (torch.bfloat16, 64), (torch.float32, 32)])
+def test_attention_colsum_call_matches_fused(dl, dtype, d):
+    # the column-sum pass as a call of its own reproduces the fused colsum_out
+    # bit for bit and matches the oracle
+    B, M_max, L, H = 2, 200, 517, 3
+    counts = [200, 61]
+    g = torch.Generator().manual_seed(31 + d)
+    q = workloads.normal(g, (B, M_max, H, d), 1.0, dtype)
+    k = workloads.normal(g, (B, L, H, d), 1.0, dtype)
+    v = workloads.normal(g, (B, L, H, d), 1.0, dtype)
+    cnt = dev(torch.tensor(counts, dtype=torch.int32))
+    o, lse, cs = dl.dllm_partial_attention(dev(q), dev(k), dev(v), cnt)
+    cs2 = dl.dllm_attention_colsum(dev(q), dev(k), cnt, lse)
+    torch.cuda.synchronize()
+    assert torch.equal(cs, cs2)
+    _, _, rc = oracle.partial_attention(f64(q), f64(k), f64(v), counts)
+    assert np.max(np.abs(f64(cs2) - rc)) <= SCORE_TOL
+
+
 # ------------------------------------------------------------------ stable prefix
 
 def test_stable_prefix_brute_force(dl):
