@@ -46,17 +46,27 @@ constexpr int kBM = 128;       // query rows per tile
 constexpr int kBN = 128;       // keys per tile
 constexpr int kHD = 128;       // head dim
 constexpr int kStages = 2;     // K/V (forward) or Q (column sums) ring depth
-constexpr int kThreads = 192;  // 6 warps
+constexpr int kThreads = 192;  // column-sum kernel: 6 warps
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-dim bf16 box (swizzled)
 constexpr uint32_t kTile = 2 * kBox;      // 128 rows x 128 dims
 constexpr float kRescaleThreshold = 8.0f; // log2 units: P stays below 2^8
+
+// Forward kernel roles: warps 0-3 softmax of query tile A, warps 4-7 softmax
+// of query tile B (warp w reads TMEM lanes 32 * (w % 4) .. + 31), warp 8 TMA
+// producer, warp 9 MMA issuer.
+constexpr int kFwdThreads = 320;
+constexpr int kWarpTma = 8;
+constexpr int kWarpMma = 9;
+// Exponentials on the FMA pipe instead of MUFU: pairs c with (c % 4) == 3,
+// a quarter of them, so that MUFU keeps pace with the tensor cores.
+constexpr int kPolyEvery = 4;
 
 struct FwdParams {
   const int32_t* count;
   __nv_bfloat16* o;
   float* lse;
-  float* ws_o;   // split partials: [item][128 rows][128 dims] unnormalised O
-  float* ws_ml;  // split partials: [item][128 rows][2] = (running max (log2 units), sum)
+  float* ws_o;   // split partials: [item][2 tiles][128 rows][128 dims] unnormalised O
+  float* ws_ml;  // split partials: [item][2 tiles][128 rows][2] = (max (log2 units), sum)
   int B, L, H, M_max;
   int max_split_items;  // capacity of the workspace in items (0: never split)
   float scale_log2;
@@ -73,11 +83,16 @@ struct ColsumParams {
 };
 
 // shared-memory map of the forward kernel (offsets from a 1024-aligned base)
-constexpr uint32_t kFwdQ = 0;
-constexpr uint32_t kFwdK = kTile;                         // + s * 2 * kTile
-constexpr uint32_t kFwdP = kTile + kStages * 2 * kTile;   // 160 KB
-constexpr uint32_t kFwdBar = kFwdP + kTile;               // 192 KB
+constexpr uint32_t kFwdQ = 0;                              // Q tile A, then Q tile B
+constexpr uint32_t kFwdKV = 2 * kTile;                     // + s * 2 * kTile: K, then V
+constexpr uint32_t kFwdBar = kFwdKV + kStages * 2 * kTile; // 192 KB
 constexpr uint32_t kFwdSmem = kFwdBar + 256 + 1024;
+
+// tensor-memory columns of the forward kernel (512 allocated): scores S of
+// tile A and B (P overwrites the first 64 columns of its S as bf16 pairs),
+// then the O accumulators of A and B
+constexpr uint32_t kTmS = 0;     // + X * 128
+constexpr uint32_t kTmO = 256;   // + X * 128
 
 // shared-memory map of the column-sum kernel
 constexpr uint32_t kCsK = 0;
@@ -86,16 +101,10 @@ constexpr uint32_t kCsLse = kTile + kStages * kTile;      // 2 x 128 floats
 constexpr uint32_t kCsBar = kCsLse + 2 * kBM * 4;
 constexpr uint32_t kCsSmem = kCsBar + 256 + 1024;
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-               "r"(d)
-               : "memory");
-}
-
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Bounded wait whose outcome is the same for every lane of the warp (the
@@ -105,18 +114,48 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, r);
 }
 
-// Named barrier among the four softmax / epilogue warps (ids 2-5).
+// Named barrier among the four column-sum warps (ids 2-5).
 __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x for a pair on the FMA pipe (x <= 128): Cody-Waite split x = n + f with
+// n = round(x) (the 1.5 * 2^23 shifter), f in [-1/2, 1/2]; 2^f from a degree-4
+// polynomial (relative-error minimax fit of 2^f on [-1/2, 1/2] made for this
+// library by iteratively reweighted least squares; max relative error
+// 2.7e-6 evaluated in float32); 2^n added to the exponent field.  x is clamped
+// at -125, so arguments below it give 2^-125 (about 2e-38) instead of 0.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 shifter = make_float2(12582912.0f, 12582912.0f);
+  const float2 t = __fadd2_rn(x, shifter);
+  const float2 n = __fadd2_rn(t, make_float2(-12582912.0f, -12582912.0f));
+  const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
+  float2 p = make_float2(0x1.3997cap-7f, 0x1.3997cap-7f);
+  p = __ffma2_rn(p, f, make_float2(0x1.ca1442p-5f, 0x1.ca1442p-5f));
+  p = __ffma2_rn(p, f, make_float2(0x1.ec06dap-3f, 0x1.ec06dap-3f));
+  p = __ffma2_rn(p, f, make_float2(0x1.62e0dcp-1f, 0x1.62e0dcp-1f));
+  p = __ffma2_rn(p, f, make_float2(0x1.ffffe8p-1f, 0x1.ffffe8p-1f));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
 // Work plan shared by the forward and merge kernels, computed on the device
-// from the active counts: query tiles of 128 active rows per (batch, head);
-// when there are fewer tiles than CTAs the key range of each tile is split
-// so that every SM gets work.
+// from the active counts.  A work item is a pair of query tiles of 128
+// active rows (tile A, and tile B when the head has one more tile) of one
+// (batch row, head), optionally limited to a slice of the key range: when
+// there are fewer pairs than CTAs the key range of each pair is split so
+// that every SM gets work.
 struct FwdPlan {
-  int total_qt;  // query tiles over all (b, h)
-  int nsplit;    // key-range splits per query tile
+  int total_qp;  // tile pairs over all (b, h)
+  int nsplit;    // key-range splits per pair
   int tps;       // key tiles per split
   int nkt;       // key tiles of the sequence
 };
@@ -126,18 +165,20 @@ __device__ __forceinline__ int clamp_count(const int32_t* count, int b, int M_ma
   return n < 0 ? 0 : (n > M_max ? M_max : n);
 }
 
+__device__ __forceinline__ int pairs_of(int n) { return (((n + kBM - 1) / kBM) + 1) / 2; }
+
 __device__ FwdPlan make_plan(const FwdParams& p, int n_ctas) {
   FwdPlan pl;
   pl.nkt = (p.L + kBN - 1) / kBN;
-  int qt = 0;
-  for (int b = 0; b < p.B; ++b) qt += p.H * ((clamp_count(p.count, b, p.M_max) + kBM - 1) / kBM);
-  pl.total_qt = qt;
+  int qp = 0;
+  for (int b = 0; b < p.B; ++b) qp += p.H * pairs_of(clamp_count(p.count, b, p.M_max));
+  pl.total_qp = qp;
   int ns = 1;
-  if (qt > 0 && qt < n_ctas && p.max_split_items > 0) {
-    ns = (n_ctas + qt - 1) / qt;
+  if (qp > 0 && qp < n_ctas && p.max_split_items > 0) {
+    ns = (n_ctas + qp - 1) / qp;
     const int max_by_tiles = pl.nkt / 2 > 1 ? pl.nkt / 2 : 1;  // at least two key tiles each
     ns = ns < max_by_tiles ? ns : max_by_tiles;
-    const int max_by_ws = p.max_split_items / qt;
+    const int max_by_ws = p.max_split_items / qp;
     ns = ns < max_by_ws ? ns : max_by_ws;
     if (ns < 1) ns = 1;
   }
@@ -146,26 +187,37 @@ __device__ FwdPlan make_plan(const FwdParams& p, int n_ctas) {
   return pl;
 }
 
-// Query tile index qi -> (b, h, tile) in batch-major, head-major order.
-__device__ __forceinline__ void decode_qtile(const FwdParams& p, int qi, int* b, int* h, int* t) {
+// Pair index qi -> (b, h, pair, query tiles in the pair), batch-major then
+// head-major.
+__device__ __forceinline__ void decode_pair(const FwdParams& p, int qi, int* b, int* h,
+                                            int* pair, int* nq) {
   for (int bb = 0; bb < p.B; ++bb) {
-    const int per_head = (clamp_count(p.count, bb, p.M_max) + kBM - 1) / kBM;
-    const int n = per_head * p.H;
-    if (qi < n) {
+    const int n = clamp_count(p.count, bb, p.M_max);
+    const int nqt = (n + kBM - 1) / kBM;
+    const int per_head = (nqt + 1) / 2;
+    if (qi < per_head * p.H) {
       *b = bb;
       *h = qi / per_head;
-      *t = qi - *h * per_head;
+      *pair = qi - *h * per_head;
+      *nq = min(2, nqt - 2 * *pair);
       return;
     }
-    qi -= n;
+    qi -= per_head * p.H;
   }
-  *b = *h = *t = 0;
+  *b = *h = *pair = 0;
+  *nq = 0;
 }
 
-// Persistent forward kernel: one CTA per SM walks the work items (query tile,
-// key-range split) round-robin; the TMA, MMA and softmax roles keep their
-// pipeline phases across items.
-__global__ void __launch_bounds__(kThreads, 1)
+// Persistent forward kernel: one CTA per SM walks the work items round-robin.
+// Per key tile t the MMA warp issues, in this order,
+//   O_A += P_A(t) V(t),  S_A = Q_A K(t+1)^T,  O_B += P_B(t) V(t),  S_B = Q_B K(t+1)^T
+// so that the tensor cores work on one tile while the softmax warps of the
+// other tile compute its probabilities.  P overwrites the S it came from in
+// tensor memory and feeds the P V product from there.  Because tcgen05
+// operations of one thread complete in issue order, "S_X(t+1) is full"
+// also means O_X += P_X(t) V(t) has completed, so the softmax warps may
+// rescale O_X in place when their running maximum grows.
+__global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, FwdParams p) {
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -173,27 +225,25 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (p.count[b] < 0 || p.count[b] > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
   }
   const FwdPlan plan = make_plan(p, gridDim.x);
-  const int n_items = plan.total_qt * plan.nsplit;
+  const int n_items = plan.total_qp * plan.nsplit;
   if ((int)blockIdx.x >= n_items) return;
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_addr);
-  const uint32_t sQ = base + kFwdQ, sP = base + kFwdP;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kFwdBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
   uint64_t* kv_full = bars + 2;   // [kStages]
   uint64_t* kv_empty = bars + 4;  // [kStages]
-  uint64_t* s_full = bars + 6;    // [2]
-  uint64_t* s_free = bars + 8;    // [2]
-  uint64_t* p_full = bars + 10;
-  uint64_t* o_ready = bars + 11;
-  uint64_t* o_free = bars + 12;
-  uint64_t* mma_done = bars + 13;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
-  int* abort_flag = reinterpret_cast<int*>(bars + 15);
+  uint64_t* s_full = bars + 6;    // [2]: S of tile A / B written
+  uint64_t* p_full = bars + 8;    // [2]: P of tile A / B written (4 warps each)
+  uint64_t* o_done = bars + 10;   // [2]: last P V of the item completed
+  uint64_t* o_free = bars + 12;   // [2]: epilogue has read O (4 warps each)
+  uint64_t* mma_done = bars + 14;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  int* abort_flag = reinterpret_cast<int*>(bars + 16);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -203,25 +253,24 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_init(&kv_full[s], 1);
       mbar_init(&kv_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&p_full[x], 4);
+      mbar_init(&o_done[x], 1);
+      mbar_init(&o_free[x], 4);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_ready, 1);
-    mbar_init(o_free, 4);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 512);
+  if (warp == kWarpTma) tmem_alloc(tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S0: +0, S1: +128, O: +256
+  const uint32_t tmem = *tmem_slot;
   volatile int* abort = abort_flag;
 
-  if (warp == 0) {
+  if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
@@ -230,22 +279,25 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       int j = 0, g = 0;
       bool ok = true;
       for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
-        int b, h, qt;
-        decode_qtile(p, v / plan.nsplit, &b, &h, &qt);
+        int b, h, pair, nq;
+        decode_pair(p, v / plan.nsplit, &b, &h, &pair, &nq);
         const int split = v % plan.nsplit;
         const int kt0 = split * plan.tps;
         const int nt = min(plan.tps, plan.nkt - kt0);
         if (j > 0 && !mbar_wait(q_empty, (j - 1) & 1, abort)) break;
-        mbar_expect_tx(q_full, kTile);
-        tma_load_4d(gbase + kFwdQ, &tq, q_full, 0, h, qt * kBM, b);
-        tma_load_4d(gbase + kFwdQ + kBox, &tq, q_full, 64, h, qt * kBM, b);
+        mbar_expect_tx(q_full, (uint32_t)nq * kTile);
+        for (int x = 0; x < nq; ++x) {
+          const int row0 = (2 * pair + x) * kBM;
+          tma_load_4d(gbase + kFwdQ + x * kTile, &tq, q_full, 0, h, row0, b);
+          tma_load_4d(gbase + kFwdQ + x * kTile + kBox, &tq, q_full, 64, h, row0, b);
+        }
         for (int t = 0; t < nt; ++t, ++g) {
           const int s = g % kStages;
           if (g >= kStages && !mbar_wait(&kv_empty[s], ((g / kStages) - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          uint8_t* kdst = gbase + kFwdK + s * 2 * kTile;
+          uint8_t* kdst = gbase + kFwdKV + s * 2 * kTile;
           uint8_t* vdst = kdst + kTile;
           const int key0 = (kt0 + t) * kBN;
           mbar_expect_tx(&kv_full[s], 2 * kTile);
@@ -261,66 +313,76 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       for (int k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
         mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &none);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       const uint32_t id_pv = idesc_bf16_f32(kBM, kHD, false, true);
-      auto issue_qk = [&](int g) -> bool {
-        const int s = g % kStages, sb = g & 1;
-        if (!mbar_wait(&kv_full[s], (g / kStages) & 1, abort)) return false;
-        if (g >= 2 && !mbar_wait(&s_free[sb], ((g >> 1) - 1) & 1, abort)) return false;
-        tc_fence_after();
-        const uint32_t sK = base + kFwdK + s * 2 * kTile;
+      auto issue_qk = [&](int x, int s) {
+        const uint32_t sQ = base + kFwdQ + x * kTile;
+        const uint32_t sK = base + kFwdKV + s * 2 * kTile;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + sb * kBN, smem_desc_sw128(sQ + off, 16, 1024),
+          mma_bf16_ss(tmem + kTmS + x * kBN, smem_desc_sw128(sQ + off, 16, 1024),
                       smem_desc_sw128(sK + off, 16, 1024), id_qk, kk > 0);
         }
-        mma_commit(&s_full[sb]);
-        return true;
+        mma_commit(&s_full[x]);
       };
-      int j = 0, g = 0;
+      auto issue_pv = [&](int x, int s, bool acc) {
+        const uint32_t sV = base + kFwdKV + s * 2 * kTile + kTile;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_bf16_ts(tmem + kTmO + x * kHD, tmem + kTmS + x * kBN + kk * 8,
+                      smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), id_pv,
+                      (acc || kk > 0) ? 1u : 0u);
+      };
+      int j = 0, g = 0;          // items, K/V tiles
+      int gt[2] = {0, 0};        // tiles processed per query tile slot
+      int jt[2] = {0, 0};        // items processed per query tile slot
       bool ok = true;
       for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
+        int b, h, pair, nq;
+        decode_pair(p, v / plan.nsplit, &b, &h, &pair, &nq);
         const int split = v % plan.nsplit;
         const int nt = min(plan.tps, plan.nkt - split * plan.tps);
         if (!mbar_wait(q_full, j & 1, abort)) break;
-        const int g0 = g;
-        if (!issue_qk(g0)) break;
-        for (int t = 0; t < nt; ++t) {
-          const int gg = g0 + t;
-          if (t + 1 < nt) {
-            if (!issue_qk(gg + 1)) {
+        if (!mbar_wait(&kv_full[g % kStages], (g / kStages) & 1, abort)) break;
+        tc_fence_after();
+        for (int x = 0; x < nq; ++x) issue_qk(x, g % kStages);
+        if (nt == 1) mma_commit(q_empty);
+        for (int t = 0; t < nt && ok; ++t) {
+          const int s = (g + t) % kStages;
+          const int s1 = (g + t + 1) % kStages;
+          const bool more = t + 1 < nt;
+          for (int x = 0; x < nq; ++x) {
+            if (!mbar_wait(&p_full[x], gt[x] & 1, abort)) {
               ok = false;
               break;
             }
-          } else {
-            mma_commit(q_empty);  // the last QK^T of the item is issued: Q may be replaced
+            if (t == 0 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(x, s, t > 0);
+            if (x == nq - 1) mma_commit(&kv_empty[s]);  // V(t) (and K(t)) no longer read
+            if (more) {
+              if (x == 0 && !mbar_wait(&kv_full[s1], ((g + t + 1) / kStages) & 1, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_qk(x, s1);
+              if (x == nq - 1 && t + 2 == nt) mma_commit(q_empty);  // last read of Q
+            } else {
+              mma_commit(&o_done[x]);
+            }
+            ++gt[x];
           }
-          if (!mbar_wait(p_full, gg & 1, abort)) {
-            ok = false;
-            break;
-          }
-          if (t == 0 && j > 0 && !mbar_wait(o_free, (j - 1) & 1, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const int s = gg % kStages;
-          const uint32_t sV = base + kFwdK + s * 2 * kTile + kTile;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk) {
-            const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_bf16_ss(tmem + 2 * kBN, smem_desc_sw128(sP + aoff, 16, 1024),
-                        smem_desc_sw128(sV + kk * 16 * 128, kBox, 1024), id_pv,
-                        (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(o_ready);
-          mma_commit(&kv_empty[s]);
         }
-        g = g0 + nt;
+        g += nt;
+        for (int x = 0; x < nq; ++x) ++jt[x];
       }
       // Every MMA issued above completes before the tensor memory is freed.
       mma_commit(mma_done);
@@ -329,111 +391,135 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else {
     // ------------------------------------------------------------ softmax warps
+    const int x = warp >> 2;           // query tile slot: 0 = A, 1 = B
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
+    const int r = quarter * 32 + lane;  // row of the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const uint32_t tS = tmem + lane_base + kTmS + x * kBN;
+    const uint32_t tO = tmem + lane_base + kTmO + x * kHD;
     const float sl2 = p.scale_log2;
-    int j = 0, g = 0;
+    int gx = 0, jx = 0;
     bool ok = true;
-    for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
-      int b, h, qt;
-      decode_qtile(p, v / plan.nsplit, &b, &h, &qt);
+    for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x) {
+      int b, h, pair, nq;
+      decode_pair(p, v / plan.nsplit, &b, &h, &pair, &nq);
+      if (x >= nq) continue;
       const int split = v % plan.nsplit;
       const int kt0 = split * plan.tps;
       const int nt = min(plan.tps, plan.nkt - kt0);
       float m = -INFINITY, l = 0.f;
-      for (int t = 0; t < nt; ++t) {
-        const int gg = g + t;
-        const int sb = gg & 1;
-        if (!warp_wait(&s_full[sb], (gg >> 1) & 1, abort)) {
+      for (int t = 0; t < nt; ++t, ++gx) {
+        if (!warp_wait(&s_full[x], gx & 1, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        uint32_t raw[kBN];
-#pragma unroll
-        for (int c = 0; c < kBN / 32; ++c)
-          tmem_ld_32x32b_x32(tmem + lane_base + sb * kBN + c * 32,
-                             *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[sb]);
-
-        const int kvalid = min(kBN, p.L - (kt0 + t) * kBN);
-        float sv[kBN];
+        // Pass 1: the row maximum over the tile (S stays in tensor memory).
+        const int kvalid = p.L - (kt0 + t) * kBN;  // < kBN only on the last, partial tile
         float mx = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < kBN; ++jj) {
-          const float sc = (jj < kvalid) ? __uint_as_float(raw[jj]) * sl2 : -INFINITY;
-          sv[jj] = sc;
-          mx = fmaxf(mx, sc);
-        }
-        const float m_new = fmaxf(m, mx);
-        const bool grow = m_new > m + kRescaleThreshold;
-        const float m_use = grow ? m_new : m;
-        // P V of the previous tile must be done: the P buffer is reused and O
-        // may be rescaled below.
-        if (t > 0 && !warp_wait(o_ready, (gg - 1) & 1, abort)) {
-          ok = false;
-          break;
-        }
-        if (grow) {
-          const float alpha = ex2_approx(m - m_use);
-          l *= alpha;
-          if (t > 0) {
-            tc_fence_after();
-#pragma unroll 1
-            for (int c = 0; c < kHD / 32; ++c) {
-              uint32_t ov[32];
-              tmem_ld_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
-              tmem_ld_wait();
+        for (int c = 0; c < kBN / 64; ++c) {
+          uint32_t ra[32], rb[32];
+          tmem_ld_32x32b_x32(tS + c * 64, ra);
+          tmem_ld_32x32b_x32(tS + c * 64 + 32, rb);
+          tmem_ld_wait();
+          if (kvalid < kBN) {  // warp-uniform
 #pragma unroll
-              for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha);
-              tmem_st_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
+            for (int q = 0; q < 32; ++q) {
+              if (c * 64 + q >= kvalid) ra[q] = 0xff800000u;  // -inf
+              if (c * 64 + 32 + q >= kvalid) rb[q] = 0xff800000u;
             }
-            tmem_st_wait();
+          }
+#pragma unroll
+          for (int q = 0; q < 32; q += 2)
+            mx = fmax3(mx, fmaxf(__uint_as_float(ra[q]), __uint_as_float(ra[q + 1])),
+                       fmaxf(__uint_as_float(rb[q]), __uint_as_float(rb[q + 1])));
+        }
+        const float m_new = fmaxf(m, mx * sl2);
+        const bool grow = m_new > m + kRescaleThreshold;
+        const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
+        if (grow) {
+          l *= alpha;
+          m = m_new;
+        }
+        // Pass 2: P = 2^(s * scale * log2 e - m) in bf16 pairs over the first
+        // 64 columns of S.  Chunk c reads S columns [32c, 32c + 32) and writes
+        // P columns [16c, 16c + 16), which were read in chunk c / 2 <= c.
+        const float2 sl2x2 = make_float2(sl2, sl2);
+        const float2 negm = make_float2(-m, -m);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int c = 0; c < kBN / 32; ++c) {
+          uint32_t raw[32];
+          tmem_ld_32x32b_x32(tS + c * 32, raw);
+          tmem_ld_wait();
+          if (kvalid < kBN) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if (c * 32 + q >= kvalid) raw[q] = 0xff800000u;
+          }
+          uint32_t pk[16];
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const float2 a = __ffma2_rn(
+                make_float2(__uint_as_float(raw[2 * cc]), __uint_as_float(raw[2 * cc + 1])),
+                sl2x2, negm);
+            float2 e;
+            if (cc % kPolyEvery == kPolyEvery - 1) {
+              e = exp2_poly2(a);
+            } else {
+              e.x = ex2_approx(a.x);
+              e.y = ex2_approx(a.y);
+            }
+            if (cc & 1)
+              acc1 = __fadd2_rn(acc1, e);
+            else
+              acc0 = __fadd2_rn(acc0, e);
+            pk[cc] = pack_bf16(e.x, e.y);
+          }
+          tmem_st_32x32b_x16(tS + c * 16, pk);
+        }
+        // O is rescaled in place when some row's maximum grew (tcgen05.ld/st
+        // are warp-collective, so the warp votes; rows that did not grow
+        // multiply by 1).  O of the first tile of an item is written without
+        // accumulation and needs none.
+        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+#pragma unroll 1
+          for (int c = 0; c < kHD / 32; ++c) {
+            uint32_t ov[32];
+            tmem_ld_32x32b_x32(tO + c * 32, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * alpha);
+            tmem_st_32x32b_x32(tO + c * 32, ov);
           }
         }
-        float sum = 0.f;
-#pragma unroll
-        for (int c = 0; c < kBN / 8; ++c) {
-          float e[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            e[k] = ex2_approx(sv[c * 8 + k] - m_use);
-            sum += e[k];
-          }
-          const uint32_t addr = sP + (c >> 3) * kBox + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
-          st_shared_v4(addr, pack_bf16(e[0], e[1]), pack_bf16(e[2], e[3]), pack_bf16(e[4], e[5]),
-                       pack_bf16(e[6], e[7]));
-        }
-        l += sum;
-        m = m_use;
-        fence_proxy_async_smem();
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(p_full);
+        if (lane == 0) mbar_arrive(&p_full[x]);
+        l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
-      if (!ok || !warp_wait(o_ready, (g + nt - 1) & 1, abort)) {
+      if (!ok || !warp_wait(&o_done[x], jx & 1, abort)) {
         ok = false;
         break;
       }
-      g += nt;
+      ++jx;
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
       const int n = clamp_count(p.count, b, p.M_max);
-      const int i = qt * kBM + r;
+      const int i = (2 * pair + x) * kBM + r;
       const bool store = i < n;
       const bool partial = plan.nsplit > 1;
       const float inv = partial ? 1.0f : 1.0f / l;
+      const int64_t slot = (int64_t)v * 2 + x;  // workspace tile slot
       __nv_bfloat16* orow =
           p.o + ((int64_t)b * p.M_max + i) * ((int64_t)p.H * kHD) + (int64_t)h * kHD;
-      float* prow = p.ws_o + ((int64_t)v * kBM + r) * kHD;
+      float* prow = p.ws_o + (slot * kBM + r) * kHD;
 #pragma unroll 1
       for (int c = 0; c < kHD / 32; ++c) {
         uint32_t ov[32];
-        tmem_ld_32x32b_x32(tmem + lane_base + 2 * kBN + c * 32, ov);
+        tmem_ld_32x32b_x32(tO + c * 32, ov);
         tmem_ld_wait();
         if (store && partial) {
           float4* dst = reinterpret_cast<float4*>(prow + c * 32);
@@ -457,11 +543,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       // O is read: the next item's first P V may overwrite it.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(o_free);
+      if (lane == 0) mbar_arrive(&o_free[x]);
       if (store) {
         if (partial) {
-          p.ws_ml[((int64_t)v * kBM + r) * 2 + 0] = m;
-          p.ws_ml[((int64_t)v * kBM + r) * 2 + 1] = l;
+          p.ws_ml[(slot * kBM + r) * 2 + 0] = m;
+          p.ws_ml[(slot * kBM + r) * 2 + 1] = l;
         } else if (p.lse != nullptr) {
           p.lse[((int64_t)b * p.H + h) * p.M_max + i] = (m + log2f(l)) * 0.69314718055994531f;
         }
@@ -471,7 +557,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kWarpTma) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -506,25 +592,27 @@ attn_split_merge_kernel(FwdParams p, int n_ctas) {
       const int nb = clamp_count(p.count, b, p.M_max);
       if (rem < nb) break;
       rem -= nb;
-      qi += p.H * ((nb + kBM - 1) / kBM);
+      qi += p.H * pairs_of(nb);
     }
     const int i = rem;
     const int n = clamp_count(p.count, b, p.M_max);
-    const int per_head = (n + kBM - 1) / kBM;
-    qi += h * per_head + i / kBM;
+    qi += h * pairs_of(n) + i / (2 * kBM);
+    const int x = (i / kBM) & 1;
     const int r = i % kBM;
     float M = -INFINITY;
-    for (int s = 0; s < plan.nsplit; ++s)
-      M = fmaxf(M, p.ws_ml[(((int64_t)qi * plan.nsplit + s) * kBM + r) * 2]);
+    for (int s = 0; s < plan.nsplit; ++s) {
+      const int64_t slot = ((int64_t)qi * plan.nsplit + s) * 2 + x;
+      M = fmaxf(M, p.ws_ml[(slot * kBM + r) * 2]);
+    }
     float l = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < plan.nsplit; ++s) {
-      const int64_t item = (int64_t)qi * plan.nsplit + s;
-      const float ms = p.ws_ml[(item * kBM + r) * 2];
-      const float ls = p.ws_ml[(item * kBM + r) * 2 + 1];
+      const int64_t slot = ((int64_t)qi * plan.nsplit + s) * 2 + x;
+      const float ms = p.ws_ml[(slot * kBM + r) * 2];
+      const float ls = p.ws_ml[(slot * kBM + r) * 2 + 1];
       const float wgt = ex2_approx(ms - M);
       l += wgt * ls;
-      const float4 o4 = reinterpret_cast<const float4*>(p.ws_o + (item * kBM + r) * kHD)[lane];
+      const float4 o4 = reinterpret_cast<const float4*>(p.ws_o + (slot * kBM + r) * kHD)[lane];
       acc[0] = fmaf(wgt, o4.x, acc[0]);
       acc[1] = fmaf(wgt, o4.y, acc[1]);
       acc[2] = fmaf(wgt, o4.z, acc[2]);
@@ -732,8 +820,9 @@ bool attention_tc_supported(int dtype, int d, const void* q, const void* k, cons
 }
 
 size_t attention_tc_workspace_bytes(int n_ctas) {
-  // 2 x n_ctas split items of 128 rows: unnormalised O (128 floats) + (max, sum)
-  return (size_t)2 * n_ctas * kBM * (kHD + 2) * sizeof(float);
+  // at most 2 x n_ctas split items of two 128-row tiles: unnormalised O (128
+  // floats) + (max, sum) per row
+  return (size_t)2 * n_ctas * 2 * kBM * (kHD + 2) * sizeof(float);
 }
 
 cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int B, int L, int H,
@@ -756,7 +845,7 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
   fp.o = static_cast<__nv_bfloat16*>(o);
   fp.lse = lse;
   fp.ws_o = can_split ? static_cast<float*>(ws) : nullptr;
-  fp.ws_ml = can_split ? static_cast<float*>(ws) + (size_t)2 * n_ctas * kBM * kHD : nullptr;
+  fp.ws_ml = can_split ? static_cast<float*>(ws) + (size_t)2 * n_ctas * 2 * kBM * kHD : nullptr;
   fp.B = B;
   fp.L = L;
   fp.H = H;
@@ -764,7 +853,7 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
   fp.max_split_items = can_split ? 2 * n_ctas : 0;
   fp.scale_log2 = scale * kLog2e;
   fp.dev_status = dev_status;
-  attn_fwd_tc_kernel<<<n_ctas, kThreads, kFwdSmem, stream>>>(tq, tk, tv, fp);
+  attn_fwd_tc_kernel<<<n_ctas, kFwdThreads, kFwdSmem, stream>>>(tq, tk, tv, fp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (can_split) {

@@ -339,6 +339,24 @@ __device__ __forceinline__ uint4 ld_shared16(uint32_t addr) {
   return r;
 }
 
+// Whether any element of the 16-byte vector equals m (m is not NaN).
+template <typename T>
+__device__ __forceinline__ bool vec_contains(const uint4& v, float m) {
+  if constexpr (std::is_same<T, float>::value) {
+    return __uint_as_float(v.x) == m || __uint_as_float(v.y) == m ||
+           __uint_as_float(v.z) == m || __uint_as_float(v.w) == m;
+  } else {
+    const __nv_bfloat162 a = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.x),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    const __nv_bfloat162 c = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&v.z),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&v.w));
+    const __nv_bfloat162 mx = __hmax2(a, c);
+    // m is the maximum of a set that contains these elements, so equality
+    // with the vector's maximum is the test
+    return fmaxf(__bfloat162float(mx.x), __bfloat162float(mx.y)) == m;
+  }
+}
+
 struct Top2Sum {
   float m1, m2, l;
 };
@@ -502,10 +520,15 @@ conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, i
     const int nvec = ok ? max(0, min(SE, V - s0)) / E : 0;
     const uint32_t sbase = base + stage * kStreamChunkBytes + warp * kStreamSliceBytes;
     uint4 x[kStreamVPL];
+    if (nvec == kStreamVPL * 32) {  // full slice: no bounds test per vector
 #pragma unroll
-    for (int u = 0; u < kStreamVPL; ++u) {
-      const int vi = u * 32 + lane;
-      x[u] = vi < nvec ? ld_shared16(sbase + vi * 16) : make_uint4(sent, sent, sent, sent);
+      for (int u = 0; u < kStreamVPL; ++u) x[u] = ld_shared16(sbase + (u * 32 + lane) * 16);
+    } else {
+#pragma unroll
+      for (int u = 0; u < kStreamVPL; ++u) {
+        const int vi = u * 32 + lane;
+        x[u] = vi < nvec ? ld_shared16(sbase + vi * 16) : make_uint4(sent, sent, sent, sent);
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);  // this warp's slice is in registers
@@ -521,12 +544,17 @@ conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, i
     }
     int arg = INT_MAX;
     if (own_max == t.m1 && own_max != -INFINITY) {
-      // the reverse scan leaves the lowest index (u, then e, ascend with it)
+      // Only lanes holding the slice maximum search (usually one lane): find
+      // the first vector containing it with a cheap per-vector test, then
+      // the first element in that vector.  Indices ascend with u, then e.
 #pragma unroll
-      for (int u = kStreamVPL - 1; u >= 0; --u)
+      for (int u = 0; u < kStreamVPL; ++u) {
+        if (arg == INT_MAX && vec_contains<T>(x[u], t.m1)) {
 #pragma unroll
-        for (int e = E - 1; e >= 0; --e)
-          if (elem_of<T>(x[u], e) == t.m1) arg = s0 + (u * 32 + lane) * E + e;
+          for (int e = E - 1; e >= 0; --e)
+            if (elem_of<T>(x[u], e) == t.m1) arg = s0 + (u * 32 + lane) * E + e;
+        }
+      }
     }
     arg = __reduce_min_sync(0xffffffffu, arg);
     if (lane == 0) {
