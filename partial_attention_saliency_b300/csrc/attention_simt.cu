@@ -31,15 +31,17 @@ constexpr int kRowsPerWarp = kQT / kWarps;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
-attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
-                 int L, int H, int M_max, const int32_t* __restrict__ count, float scale_log2,
-                 T* __restrict__ o, float* __restrict__ lse, int32_t* dev_status) {
+attn_simt_kernel(const T* q, const T* k, const T* v,
+                 int L, int H, int M_max, const int32_t* count, float scale_log2,
+                 T* o, float* lse, int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ float Qs[kQT][D];
   __shared__ float Ks[kKT][D + 1];
   __shared__ float Vs[kKT][D];
   const int h = blockIdx.y, b = blockIdx.z;
   const int i0 = blockIdx.x * kQT;
-  int n = count[b];
+  int n = __ldcg(count + b);
   if (n < 0 || n > M_max) {
     if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
     n = n < 0 ? 0 : M_max;
@@ -51,7 +53,7 @@ attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
   for (int e = tid; e < kQT * D; e += kWarps * 32) {
     const int r = e / D, t = e - r * D;
     const int i = i0 + r;
-    Qs[r][t] = i < n ? Elem<T>::to_f32(q[((int64_t)b * M_max + i) * hd + (int64_t)h * D + t]) : 0.f;
+    Qs[r][t] = i < n ? Elem<T>::to_f32(__ldcg(q + ((int64_t)b * M_max + i) * hd + (int64_t)h * D + t)) : 0.f;
   }
 
   constexpr int C = D / 32;  // output dims per lane
@@ -73,8 +75,8 @@ attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
       float kv = 0.f, vv = 0.f;
       if (jj < L) {
         const int64_t off = ((int64_t)b * L + jj) * hd + (int64_t)h * D + t;
-        kv = Elem<T>::to_f32(k[off]);
-        vv = Elem<T>::to_f32(v[off]);
+        kv = Elem<T>::to_f32(__ldcg(k + off));
+        vv = Elem<T>::to_f32(__ldcg(v + off));
       }
       Ks[j][t] = kv;
       Vs[j][t] = vv;
@@ -118,9 +120,11 @@ attn_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, const T* __re
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32)
-colsum_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, int L, int H, int M_max,
-                   const int32_t* __restrict__ count, float scale_log2,
-                   const float* __restrict__ lse, float* __restrict__ colsum) {
+colsum_simt_kernel(const T* q, const T* k, int L, int H, int M_max,
+                   const int32_t* count, float scale_log2,
+                   const float* lse, float* colsum) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ float Ks[kKT][D + 1];
   __shared__ float Qs[kQT][D];
   __shared__ float Ls[kQT];
@@ -128,13 +132,13 @@ colsum_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, int L, int 
   const int h = blockIdx.y, b = blockIdx.z;
   const int j0 = blockIdx.x * kKT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int n = count[b];
+  int n = __ldcg(count + b);
   n = n < 0 ? 0 : (n > M_max ? M_max : n);
   const int64_t hd = (int64_t)H * D;
   for (int e = tid; e < kKT * D; e += kWarps * 32) {
     const int j = e / D, t = e - j * D;
     const int jj = j0 + j;
-    Ks[j][t] = jj < L ? Elem<T>::to_f32(k[((int64_t)b * L + jj) * hd + (int64_t)h * D + t]) : 0.f;
+    Ks[j][t] = jj < L ? Elem<T>::to_f32(__ldcg(k + ((int64_t)b * L + jj) * hd + (int64_t)h * D + t)) : 0.f;
   }
   float acc = 0.f;
   for (int i0 = 0; i0 < n; i0 += kQT) {
@@ -142,11 +146,11 @@ colsum_simt_kernel(const T* __restrict__ q, const T* __restrict__ k, int L, int 
     for (int e = tid; e < kQT * D; e += kWarps * 32) {
       const int r = e / D, t = e - r * D;
       const int i = i0 + r;
-      Qs[r][t] = i < n ? Elem<T>::to_f32(q[((int64_t)b * M_max + i) * hd + (int64_t)h * D + t]) : 0.f;
+      Qs[r][t] = i < n ? Elem<T>::to_f32(__ldcg(q + ((int64_t)b * M_max + i) * hd + (int64_t)h * D + t)) : 0.f;
     }
     if (tid < kQT) {
       const int i = i0 + tid;
-      Ls[tid] = i < n ? lse[((int64_t)b * H + h) * M_max + i] * kLog2e : INFINITY;
+      Ls[tid] = i < n ? __ldcg(lse + ((int64_t)b * H + h) * M_max + i) * kLog2e : INFINITY;
     }
     __syncthreads();
 #pragma unroll
@@ -172,7 +176,7 @@ cudaError_t launch_attn(const void* q, const void* k, const void* v, int B, int 
                         int M_max, const int32_t* count, float scale, void* o, float* lse,
                         int32_t* dev_status, cudaStream_t stream) {
   dim3 grid((M_max + kQT - 1) / kQT, H, B);
-  attn_simt_kernel<T, D><<<grid, kWarps * 32, 0, stream>>>(
+  launch_pdl(attn_simt_kernel<T, D>, grid, kWarps * 32, 0, stream,
       static_cast<const T*>(q), static_cast<const T*>(k), static_cast<const T*>(v), L, H, M_max,
       count, scale * kLog2e, static_cast<T*>(o), lse, dev_status);
   return cudaGetLastError();
@@ -183,7 +187,7 @@ cudaError_t launch_cs(const void* q, const void* k, int B, int L, int H, int M_m
                       const int32_t* count, float scale, const float* lse, float* colsum,
                       cudaStream_t stream) {
   dim3 grid((L + kKT - 1) / kKT, H, B);
-  colsum_simt_kernel<T, D><<<grid, kWarps * 32, 0, stream>>>(
+  launch_pdl(colsum_simt_kernel<T, D>, grid, kWarps * 32, 0, stream,
       static_cast<const T*>(q), static_cast<const T*>(k), L, H, M_max, count, scale * kLog2e, lse,
       colsum);
   return cudaGetLastError();

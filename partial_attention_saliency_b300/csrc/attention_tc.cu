@@ -119,34 +119,6 @@ __device__ __forceinline__ void epi_bar_sync() {
   asm volatile("bar.sync 1, 128;" ::: "memory");
 }
 
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// 2^x for a pair on the FMA pipe (x <= 128): Cody-Waite split x = n + f with
-// n = round(x) (the 1.5 * 2^23 shifter), f in [-1/2, 1/2]; 2^f from a degree-4
-// polynomial (relative-error minimax fit of 2^f on [-1/2, 1/2] made for this
-// library by iteratively reweighted least squares; max relative error
-// 2.7e-6 evaluated in float32); 2^n added to the exponent field.  x is clamped
-// at -125, so arguments below it give 2^-125 (about 2e-38) instead of 0.
-__device__ __forceinline__ float2 exp2_poly2(float2 x) {
-  x.x = fmaxf(x.x, -125.0f);
-  x.y = fmaxf(x.y, -125.0f);
-  const float2 shifter = make_float2(12582912.0f, 12582912.0f);
-  const float2 t = __fadd2_rn(x, shifter);
-  const float2 n = __fadd2_rn(t, make_float2(-12582912.0f, -12582912.0f));
-  const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
-  float2 p = make_float2(0x1.3997cap-7f, 0x1.3997cap-7f);
-  p = __ffma2_rn(p, f, make_float2(0x1.ca1442p-5f, 0x1.ca1442p-5f));
-  p = __ffma2_rn(p, f, make_float2(0x1.ec06dap-3f, 0x1.ec06dap-3f));
-  p = __ffma2_rn(p, f, make_float2(0x1.62e0dcp-1f, 0x1.62e0dcp-1f));
-  p = __ffma2_rn(p, f, make_float2(0x1.ffffe8p-1f, 0x1.ffffe8p-1f));
-  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
-}
-
 // Work plan shared by the forward and merge kernels, computed on the device
 // from the active counts.  A work item is a pair of query tiles of 128
 // active rows (tile A, and tile B when the head has one more tile) of one
@@ -161,7 +133,7 @@ struct FwdPlan {
 };
 
 __device__ __forceinline__ int clamp_count(const int32_t* count, int b, int M_max) {
-  const int n = count[b];
+  const int n = __ldcg(count + b);
   return n < 0 ? 0 : (n > M_max ? M_max : n);
 }
 
@@ -220,9 +192,11 @@ __device__ __forceinline__ void decode_pair(const FwdParams& p, int qi, int* b, 
 __global__ void __launch_bounds__(kFwdThreads, 1)
 attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                    const __grid_constant__ CUtensorMap tv, FwdParams p) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     for (int b = 0; b < p.B; ++b)
-      if (p.count[b] < 0 || p.count[b] > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
+      if (__ldcg(p.count + b) < 0 || __ldcg(p.count + b) > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
   }
   const FwdPlan plan = make_plan(p, gridDim.x);
   const int n_items = plan.total_qp * plan.nsplit;
@@ -312,6 +286,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       if (j > 0) mbar_wait(q_full, (j - 1) & 1, &none);
       for (int k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
         mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &none);
+      if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
@@ -388,6 +363,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mma_commit(mma_done);
       int none = 0;
       mbar_wait(mma_done, 0, &none);
+      if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
   } else {
     // ------------------------------------------------------------ softmax warps
@@ -570,6 +546,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 // not split.
 __global__ void __launch_bounds__(256)
 attn_split_merge_kernel(FwdParams p, int n_ctas) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ FwdPlan s_plan;
   __shared__ int s_rows;  // active rows summed over batch rows
   if (threadIdx.x == 0) {
@@ -602,17 +580,17 @@ attn_split_merge_kernel(FwdParams p, int n_ctas) {
     float M = -INFINITY;
     for (int s = 0; s < plan.nsplit; ++s) {
       const int64_t slot = ((int64_t)qi * plan.nsplit + s) * 2 + x;
-      M = fmaxf(M, p.ws_ml[(slot * kBM + r) * 2]);
+      M = fmaxf(M, __ldcg(p.ws_ml + (slot * kBM + r) * 2));
     }
     float l = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     for (int s = 0; s < plan.nsplit; ++s) {
       const int64_t slot = ((int64_t)qi * plan.nsplit + s) * 2 + x;
-      const float ms = p.ws_ml[(slot * kBM + r) * 2];
-      const float ls = p.ws_ml[(slot * kBM + r) * 2 + 1];
+      const float ms = __ldcg(p.ws_ml + (slot * kBM + r) * 2);
+      const float ls = __ldcg(p.ws_ml + (slot * kBM + r) * 2 + 1);
       const float wgt = ex2_approx(ms - M);
       l += wgt * ls;
-      const float4 o4 = reinterpret_cast<const float4*>(p.ws_o + (slot * kBM + r) * kHD)[lane];
+      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * kBM + r) * kHD) + lane);
       acc[0] = fmaf(wgt, o4.x, acc[0]);
       acc[1] = fmaf(wgt, o4.y, acc[1]);
       acc[2] = fmaf(wgt, o4.z, acc[2]);
@@ -633,8 +611,10 @@ attn_split_merge_kernel(FwdParams p, int n_ctas) {
 __global__ void __launch_bounds__(kThreads, 1)
 attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       ColsumParams p) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  int n = p.count[b];
+  int n = __ldcg(p.count + b);
   n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
   const int nqt = (n + kBM - 1) / kBM;
   const int key0 = kt * kBN;
@@ -704,6 +684,7 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mbar_wait(k_full, 0, &none);
       for (int it = issued - kStages < 0 ? 0 : issued - kStages; it < issued; ++it)
         mbar_wait(&q_full[it % kStages], (it / kStages) & 1, &none);
+      if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -727,6 +708,7 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       mma_commit(mma_done);
       int none = 0;
       mbar_wait(mma_done, 0, &none);
+      if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
   } else {
     const int quarter = warp & 3;
@@ -742,7 +724,7 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       // also after an abort, so the barrier can never wait for a thread that left
       const int sb = it & 1;
       const int i = it * kBM + t;
-      lse_s[sb * kBM + t] = i < n ? lse_g[i] * kLog2e : 0.f;
+      lse_s[sb * kBM + t] = i < n ? __ldcg(lse_g + i) * kLog2e : 0.f;
       epi_bar_sync();
       if (!ok) continue;
       if (!warp_wait(&s_full[sb], (it >> 1) & 1, abort)) {
@@ -853,12 +835,12 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
   fp.max_split_items = can_split ? 2 * n_ctas : 0;
   fp.scale_log2 = scale * kLog2e;
   fp.dev_status = dev_status;
-  attn_fwd_tc_kernel<<<n_ctas, kFwdThreads, kFwdSmem, stream>>>(tq, tk, tv, fp);
+  launch_pdl(attn_fwd_tc_kernel, n_ctas, kFwdThreads, kFwdSmem, stream, tq, tk, tv, fp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (can_split) {
     // at most 2 * n_ctas split items of 128 rows exist: size the grid for them
-    attn_split_merge_kernel<<<2 * n_ctas, 256, 0, stream>>>(fp, n_ctas);
+    launch_pdl(attn_split_merge_kernel, 2 * n_ctas, 256, 0, stream, fp, n_ctas);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -877,7 +859,7 @@ cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, 
     return cudaErrorInvalidValue;
   ColsumParams cp{count, lse, colsum, L, H, M_max, scale * kLog2e, dev_status};
   dim3 cgrid((L + kBN - 1) / kBN, H, B);
-  attn_colsum_tc_kernel<<<cgrid, kThreads, kCsSmem, stream>>>(tq, tk, cp);
+  launch_pdl(attn_colsum_tc_kernel, cgrid, kThreads, kCsSmem, stream, tq, tk, cp);
   return cudaGetLastError();
 }
 

@@ -5,6 +5,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "dllm.h"
 
 namespace dllm {
@@ -20,10 +22,14 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// 16-byte streaming load: read-only path, no L1 allocation.
+// 16-byte streaming load, cached in L2 only.  Never the non-coherent
+// (ld.global.nc) path: with programmatic dependent launch a kernel is
+// resident while the previous kernel still writes, so no buffer is read-only
+// for a whole kernel lifetime and .nc could return stale L1 lines.  For the
+// same reason no kernel parameter of this library is __restrict__.
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;
@@ -34,6 +40,63 @@ __device__ __forceinline__ float ex2_approx(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// 2^x for a pair on the FMA pipe (x <= 128): Cody-Waite split x = n + f with
+// n = round(x) (the 1.5 * 2^23 shifter), f in [-1/2, 1/2]; 2^f from a degree-4
+// polynomial (relative-error minimax fit of 2^f on [-1/2, 1/2] made for this
+// library by iteratively reweighted least squares; max relative error
+// 2.7e-6 evaluated in float32); 2^n added to the exponent field.  x is clamped
+// at -125, so arguments below it give 2^-125 (about 2e-38) instead of 0.
+__device__ __forceinline__ float2 exp2_poly2(float2 x) {
+  x.x = fmaxf(x.x, -125.0f);
+  x.y = fmaxf(x.y, -125.0f);
+  const float2 shifter = make_float2(12582912.0f, 12582912.0f);
+  const float2 t = __fadd2_rn(x, shifter);
+  const float2 n = __fadd2_rn(t, make_float2(-12582912.0f, -12582912.0f));
+  const float2 f = __fadd2_rn(x, make_float2(-n.x, -n.y));
+  float2 p = make_float2(0x1.3997cap-7f, 0x1.3997cap-7f);
+  p = __ffma2_rn(p, f, make_float2(0x1.ca1442p-5f, 0x1.ca1442p-5f));
+  p = __ffma2_rn(p, f, make_float2(0x1.ec06dap-3f, 0x1.ec06dap-3f));
+  p = __ffma2_rn(p, f, make_float2(0x1.62e0dcp-1f, 0x1.62e0dcp-1f));
+  p = __ffma2_rn(p, f, make_float2(0x1.ffffe8p-1f, 0x1.ffffe8p-1f));
+  return make_float2(__uint_as_float(__float_as_uint(p.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(p.y) + (__float_as_uint(t.y) << 23)));
+}
+
+// Programmatic dependent launch.  Every kernel of the library is launched
+// with programmatic stream serialization (launch_pdl below): its CTAs may
+// become resident while the previous kernel on the stream is still running,
+// and pdl_wait() blocks until that kernel has completed and its memory
+// operations are visible.  Each kernel calls pdl_wait() before its first
+// global read or write, so the ordering of the stream is unchanged; it then
+// calls pdl_trigger() to let the next kernel's CTAs launch early.  Without
+// the launch attribute both are no-ops.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 template <typename T> struct Elem;

@@ -102,14 +102,14 @@ __device__ __forceinline__ uint4 load_vec(const T* row, int vi, int V) {
 __device__ __forceinline__ bool row_valid(int b, int r, int R_max, int R_src,
                                           const int32_t* row_idx, const int32_t* count,
                                           int* row_out, bool* bad) {
-  int n = count ? count[b] : R_max;
+  int n = count ? __ldcg(count + b) : R_max;
   *bad = false;
   if (n < 0 || n > R_max) {
     *bad = true;
     n = n < 0 ? 0 : R_max;
   }
   if (r >= n) return false;
-  const int row = row_idx ? row_idx[(int64_t)b * R_max + r] : r;
+  const int row = row_idx ? __ldcg(row_idx + (int64_t)b * R_max + r) : r;
   if (row < 0 || row >= R_src) {
     *bad = true;
     return false;
@@ -120,10 +120,12 @@ __device__ __forceinline__ bool row_valid(int b, int r, int R_max, int R_src,
 
 template <typename T, bool VEC>
 __global__ void __launch_bounds__(kConfThreads)
-conf_partial_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, int64_t bs,
-                    int R_max, const int32_t* __restrict__ row_idx,
-                    const int32_t* __restrict__ count, int nchunks,
-                    ConfPartial* __restrict__ ws) {
+conf_partial_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
+                    int R_max, const int32_t* row_idx,
+                    const int32_t* count, int nchunks,
+                    ConfPartial* ws) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   constexpr int E = vec_elems<T>();
   const int br = blockIdx.x;
   const int chunk = blockIdx.y;
@@ -261,12 +263,14 @@ conf_partial_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, 
   }
 }
 
-__global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* __restrict__ row_idx,
-                                  const int32_t* __restrict__ count,
-                                  const int32_t* __restrict__ out_idx, int out_cols, int nchunks,
-                                  const ConfPartial* __restrict__ ws, float* __restrict__ conf_out,
-                                  int32_t* __restrict__ argmax_out, float* __restrict__ margin_out,
+__global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* row_idx,
+                                  const int32_t* count,
+                                  const int32_t* out_idx, int out_cols, int nchunks,
+                                  const ConfPartial* ws, float* conf_out,
+                                  int32_t* argmax_out, float* margin_out,
                                   int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int64_t br = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (br >= (int64_t)B * R_max) return;
@@ -278,7 +282,7 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* __
   if (!ok) return;
   int col = r;
   if (out_idx != nullptr) {
-    col = out_idx[br];
+    col = __ldcg(out_idx + br);
     if (col < 0 || col >= out_cols) {
       if (lane == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
       return;
@@ -289,7 +293,16 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* __
   acc.m2 = -INFINITY;
   acc.l = 0.f;
   acc.arg = INT_MAX;
-  for (int c = lane; c < nchunks; c += 32) acc = merge(acc, ws[br * nchunks + c]);
+  for (int c = lane; c < nchunks; c += 32) {
+    const ConfPartial* src = ws + br * nchunks + c;
+    ConfPartial w;
+    const float4 raw = __ldcg(reinterpret_cast<const float4*>(src));
+    w.m1 = raw.x;
+    w.m2 = raw.y;
+    w.l = raw.z;
+    w.arg = __float_as_int(raw.w);
+    acc = merge(acc, w);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     ConfPartial other;
@@ -433,7 +446,9 @@ __device__ __forceinline__ Top2Sum lane_reduce(const uint4 (&x)[kStreamVPL]) {
         for (int k = 0; k < 4; ++k) {
           const float2 z = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
           const float2 arg = __ffma2_rn(z, l2e, neg);
-          const float2 e = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+          // a quarter of the exponentials on the FMA pipe, the rest on MUFU
+          const float2 e = (k == 3) ? exp2_poly2(arg)
+                                    : make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
           if (k & 1)
             acc1 = __fadd2_rn(acc1, e);
           else
@@ -448,10 +463,12 @@ __device__ __forceinline__ Top2Sum lane_reduce(const uint4 (&x)[kStreamVPL]) {
 
 template <typename T>
 __global__ void __launch_bounds__(kStreamThreads, 1)
-conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, int64_t bs,
-                   int B, int R_max, const int32_t* __restrict__ row_idx,
-                   const int32_t* __restrict__ count, int nchunks,
-                   ConfPartial* __restrict__ ws, int32_t* dev_status) {
+conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
+                   int B, int R_max, const int32_t* row_idx,
+                   const int32_t* count, int nchunks,
+                   ConfPartial* ws, int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   using namespace sm100;
   constexpr int E = vec_elems<T>();
   constexpr int CE = kStreamChunkBytes / sizeof(T);  // elements per chunk
@@ -463,6 +480,8 @@ conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, i
   uint64_t* full = reinterpret_cast<uint64_t*>(gbase + kStreamStages * kStreamChunkBytes);
   uint64_t* empty = full + kStreamStages;
   int* abort_flag = reinterpret_cast<int*>(empty + kStreamStages);
+  // (batch row * R_max + row, chunk) of each staged chunk; br < 0 ends the stream
+  int2* stage_info = reinterpret_cast<int2*>(abort_flag + 2);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
@@ -475,22 +494,33 @@ conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, i
   }
   __syncthreads();
   volatile int* abort = abort_flag;
-  const int total = B * R_max * nchunks;  // < 2^31 (checked on the host)
 
   if (warp == kStreamWarps) {
     // ------------------------------------------------------------ producer
+    // The producer alone reads counts and row indices; the consumers learn
+    // which row and chunk each stage holds from stage_info.
     if (lane == 0) {
-      int j = 0;
+      const int total = B * R_max * nchunks;  // < 2^31 (checked on the host)
+      int j = 0, cached_b = -1, n_b = 0;
+      bool ok = true;
       for (int v = blockIdx.x; v < total; v += gridDim.x) {
         const int br = v / nchunks, c = v - br * nchunks;
         const int b = br / R_max, r = br - b * R_max;
-        int row;
-        bool bad;
-        if (!row_valid(b, r, R_max, R_src, row_idx, count, &row, &bad)) continue;
+        if (b != cached_b) {
+          cached_b = b;
+          n_b = count ? __ldcg(count + b) : R_max;
+          n_b = n_b < 0 ? 0 : (n_b > R_max ? R_max : n_b);  // the merge kernel reports it
+        }
+        if (r >= n_b) continue;
+        const int row = row_idx ? __ldcg(row_idx + br) : r;
+        if (row < 0 || row >= R_src) continue;  // the merge kernel reports it
         const int stage = j % kStreamStages;
         if (j >= kStreamStages &&
-            !mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort))
+            !mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort)) {
+          ok = false;
           break;
+        }
+        stage_info[stage] = make_int2(br, c);
         const int e0 = c * CE;
         const uint32_t bytes = (uint32_t)min(CE, V - e0) * (uint32_t)sizeof(T);
         mbar_expect_tx(&full[stage], bytes);
@@ -498,26 +528,38 @@ conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, i
                   logits + (int64_t)b * bs + (int64_t)row * rs + e0, bytes, &full[stage]);
         ++j;
       }
-      int none = 0;  // never leave with copies in flight into shared memory
-      for (int k = j - kStreamStages < 0 ? 0 : j - kStreamStages; k < j; ++k)
+      bool sentinel = false;
+      if (ok) {  // end-of-stream stage: a plain arrival with br = -1
+        const int stage = j % kStreamStages;
+        if (j < kStreamStages || mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort)) {
+          stage_info[stage] = make_int2(-1, 0);
+          mbar_arrive(&full[stage]);
+          sentinel = true;
+        }
+      }
+      // Never leave with copies in flight into shared memory: wait for the
+      // data stages that may still be loading.  After the sentinel, the use
+      // j - kStreamStages of its stage is known to be consumed, and that
+      // stage's barrier has moved one phase further, so it is left out.
+      int none = 0;
+      int k0 = j - kStreamStages + (sentinel ? 1 : 0);
+      for (int k = k0 < 0 ? 0 : k0; k < j; ++k)
         mbar_wait(&full[k % kStreamStages], (k / kStreamStages) & 1, &none);
+      if (none) report(dev_status, DLLM_ERR_TIMEOUT);
     }
     return;
   }
 
   // -------------------------------------------------------------- consumers
   const uint32_t sent = std::is_same<T, float>::value ? 0xff800000u : 0xff80ff80u;
-  int j = 0;
-  for (int v = blockIdx.x; v < total; v += gridDim.x) {
-    const int br = v / nchunks, c = v - br * nchunks;
-    const int b = br / R_max, r = br - b * R_max;
-    int row;
-    bool bad;
-    if (!row_valid(b, r, R_max, R_src, row_idx, count, &row, &bad)) continue;
+  for (int j = 0;; ++j) {
     const int stage = j % kStreamStages;
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStreamStages) & 1, abort));
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStreamStages) & 1, abort))) break;
+    const int2 info = stage_info[stage];
+    if (info.x < 0) break;
+    const int br = info.x, c = info.y;
     const int s0 = c * CE + warp * SE;  // first element of this warp's slice
-    const int nvec = ok ? max(0, min(SE, V - s0)) / E : 0;
+    const int nvec = max(0, min(SE, V - s0)) / E;
     const uint32_t sbase = base + stage * kStreamChunkBytes + warp * kStreamSliceBytes;
     uint4 x[kStreamVPL];
     if (nvec == kStreamVPL * 32) {  // full slice: no bounds test per vector
@@ -565,7 +607,6 @@ conf_stream_kernel(const T* __restrict__ logits, int R_src, int V, int64_t rs, i
       out.arg = arg;
       ws[((int64_t)br * nchunks + c) * kStreamWarps + warp] = out;
     }
-    ++j;
   }
   if (lane == 0 && *abort) report(dev_status, DLLM_ERR_TIMEOUT);
 }
@@ -595,23 +636,23 @@ cudaError_t launch_typed(const T* logits, int B, int R_src, int V, int64_t rs, i
         ensure_smem_limit(reinterpret_cast<const void*>(conf_stream_kernel<T>), (int)kStreamSmem);
     if (ea != cudaSuccess) return ea;
     const int snc = stream_nchunks(V, (int)sizeof(T));
-    conf_stream_kernel<T><<<num_sms(), kStreamThreads, kStreamSmem, stream>>>(
+    launch_pdl(conf_stream_kernel<T>, num_sms(), kStreamThreads, kStreamSmem, stream,
         logits, R_src, V, rs, bs, B, R_max, row_idx, count, snc, part, dev_status);
     parts = snc * kStreamWarps;
   } else {
     dim3 grid(B * R_max, nchunks);
     if (vec)
-      conf_partial_kernel<T, true><<<grid, kConfThreads, 0, stream>>>(
+      launch_pdl(conf_partial_kernel<T, true>, grid, kConfThreads, 0, stream,
           logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
     else
-      conf_partial_kernel<T, false><<<grid, kConfThreads, 0, stream>>>(
+      launch_pdl(conf_partial_kernel<T, false>, grid, kConfThreads, 0, stream,
           logits, R_src, V, rs, bs, R_max, row_idx, count, nchunks, part);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)B * R_max;
   const int warps = 8;
-  conf_merge_kernel<<<(unsigned)((rows + warps - 1) / warps), warps * 32, 0, stream>>>(
+  launch_pdl(conf_merge_kernel, (unsigned)((rows + warps - 1) / warps), warps * 32, 0, stream,
       B, R_src, R_max, row_idx, count, out_idx, out_cols, parts, part, conf_out, argmax_out,
       margin_out, dev_status);
   return cudaGetLastError();

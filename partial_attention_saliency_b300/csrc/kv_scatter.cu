@@ -20,21 +20,23 @@ constexpr int kScatterThreads = 256;
 
 template <bool VEC>
 __global__ void __launch_bounds__(kScatterThreads)
-kv_scatter_kernel(char* __restrict__ kc, char* __restrict__ vc, const char* __restrict__ kn,
-                  const char* __restrict__ vn, int L, int M_max, int64_t row_bytes,
-                  const int32_t* __restrict__ idx, const int32_t* __restrict__ count,
+kv_scatter_kernel(char* kc, char* vc, const char* kn,
+                  const char* vn, int L, int M_max, int64_t row_bytes,
+                  const int32_t* idx, const int32_t* count,
                   int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   const int i = blockIdx.x;
   const int b = blockIdx.y;
-  int n = count[b];
+  int n = __ldcg(count + b);
   if (n < 0 || n > M_max) {
     if (i == 0 && threadIdx.x == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
     n = n < 0 ? 0 : M_max;
   }
   if (i >= n) return;
   const int32_t* ib = idx + (int64_t)b * M_max;
-  const int p = ib[i];
-  const bool ordered = (i == 0) || (ib[i - 1] < p);
+  const int p = __ldcg(ib + i);
+  const bool ordered = (i == 0) || (__ldcg(ib + i - 1) < p);
   if (p < 0 || p >= L || !ordered) {
     if (threadIdx.x == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
     return;
@@ -88,12 +90,12 @@ cudaError_t launch_kv_scatter(void* k_cache, void* v_cache, const void* k_new,
                    reinterpret_cast<uintptr_t>(v_new) % 16 == 0;
   dim3 grid(M_max, B);
   if (vec)
-    kv_scatter_kernel<true><<<grid, kScatterThreads, 0, stream>>>(
+    launch_pdl(kv_scatter_kernel<true>, grid, kScatterThreads, 0, stream,
         static_cast<char*>(k_cache), static_cast<char*>(v_cache),
         static_cast<const char*>(k_new), static_cast<const char*>(v_new), L, M_max, row_bytes,
         idx, count, dev_status);
   else
-    kv_scatter_kernel<false><<<grid, kScatterThreads, 0, stream>>>(
+    launch_pdl(kv_scatter_kernel<false>, grid, kScatterThreads, 0, stream,
         static_cast<char*>(k_cache), static_cast<char*>(v_cache),
         static_cast<const char*>(k_new), static_cast<const char*>(v_new), L, M_max, row_bytes,
         idx, count, dev_status);

@@ -71,8 +71,10 @@ __device__ __forceinline__ float cosine_from_sums(float dot, float na, float nb)
 // D is a multiple of the vector width.
 template <typename T, bool VEC, int TPR>
 __global__ void __launch_bounds__(kCosWarps * 32)
-cos_rows_kernel(const T* __restrict__ cur, const T* __restrict__ prev, int B, int Lw, int D,
-                int64_t rs, int64_t bs, float* __restrict__ cos_out) {
+cos_rows_kernel(const T* cur, const T* prev, int B, int Lw, int D,
+                int64_t rs, int64_t bs, float* cos_out) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   constexpr int kRowsPerCta = kCosWarps * 32 / TPR;
   constexpr int kWarpsPerRow = TPR / 32;
   __shared__ float red[kCosWarps][3];
@@ -151,9 +153,11 @@ constexpr int kCompactThreads = 1024;
 constexpr int kCompactItems = 4;  // consecutive positions per thread per chunk
 
 __global__ void __launch_bounds__(kCompactThreads)
-compact_kernel(const float* __restrict__ cos, const uint8_t* __restrict__ locked, int Lw,
-               float tau, int32_t idx_base, int32_t* __restrict__ idx_out,
-               int32_t* __restrict__ count_out) {
+compact_kernel(const float* cos, const uint8_t* locked, int Lw,
+               float tau, int32_t idx_base, int32_t* idx_out,
+               int32_t* count_out) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ int warp_tot[kCompactThreads / 32];
   __shared__ int chunk_total;
   const int b = blockIdx.x;
@@ -170,8 +174,8 @@ compact_kernel(const float* __restrict__ cos, const uint8_t* __restrict__ locked
       const int p = start + tid * kCompactItems + k;
       bool a = false;
       if (p < Lw) {
-        a = !(c[p] >= tau);  // NaN cosine counts as salient
-        if (lk != nullptr && lk[p] != 0) a = false;
+        a = !(__ldcg(c + p) >= tau);  // NaN cosine counts as salient
+        if (lk != nullptr && __ldcg(lk + p) != 0) a = false;
       }
       act[k] = a;
       mine += a ? 1 : 0;
@@ -217,7 +221,7 @@ void launch_cos(const T* cur, const T* prev, int B, int Lw, int D, int64_t rs, i
   const int64_t want = (rows + kRowsPerCta - 1) / kRowsPerCta;
   const int64_t cap = (int64_t)num_sms() * 16;
   const int grid = (int)(want < cap ? want : cap);
-  cos_rows_kernel<T, VEC, TPR><<<grid, kCosWarps * 32, 0, stream>>>(cur, prev, B, Lw, D, rs, bs,
+  launch_pdl(cos_rows_kernel<T, VEC, TPR>, grid, kCosWarps * 32, 0, stream, cur, prev, B, Lw, D, rs, bs,
                                                                     cos_out);
 }
 
@@ -265,7 +269,7 @@ cudaError_t launch_saliency_select(const void* cur, const void* prev, int dtype,
     e = launch_typed(static_cast<const float*>(cur), static_cast<const float*>(prev), B, Lw, D,
                      row_stride, batch_stride, cos_out, stream);
   if (e != cudaSuccess) return e;
-  compact_kernel<<<B, kCompactThreads, 0, stream>>>(cos_out, locked, Lw, tau, idx_base, idx_out,
+  launch_pdl(compact_kernel, B, kCompactThreads, 0, stream, cos_out, locked, Lw, tau, idx_base, idx_out,
                                                     count_out);
   return cudaGetLastError();
 }

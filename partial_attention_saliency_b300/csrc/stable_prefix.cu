@@ -21,13 +21,15 @@ constexpr int kPrefixThreads = 256;
 constexpr int kPrefixUnroll = 4;
 
 __global__ void __launch_bounds__(kPrefixThreads)
-stable_prefix_kernel(const float* __restrict__ score, int L, int32_t* __restrict__ start,
-                     float tau, int min_commit, int advance, int32_t* __restrict__ len_out,
+stable_prefix_kernel(const float* score, int L, int32_t* start,
+                     float tau, int min_commit, int advance, int32_t* len_out,
                      int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
   __shared__ int warp_min[kPrefixThreads / 32];
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = start[b];
+  const int s = __ldcg(start + b);
   if (s < 0 || s > L) {
     if (tid == 0) {
       report(dev_status, DLLM_ERR_DEVICE_CHECK);
@@ -42,7 +44,7 @@ stable_prefix_kernel(const float* __restrict__ score, int L, int32_t* __restrict
 #pragma unroll
     for (int u = 0; u < kPrefixUnroll; ++u) {
       const int p = base + u * kPrefixThreads + tid;
-      v[u] = p < L ? row[p] : INFINITY;
+      v[u] = p < L ? __ldcg(row + p) : INFINITY;
     }
 #pragma unroll
     for (int u = kPrefixUnroll - 1; u >= 0; --u) {
@@ -69,7 +71,7 @@ stable_prefix_kernel(const float* __restrict__ score, int L, int32_t* __restrict
 cudaError_t launch_stable_prefix(const float* score, int B, int L, int32_t* start, float tau,
                                  int min_commit, int advance_start, int32_t* len_out,
                                  int32_t* dev_status, cudaStream_t stream) {
-  stable_prefix_kernel<<<B, kPrefixThreads, 0, stream>>>(score, L, start, tau, min_commit,
+  launch_pdl(stable_prefix_kernel, B, kPrefixThreads, 0, stream, score, L, start, tau, min_commit,
                                                          advance_start, len_out, dev_status);
   return cudaGetLastError();
 }

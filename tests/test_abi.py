@@ -92,3 +92,24 @@ def test_binding_fails_loudly_without_library(tmp_path):
             _lib.load_library(str(tmp_path / "missing.so"))
         finally:
             _lib._LIB = saved
+
+
+def test_every_kernel_waits_for_its_predecessor():
+    # Every kernel is launched with programmatic dependent launch, so it may
+    # be resident while the previous kernel on the stream still runs; it must
+    # execute pdl_wait() before touching global memory.  Static check of the
+    # sources: each __global__ body starts with pdl_wait(), and no launch
+    # bypasses launch_pdl.
+    src_dir = os.path.join(ROOT, "partial_attention_saliency_b300", "csrc")
+    kernels = 0
+    for name in sorted(os.listdir(src_dir)):
+        if not name.endswith(".cu"):
+            continue
+        with open(os.path.join(src_dir, name)) as f:
+            text = f.read()
+        assert "<<<" not in text, f"{name}: kernel launched without launch_pdl"
+        for m in re.finditer(r"__global__[^{;]*\{", text):
+            body = text[m.end():m.end() + 120].strip()
+            assert body.startswith("pdl_wait();"), f"{name}: kernel body does not start with pdl_wait()"
+            kernels += 1
+    assert kernels >= 12

@@ -154,6 +154,29 @@ def test_confidence_1k_full_size(dl):
     _conf_compare(f64(conf), i32(am), f64(mg), rc, ra, rm)
 
 
+def test_confidence_repeated_calls_reuse_buffers(dl):
+    # Back-to-back calls on the same workspace and outputs with different
+    # logits: each call's merge must see only that call's partial results
+    # (no stale data from the previous call on the same addresses).
+    s = workloads.STEP_1K
+    R = 256
+    ws = torch.empty((dl.dllm_confidence_workspace_bytes(1, R, s.V, s.dtype),), dtype=torch.uint8,
+                     device="cuda")
+    conf = torch.empty((1, R), device="cuda")
+    am = torch.empty((1, R), dtype=torch.int32, device="cuda")
+    mg = torch.empty((1, R), device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    for seed in (11, 12, 13):
+        g = torch.Generator().manual_seed(seed)
+        logits = workloads.normal(g, (1, R, s.V), 2.0, s.dtype)
+        dl.dllm_confidence(dev(logits), conf_out=conf, argmax_out=am, margin_out=mg, ws=ws,
+                           dev_status=st)
+        torch.cuda.synchronize()
+        rc, ra, rm = oracle.confidence(f64(logits))
+        _conf_compare(f64(conf), i32(am), f64(mg), rc, ra, rm)
+    assert int(st[0]) == 0
+
+
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 @pytest.mark.parametrize("V", [2, 7, 1001, 16384, 40000])
 def test_confidence_ragged_vocab_and_ties(dl, dtype, V):
@@ -470,3 +493,30 @@ def test_confidence_repeatable_run_to_run(dl):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x, y)
+
+
+def test_step_repeated_no_bounded_wait_expires(dl):
+    # Every pipeline wait in the kernels gives up after about a second and
+    # reports DLLM_ERR_TIMEOUT; in normal operation none may expire.  Twenty
+    # back-to-back 1K steps must leave dev_status at 0 and finish in well
+    # under one expired wait.
+    import time
+    s = workloads.STEP_1K
+    inp = workloads.make_step(s)
+    t = {k: dev(inp[k]) for k in ("cur", "prev", "k_cache", "v_cache", "k_new", "v_new", "q",
+                                   "logits")}
+    step = dl.PartialStep(s.B, s.L, s.H, s.d, s.D, s.V, s.dtype, s.win_start, s.logit_rows,
+                          s.tau, device=torch.device("cuda"))
+    score = dev(torch.full((s.B, s.L), float("inf")))
+    start = dev(torch.full((s.B,), s.win_start, dtype=torch.int32))
+    args = (t["cur"], t["prev"], t["k_cache"], t["v_cache"], t["k_new"], t["v_new"], t["q"],
+            t["logits"], score, start)
+    step.run(*args)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(20):
+        step.run(*args)
+    torch.cuda.synchronize()
+    elapsed = time.perf_counter() - t0
+    assert int(step.dev_status[0]) == 0
+    assert elapsed < 0.5, elapsed
