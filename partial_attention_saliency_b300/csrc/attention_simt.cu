@@ -41,7 +41,7 @@ attn_simt_kernel(const T* q, const T* k, const T* v,
   __shared__ float Vs[kKT][D];
   const int h = blockIdx.y, b = blockIdx.z;
   const int i0 = blockIdx.x * kQT;
-  int n = __ldcg(count + b);
+  int n = __ldca(count + b);
   if (n < 0 || n > M_max) {
     if (blockIdx.x == 0 && h == 0 && threadIdx.x == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
     n = n < 0 ? 0 : M_max;
@@ -53,7 +53,7 @@ attn_simt_kernel(const T* q, const T* k, const T* v,
   for (int e = tid; e < kQT * D; e += kWarps * 32) {
     const int r = e / D, t = e - r * D;
     const int i = i0 + r;
-    Qs[r][t] = i < n ? Elem<T>::to_f32(__ldcg(q + ((int64_t)b * M_max + i) * hd + (int64_t)h * D + t)) : 0.f;
+    Qs[r][t] = i < n ? Elem<T>::to_f32(__ldca(q + ((int64_t)b * M_max + i) * hd + (int64_t)h * D + t)) : 0.f;
   }
 
   constexpr int C = D / 32;  // output dims per lane
@@ -75,8 +75,8 @@ attn_simt_kernel(const T* q, const T* k, const T* v,
       float kv = 0.f, vv = 0.f;
       if (jj < L) {
         const int64_t off = ((int64_t)b * L + jj) * hd + (int64_t)h * D + t;
-        kv = Elem<T>::to_f32(__ldcg(k + off));
-        vv = Elem<T>::to_f32(__ldcg(v + off));
+        kv = Elem<T>::to_f32(__ldca(k + off));
+        vv = Elem<T>::to_f32(__ldca(v + off));
       }
       Ks[j][t] = kv;
       Vs[j][t] = vv;
@@ -132,13 +132,13 @@ colsum_simt_kernel(const T* q, const T* k, int L, int H, int M_max,
   const int h = blockIdx.y, b = blockIdx.z;
   const int j0 = blockIdx.x * kKT;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  int n = __ldcg(count + b);
+  int n = __ldca(count + b);
   n = n < 0 ? 0 : (n > M_max ? M_max : n);
   const int64_t hd = (int64_t)H * D;
   for (int e = tid; e < kKT * D; e += kWarps * 32) {
     const int j = e / D, t = e - j * D;
     const int jj = j0 + j;
-    Ks[j][t] = jj < L ? Elem<T>::to_f32(__ldcg(k + ((int64_t)b * L + jj) * hd + (int64_t)h * D + t)) : 0.f;
+    Ks[j][t] = jj < L ? Elem<T>::to_f32(__ldca(k + ((int64_t)b * L + jj) * hd + (int64_t)h * D + t)) : 0.f;
   }
   float acc = 0.f;
   for (int i0 = 0; i0 < n; i0 += kQT) {
@@ -146,11 +146,11 @@ colsum_simt_kernel(const T* q, const T* k, int L, int H, int M_max,
     for (int e = tid; e < kQT * D; e += kWarps * 32) {
       const int r = e / D, t = e - r * D;
       const int i = i0 + r;
-      Qs[r][t] = i < n ? Elem<T>::to_f32(__ldcg(q + ((int64_t)b * M_max + i) * hd + (int64_t)h * D + t)) : 0.f;
+      Qs[r][t] = i < n ? Elem<T>::to_f32(__ldca(q + ((int64_t)b * M_max + i) * hd + (int64_t)h * D + t)) : 0.f;
     }
     if (tid < kQT) {
       const int i = i0 + tid;
-      Ls[tid] = i < n ? __ldcg(lse + ((int64_t)b * H + h) * M_max + i) * kLog2e : INFINITY;
+      Ls[tid] = i < n ? __ldca(lse + ((int64_t)b * H + h) * M_max + i) * kLog2e : INFINITY;
     }
     __syncthreads();
 #pragma unroll

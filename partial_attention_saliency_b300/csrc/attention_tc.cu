@@ -57,9 +57,11 @@ constexpr float kRescaleThreshold = 8.0f; // log2 units: P stays below 2^8
 constexpr int kFwdThreads = 320;
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
-// Exponentials on the FMA pipe instead of MUFU: pairs c with (c % 4) == 3,
-// a quarter of them, so that MUFU keeps pace with the tensor cores.
-constexpr int kPolyEvery = 4;
+// Exponential pairs computed on the FMA pipe (exp2_poly2) instead of MUFU,
+// out of every 8: the forward softmax and the column sums are otherwise
+// bound by the MUFU ex2 rate.
+constexpr int kFwdPoly = 2;
+constexpr int kColsumPoly = 3;
 
 struct FwdParams {
   const int32_t* count;
@@ -122,49 +124,97 @@ __device__ __forceinline__ void epi_bar_sync() {
 // Work plan shared by the forward and merge kernels, computed on the device
 // from the active counts.  A work item is a pair of query tiles of 128
 // active rows (tile A, and tile B when the head has one more tile) of one
-// (batch row, head), optionally limited to a slice of the key range: when
-// there are fewer pairs than CTAs the key range of each pair is split so
-// that every SM gets work.
+// (batch row, head), optionally limited to a slice of the key range.  The
+// pairs are dealt round-robin to the persistent CTAs; the pairs of the last,
+// partly filled round (all pairs when there are fewer pairs than CTAs) are
+// split over the key range so that the round keeps every SM busy, and a
+// merge kernel combines their slices.
 struct FwdPlan {
   int total_qp;  // tile pairs over all (b, h)
-  int nsplit;    // key-range splits per pair
+  int n_full;    // pairs [0, n_full) are one item each over all keys
+  int nsplit;    // key-range splits of each pair in [n_full, total_qp)
   int tps;       // key tiles per split
   int nkt;       // key tiles of the sequence
 };
 
 __device__ __forceinline__ int clamp_count(const int32_t* count, int b, int M_max) {
-  const int n = __ldcg(count + b);
+  const int n = __ldca(count + b);
   return n < 0 ? 0 : (n > M_max ? M_max : n);
 }
 
 __device__ __forceinline__ int pairs_of(int n) { return (((n + kBM - 1) / kBM) + 1) / 2; }
 
-__device__ FwdPlan make_plan(const FwdParams& p, int n_ctas) {
+// Clamped active counts of the first kPlanMaxB batch rows, staged in shared
+// memory once per CTA (the plan is decoded for every work item); rows beyond
+// are read from global memory.
+constexpr int kPlanMaxB = 64;
+
+__device__ __forceinline__ int cnt_of(const FwdParams& p, const int* s_cnt, int b) {
+  return b < kPlanMaxB ? s_cnt[b] : clamp_count(p.count, b, p.M_max);
+}
+
+__device__ __forceinline__ void stage_counts(const FwdParams& p, int* s_cnt) {
+  for (int b = threadIdx.x; b < p.B && b < kPlanMaxB; b += blockDim.x)
+    s_cnt[b] = clamp_count(p.count, b, p.M_max);
+}
+
+__device__ FwdPlan make_plan(const FwdParams& p, const int* s_cnt, int n_ctas) {
   FwdPlan pl;
   pl.nkt = (p.L + kBN - 1) / kBN;
   int qp = 0;
-  for (int b = 0; b < p.B; ++b) qp += p.H * pairs_of(clamp_count(p.count, b, p.M_max));
+  for (int b = 0; b < p.B; ++b) qp += p.H * pairs_of(cnt_of(p, s_cnt, b));
   pl.total_qp = qp;
-  int ns = 1;
-  if (qp > 0 && qp < n_ctas && p.max_split_items > 0) {
-    ns = (n_ctas + qp - 1) / qp;
+  int ns = 1, tail = 0;
+  if (qp > 0 && p.max_split_items > 0) {
+    if (qp < n_ctas) {
+      tail = qp;
+      ns = (n_ctas + qp - 1) / qp;
+    } else if (2 * (qp % n_ctas) <= n_ctas) {  // a last round at most half full
+      tail = qp % n_ctas;
+      ns = tail > 0 ? n_ctas / tail : 1;
+    }
     const int max_by_tiles = pl.nkt / 2 > 1 ? pl.nkt / 2 : 1;  // at least two key tiles each
     ns = ns < max_by_tiles ? ns : max_by_tiles;
-    const int max_by_ws = p.max_split_items / qp;
-    ns = ns < max_by_ws ? ns : max_by_ws;
+    if (tail > 0) {
+      const int max_by_ws = p.max_split_items / tail;
+      ns = ns < max_by_ws ? ns : max_by_ws;
+    }
     if (ns < 1) ns = 1;
   }
   pl.tps = (pl.nkt + ns - 1) / ns;
   pl.nsplit = (pl.nkt + pl.tps - 1) / pl.tps;  // no empty split
+  pl.n_full = pl.nsplit > 1 ? qp - tail : qp;
   return pl;
+}
+
+__device__ __forceinline__ int plan_items(const FwdPlan& pl) {
+  return pl.n_full + (pl.total_qp - pl.n_full) * pl.nsplit;
+}
+
+// Work item v -> (pair index, first key tile, key tiles, split slot or -1).
+__device__ __forceinline__ void item_of(const FwdPlan& pl, int v, int* qi, int* kt0, int* nt,
+                                        int* slot) {
+  if (v < pl.n_full) {
+    *qi = v;
+    *kt0 = 0;
+    *nt = pl.nkt;
+    *slot = -1;
+  } else {
+    const int u = v - pl.n_full;
+    const int split = u % pl.nsplit;
+    *qi = pl.n_full + u / pl.nsplit;
+    *kt0 = split * pl.tps;
+    *nt = min(pl.tps, pl.nkt - *kt0);
+    *slot = u;
+  }
 }
 
 // Pair index qi -> (b, h, pair, query tiles in the pair), batch-major then
 // head-major.
-__device__ __forceinline__ void decode_pair(const FwdParams& p, int qi, int* b, int* h,
-                                            int* pair, int* nq) {
+__device__ __forceinline__ void decode_pair(const FwdParams& p, const int* s_cnt, int qi, int* b,
+                                            int* h, int* pair, int* nq) {
   for (int bb = 0; bb < p.B; ++bb) {
-    const int n = clamp_count(p.count, bb, p.M_max);
+    const int n = cnt_of(p, s_cnt, bb);
     const int nqt = (n + kBM - 1) / kBM;
     const int per_head = (nqt + 1) / 2;
     if (qi < per_head * p.H) {
@@ -194,12 +244,17 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                    const __grid_constant__ CUtensorMap tv, FwdParams p) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
+  __shared__ int s_cnt[kPlanMaxB];
+  stage_counts(p, s_cnt);
   if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int b = 0; b < p.B; ++b)
-      if (__ldcg(p.count + b) < 0 || __ldcg(p.count + b) > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
+    for (int b = 0; b < p.B; ++b) {
+      const int c = __ldca(p.count + b);
+      if (c < 0 || c > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
+    }
   }
-  const FwdPlan plan = make_plan(p, gridDim.x);
-  const int n_items = plan.total_qp * plan.nsplit;
+  __syncthreads();
+  const FwdPlan plan = make_plan(p, s_cnt, gridDim.x);
+  const int n_items = plan_items(plan);
   if ((int)blockIdx.x >= n_items) return;
 
   extern __shared__ uint8_t smem_raw[];
@@ -253,11 +308,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       int j = 0, g = 0;
       bool ok = true;
       for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
-        int b, h, pair, nq;
-        decode_pair(p, v / plan.nsplit, &b, &h, &pair, &nq);
-        const int split = v % plan.nsplit;
-        const int kt0 = split * plan.tps;
-        const int nt = min(plan.tps, plan.nkt - kt0);
+        int b, h, pair, nq, qi, kt0, nt, slot;
+        item_of(plan, v, &qi, &kt0, &nt, &slot);
+        decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
         if (j > 0 && !mbar_wait(q_empty, (j - 1) & 1, abort)) break;
         mbar_expect_tx(q_full, (uint32_t)nq * kTile);
         for (int x = 0; x < nq; ++x) {
@@ -317,10 +370,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       int jt[2] = {0, 0};        // items processed per query tile slot
       bool ok = true;
       for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
-        int b, h, pair, nq;
-        decode_pair(p, v / plan.nsplit, &b, &h, &pair, &nq);
-        const int split = v % plan.nsplit;
-        const int nt = min(plan.tps, plan.nkt - split * plan.tps);
+        int b, h, pair, nq, qi, kt0, nt, slot;
+        item_of(plan, v, &qi, &kt0, &nt, &slot);
+        decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
         if (!mbar_wait(q_full, j & 1, abort)) break;
         if (!mbar_wait(&kv_full[g % kStages], (g / kStages) & 1, abort)) break;
         tc_fence_after();
@@ -377,12 +429,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     int gx = 0, jx = 0;
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x) {
-      int b, h, pair, nq;
-      decode_pair(p, v / plan.nsplit, &b, &h, &pair, &nq);
+      int b, h, pair, nq, qi, kt0, nt, wslot;
+      item_of(plan, v, &qi, &kt0, &nt, &wslot);
+      decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
       if (x >= nq) continue;
-      const int split = v % plan.nsplit;
-      const int kt0 = split * plan.tps;
-      const int nt = min(plan.tps, plan.nkt - kt0);
       float m = -INFINITY, l = 0.f;
       for (int t = 0; t < nt; ++t, ++gx) {
         if (!warp_wait(&s_full[x], gx & 1, abort)) {
@@ -390,27 +440,34 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           break;
         }
         tc_fence_after();
-        // Pass 1: the row maximum over the tile (S stays in tensor memory).
+        // The whole S row (128 keys) is read with one wait; the row maximum
+        // is a 4-way tree; P = 2^(s * scale * log2 e - m) is then produced
+        // in chunks of 32 keys and stored as bf16 pairs into the first 64
+        // columns of S (P column j holds keys 2j, 2j + 1; those S columns
+        // are already in registers).
         const int kvalid = p.L - (kt0 + t) * kBN;  // < kBN only on the last, partial tile
-        float mx = -INFINITY;
+        uint32_t raw[kBN];
 #pragma unroll
-        for (int c = 0; c < kBN / 64; ++c) {
-          uint32_t ra[32], rb[32];
-          tmem_ld_32x32b_x32(tS + c * 64, ra);
-          tmem_ld_32x32b_x32(tS + c * 64 + 32, rb);
-          tmem_ld_wait();
-          if (kvalid < kBN) {  // warp-uniform
+        for (int c = 0; c < kBN / 32; ++c)
+          tmem_ld_32x32b_x32(tS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
+        tmem_ld_wait();
+        if (kvalid < kBN) {  // warp-uniform
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
-              if (c * 64 + q >= kvalid) ra[q] = 0xff800000u;  // -inf
-              if (c * 64 + 32 + q >= kvalid) rb[q] = 0xff800000u;
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 32; q += 2)
-            mx = fmax3(mx, fmaxf(__uint_as_float(ra[q]), __uint_as_float(ra[q + 1])),
-                       fmaxf(__uint_as_float(rb[q]), __uint_as_float(rb[q + 1])));
+          for (int q = 0; q < kBN; ++q)
+            if (q >= kvalid) raw[q] = 0xff800000u;  // -inf
         }
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int q = 0; q < kBN; q += 8)
+          mx4[(q >> 3) & 3] =
+              fmax3(mx4[(q >> 3) & 3],
+                    fmax3(__uint_as_float(raw[q]), __uint_as_float(raw[q + 1]),
+                          __uint_as_float(raw[q + 2])),
+                    fmax3(__uint_as_float(raw[q + 3]),
+                          fmax3(__uint_as_float(raw[q + 4]), __uint_as_float(raw[q + 5]),
+                                __uint_as_float(raw[q + 6])),
+                          __uint_as_float(raw[q + 7])));
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float m_new = fmaxf(m, mx * sl2);
         const bool grow = m_new > m + kRescaleThreshold;
         const float alpha = grow ? ex2_approx(m - m_new) : 1.0f;
@@ -418,34 +475,23 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           l *= alpha;
           m = m_new;
         }
-        // Pass 2: P = 2^(s * scale * log2 e - m) in bf16 pairs over the first
-        // 64 columns of S.  Chunk c reads S columns [32c, 32c + 32) and writes
-        // P columns [16c, 16c + 16), which were read in chunk c / 2 <= c.
         const float2 sl2x2 = make_float2(sl2, sl2);
         const float2 negm = make_float2(-m, -m);
         float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c) {
-          uint32_t raw[32];
-          tmem_ld_32x32b_x32(tS + c * 32, raw);
-          tmem_ld_wait();
-          if (kvalid < kBN) {
-#pragma unroll
-            for (int q = 0; q < 32; ++q)
-              if (c * 32 + q >= kvalid) raw[q] = 0xff800000u;
-          }
           uint32_t pk[16];
 #pragma unroll
           for (int cc = 0; cc < 16; ++cc) {
-            const float2 a = __ffma2_rn(
-                make_float2(__uint_as_float(raw[2 * cc]), __uint_as_float(raw[2 * cc + 1])),
-                sl2x2, negm);
+            const int q = c * 32 + cc * 2;
+            const float2 a2 = __ffma2_rn(
+                make_float2(__uint_as_float(raw[q]), __uint_as_float(raw[q + 1])), sl2x2, negm);
             float2 e;
-            if (cc % kPolyEvery == kPolyEvery - 1) {
-              e = exp2_poly2(a);
+            if ((cc & 7) >= 8 - kFwdPoly) {
+              e = exp2_poly2(a2);
             } else {
-              e.x = ex2_approx(a.x);
-              e.y = ex2_approx(a.y);
+              e.x = ex2_approx(a2.x);
+              e.y = ex2_approx(a2.y);
             }
             if (cc & 1)
               acc1 = __fadd2_rn(acc1, e);
@@ -483,12 +529,12 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       ++jx;
       // ---------------------------------------------------------- epilogue
       tc_fence_after();
-      const int n = clamp_count(p.count, b, p.M_max);
+      const int n = cnt_of(p, s_cnt, b);
       const int i = (2 * pair + x) * kBM + r;
       const bool store = i < n;
-      const bool partial = plan.nsplit > 1;
+      const bool partial = wslot >= 0;
       const float inv = partial ? 1.0f : 1.0f / l;
-      const int64_t slot = (int64_t)v * 2 + x;  // workspace tile slot
+      const int64_t slot = (int64_t)wslot * 2 + x;  // workspace tile slot (split items)
       __nv_bfloat16* orow =
           p.o + ((int64_t)b * p.M_max + i) * ((int64_t)p.H * kHD) + (int64_t)h * kHD;
       float* prow = p.ws_o + (slot * kBM + r) * kHD;
@@ -540,61 +586,66 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   if (threadIdx.x == 0 && *abort) report(p.dev_status, DLLM_ERR_TIMEOUT);
 }
 
-// Combines the key-range splits of each active row: O = sum_s 2^(m_s - M) O_s
-// / sum_s 2^(m_s - M) l_s, lse = (M + log2 l) ln 2.  Grid-stride over the
-// active rows only (one warp per (b, row, h)); does nothing when the plan did
-// not split.
+// Combines the key-range splits of each active row of the split pairs:
+// O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s, lse = (M + log2 l) ln 2.
+// One warp per (split pair, tile, row), each lane four of the 128 dims;
+// does nothing when the plan split no pair.
 __global__ void __launch_bounds__(256)
 attn_split_merge_kernel(FwdParams p, int n_ctas) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  __shared__ FwdPlan s_plan;
-  __shared__ int s_rows;  // active rows summed over batch rows
-  if (threadIdx.x == 0) {
-    s_plan = make_plan(p, n_ctas);
-    int rows = 0;
-    for (int b = 0; b < p.B; ++b) rows += clamp_count(p.count, b, p.M_max);
-    s_rows = rows;
-  }
+  __shared__ int s_cnt[kPlanMaxB];
+  stage_counts(p, s_cnt);
   __syncthreads();
-  const FwdPlan plan = s_plan;
+  const FwdPlan plan = make_plan(p, s_cnt, n_ctas);
   if (plan.nsplit <= 1) return;
   const int lane = threadIdx.x & 31;
-  const int64_t total = (int64_t)s_rows * p.H;
+  const int64_t total = (int64_t)(plan.total_qp - plan.n_full) * 2 * kBM;
   for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < total;
        w += (int64_t)gridDim.x * (blockDim.x >> 5)) {
-    int rem = (int)(w / p.H);
-    const int h = (int)(w - (int64_t)rem * p.H);
-    int b = 0, qi = 0;
-    for (; b < p.B; ++b) {
-      const int nb = clamp_count(p.count, b, p.M_max);
-      if (rem < nb) break;
-      rem -= nb;
-      qi += p.H * pairs_of(nb);
-    }
-    const int i = rem;
-    const int n = clamp_count(p.count, b, p.M_max);
-    qi += h * pairs_of(n) + i / (2 * kBM);
-    const int x = (i / kBM) & 1;
-    const int r = i % kBM;
-    float M = -INFINITY;
-    for (int s = 0; s < plan.nsplit; ++s) {
-      const int64_t slot = ((int64_t)qi * plan.nsplit + s) * 2 + x;
-      M = fmaxf(M, __ldcg(p.ws_ml + (slot * kBM + r) * 2));
-    }
-    float l = 0.f;
+    const int sp = (int)(w / (2 * kBM));  // split pair
+    const int x = (int)((w / kBM) & 1);   // tile of the pair
+    const int r = (int)(w % kBM);         // row of the tile
+    int b, h, pair, nq;
+    decode_pair(p, s_cnt, plan.n_full + sp, &b, &h, &pair, &nq);
+    if (x >= nq) continue;
+    const int i = (2 * pair + x) * kBM + r;
+    if (i >= cnt_of(p, s_cnt, b)) continue;
+    // all loads of the row's slices are issued before any is used
+    constexpr int kU = 4;
+    float M = -INFINITY, l = 0.f;
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int s = 0; s < plan.nsplit; ++s) {
-      const int64_t slot = ((int64_t)qi * plan.nsplit + s) * 2 + x;
-      const float ms = __ldcg(p.ws_ml + (slot * kBM + r) * 2);
-      const float ls = __ldcg(p.ws_ml + (slot * kBM + r) * 2 + 1);
-      const float wgt = ex2_approx(ms - M);
-      l += wgt * ls;
-      const float4 o4 = __ldcg(reinterpret_cast<const float4*>(p.ws_o + (slot * kBM + r) * kHD) + lane);
-      acc[0] = fmaf(wgt, o4.x, acc[0]);
-      acc[1] = fmaf(wgt, o4.y, acc[1]);
-      acc[2] = fmaf(wgt, o4.z, acc[2]);
-      acc[3] = fmaf(wgt, o4.w, acc[3]);
+    for (int s0 = 0; s0 < plan.nsplit; s0 += kU) {
+      float2 ml[kU];
+      float4 o4[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (s0 + u < plan.nsplit) {
+          const int64_t slot = ((int64_t)sp * plan.nsplit + s0 + u) * 2 + x;
+          ml[u] = __ldca(reinterpret_cast<const float2*>(p.ws_ml + (slot * kBM + r) * 2));
+          o4[u] = __ldca(reinterpret_cast<const float4*>(p.ws_o + (slot * kBM + r) * kHD) + lane);
+        } else {
+          ml[u] = make_float2(-INFINITY, 0.f);
+          o4[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+      float Mn = M;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) Mn = fmaxf(Mn, ml[u].x);
+      const float c = ex2_approx(M - Mn);  // rescale what was accumulated so far
+      l *= c;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[q] *= c;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const float wgt = ex2_approx(ml[u].x - Mn);
+        l = fmaf(wgt, ml[u].y, l);
+        acc[0] = fmaf(wgt, o4[u].x, acc[0]);
+        acc[1] = fmaf(wgt, o4[u].y, acc[1]);
+        acc[2] = fmaf(wgt, o4[u].z, acc[2]);
+        acc[3] = fmaf(wgt, o4[u].w, acc[3]);
+      }
+      M = Mn;
     }
     const float inv = 1.0f / l;
     __nv_bfloat16* orow =
@@ -614,7 +665,7 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
   const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
-  int n = __ldcg(p.count + b);
+  int n = __ldca(p.count + b);
   n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
   const int nqt = (n + kBM - 1) / kBM;
   const int key0 = kt * kBN;
@@ -717,15 +768,20 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const float* lse_g = p.lse + ((int64_t)b * p.H + h) * p.M_max;
     const float sl2 = p.scale_log2;
-    float acc = 0.f;
+    float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
     bool ok = true;
+    // -lse in log2 units of query row it * 128 + t; padded rows get -inf, so
+    // their terms vanish.  Loaded one query tile ahead, so that the load
+    // latency overlaps the previous tile's work.
+    float nlse = t < n ? -__ldca(lse_g + t) * kLog2e : -INFINITY;
     for (int it = 0; it < nqt; ++it) {
       // every epilogue thread passes the named barrier on every iteration,
       // also after an abort, so the barrier can never wait for a thread that left
       const int sb = it & 1;
-      const int i = it * kBM + t;
-      lse_s[sb * kBM + t] = i < n ? __ldcg(lse_g + i) * kLog2e : 0.f;
+      lse_s[sb * kBM + t] = nlse;
       epi_bar_sync();
+      const int inext = (it + 1) * kBM + t;
+      nlse = (it + 1 < nqt && inext < n) ? -__ldca(lse_g + inext) * kLog2e : -INFINITY;
       if (!ok) continue;
       if (!warp_wait(&s_full[sb], (it >> 1) & 1, abort)) {
         ok = false;
@@ -741,14 +797,36 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&s_free[sb]);
-      const int nvalid = min(kBM, n - it * kBM);
-      const float* ls = lse_s + sb * kBM;
+      // sum over the tile's query rows of 2^(s * scale * log2 e - lse log2 e):
+      // packed f32x2 FMA and adds, -lse read as broadcast 16-byte vectors,
+      // and 3 of every 8 exponential pairs on the FMA pipe (kColsumPoly) so
+      // that MUFU is not the only pipe doing the work
+      const float4* nl = reinterpret_cast<const float4*>(lse_s + sb * kBM);
+      const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
-      for (int q = 0; q < kBM; ++q) {
-        const float e = ex2_approx(fmaf(__uint_as_float(raw[q]), sl2, -ls[q]));
-        acc += (q < nvalid) ? e : 0.f;
+      for (int q4 = 0; q4 < kBM / 4; ++q4) {
+        const float4 L4 = nl[q4];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const int q = q4 * 4 + hh * 2;
+          const float2 a = __ffma2_rn(
+              make_float2(__uint_as_float(raw[q]), __uint_as_float(raw[q + 1])), sl2x2,
+              hh ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y));
+          float2 e;
+          if (((q >> 1) & 7) >= 8 - kColsumPoly) {
+            e = exp2_poly2(a);
+          } else {
+            e.x = ex2_approx(a.x);
+            e.y = ex2_approx(a.y);
+          }
+          if (hh)
+            acc1 = __fadd2_rn(acc1, e);
+          else
+            acc0 = __fadd2_rn(acc0, e);
+        }
       }
     }
+    const float acc = (acc0.x + acc0.y) + (acc1.x + acc1.y);
     if (ok && key0 + j < p.L) out[key0 + j] = acc;
   }
 
@@ -839,8 +917,8 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   if (can_split) {
-    // at most 2 * n_ctas split items of 128 rows exist: size the grid for them
-    launch_pdl(attn_split_merge_kernel, 2 * n_ctas, 256, 0, stream, fp, n_ctas);
+    // one warp per (split pair, tile, row): up to 64 warps per SM
+    launch_pdl(attn_split_merge_kernel, 8 * n_ctas, 256, 0, stream, fp, n_ctas);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }

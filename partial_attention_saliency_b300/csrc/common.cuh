@@ -22,14 +22,15 @@ __device__ __forceinline__ void report(int32_t* status, int code) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-// 16-byte streaming load, cached in L2 only.  Never the non-coherent
-// (ld.global.nc) path: with programmatic dependent launch a kernel is
-// resident while the previous kernel still writes, so no buffer is read-only
-// for a whole kernel lifetime and .nc could return stale L1 lines.  For the
-// same reason no kernel parameter of this library is __restrict__.
+// 16-byte streaming load that does not allocate in L1.  A coherent load,
+// never the non-coherent (ld.global.nc) path: with programmatic dependent
+// launch a kernel is resident while the previous kernel still runs, so no
+// buffer is read-only for a whole kernel lifetime, which .nc requires.  For
+// the same reason no kernel parameter of this library is __restrict__ and
+// scalar reads of buffers other kernels write use __ldca (coherent).
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
   uint4 r;
-  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+  asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                : "l"(p));
   return r;

@@ -102,14 +102,14 @@ __device__ __forceinline__ uint4 load_vec(const T* row, int vi, int V) {
 __device__ __forceinline__ bool row_valid(int b, int r, int R_max, int R_src,
                                           const int32_t* row_idx, const int32_t* count,
                                           int* row_out, bool* bad) {
-  int n = count ? __ldcg(count + b) : R_max;
+  int n = count ? __ldca(count + b) : R_max;
   *bad = false;
   if (n < 0 || n > R_max) {
     *bad = true;
     n = n < 0 ? 0 : R_max;
   }
   if (r >= n) return false;
-  const int row = row_idx ? __ldcg(row_idx + (int64_t)b * R_max + r) : r;
+  const int row = row_idx ? __ldca(row_idx + (int64_t)b * R_max + r) : r;
   if (row < 0 || row >= R_src) {
     *bad = true;
     return false;
@@ -282,7 +282,7 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
   if (!ok) return;
   int col = r;
   if (out_idx != nullptr) {
-    col = __ldcg(out_idx + br);
+    col = __ldca(out_idx + br);
     if (col < 0 || col >= out_cols) {
       if (lane == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
       return;
@@ -296,7 +296,7 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
   for (int c = lane; c < nchunks; c += 32) {
     const ConfPartial* src = ws + br * nchunks + c;
     ConfPartial w;
-    const float4 raw = __ldcg(reinterpret_cast<const float4*>(src));
+    const float4 raw = __ldca(reinterpret_cast<const float4*>(src));
     w.m1 = raw.x;
     w.m2 = raw.y;
     w.l = raw.z;
@@ -324,17 +324,19 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
 // Streaming variant (rows 16-byte aligned, V * sizeof(T) a multiple of 16):
 // one persistent CTA per SM.  A producer warp copies 64 KB row chunks with
 // cp.async.bulk into a 3-stage shared-memory ring (up to 192 KB of HBM reads
-// in flight per SM).  Each of the 8 consumer warps reduces its own 8 KB slice
-// of every staged chunk (128 elements per lane) with warp shuffles only, no
-// block barrier, and writes one ConfPartial per slice; the merge kernel folds
-// the 8 slices x chunks of a row.  The exponentials run on packed f32x2
-// FMA/add with MUFU ex2.  Work items are (row, chunk) pairs dealt round-robin
-// to the CTAs.
-constexpr int kStreamWarps = 8;                          // consumer warps
+// in flight per SM) and tells the consumers which (row, chunk) each stage
+// holds through shared memory.  Each of the 16 consumer warps reduces its own
+// 4 KB slice of every staged chunk (64 elements per lane) with warp shuffles
+// only, no block barrier, and writes one ConfPartial per slice; the merge
+// kernel folds the 16 slices x chunks of a row.  The exponentials run on
+// packed f32x2 FMA/add with MUFU ex2 (the MUFU pipe is far from saturated
+// here; the limit is latency, hence four consumer warps per scheduler).
+// Work items are (row, chunk) pairs dealt round-robin to the CTAs.
+constexpr int kStreamWarps = 16;                         // consumer warps
 constexpr int kStreamThreads = (kStreamWarps + 1) * 32;
 constexpr int kStreamStages = 3;
 constexpr uint32_t kStreamChunkBytes = 65536;
-constexpr uint32_t kStreamSliceBytes = kStreamChunkBytes / kStreamWarps;  // 8 KB per warp
+constexpr uint32_t kStreamSliceBytes = kStreamChunkBytes / kStreamWarps;  // 4 KB per warp
 constexpr int kStreamVPL = kStreamSliceBytes / 16 / 32;                   // 16-byte vectors per lane
 constexpr uint32_t kStreamSmem = kStreamStages * kStreamChunkBytes + 256 + 1024;
 
@@ -446,9 +448,7 @@ __device__ __forceinline__ Top2Sum lane_reduce(const uint4 (&x)[kStreamVPL]) {
         for (int k = 0; k < 4; ++k) {
           const float2 z = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
           const float2 arg = __ffma2_rn(z, l2e, neg);
-          // a quarter of the exponentials on the FMA pipe, the rest on MUFU
-          const float2 e = (k == 3) ? exp2_poly2(arg)
-                                    : make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
+          const float2 e = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
           if (k & 1)
             acc1 = __fadd2_rn(acc1, e);
           else
@@ -508,11 +508,11 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
         const int b = br / R_max, r = br - b * R_max;
         if (b != cached_b) {
           cached_b = b;
-          n_b = count ? __ldcg(count + b) : R_max;
+          n_b = count ? __ldca(count + b) : R_max;
           n_b = n_b < 0 ? 0 : (n_b > R_max ? R_max : n_b);  // the merge kernel reports it
         }
         if (r >= n_b) continue;
-        const int row = row_idx ? __ldcg(row_idx + br) : r;
+        const int row = row_idx ? __ldca(row_idx + br) : r;
         if (row < 0 || row >= R_src) continue;  // the merge kernel reports it
         const int stage = j % kStreamStages;
         if (j >= kStreamStages &&

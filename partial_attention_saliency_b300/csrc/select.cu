@@ -174,8 +174,8 @@ compact_kernel(const float* cos, const uint8_t* locked, int Lw,
       const int p = start + tid * kCompactItems + k;
       bool a = false;
       if (p < Lw) {
-        a = !(__ldcg(c + p) >= tau);  // NaN cosine counts as salient
-        if (lk != nullptr && __ldcg(lk + p) != 0) a = false;
+        a = !(__ldca(c + p) >= tau);  // NaN cosine counts as salient
+        if (lk != nullptr && __ldca(lk + p) != 0) a = false;
       }
       act[k] = a;
       mine += a ? 1 : 0;

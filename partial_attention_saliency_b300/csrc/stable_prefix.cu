@@ -29,7 +29,7 @@ stable_prefix_kernel(const float* score, int L, int32_t* start,
   __shared__ int warp_min[kPrefixThreads / 32];
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = __ldcg(start + b);
+  const int s = __ldca(start + b);
   if (s < 0 || s > L) {
     if (tid == 0) {
       report(dev_status, DLLM_ERR_DEVICE_CHECK);
@@ -44,7 +44,7 @@ stable_prefix_kernel(const float* score, int L, int32_t* start,
 #pragma unroll
     for (int u = 0; u < kPrefixUnroll; ++u) {
       const int p = base + u * kPrefixThreads + tid;
-      v[u] = p < L ? __ldcg(row + p) : INFINITY;
+      v[u] = p < L ? __ldca(row + p) : INFINITY;
     }
 #pragma unroll
     for (int u = kPrefixUnroll - 1; u >= 0; --u) {
