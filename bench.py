@@ -80,7 +80,8 @@ def parse():
                     help="timed steps (default: about one second of steps)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["step_1k", "batch8_2k", "long_4k", "loop_b4_2k"],
+    ap.add_argument("--workload",
+                    choices=["step_1k", "batch8_2k", "long_4k", "long_4k_schedule", "loop_b4_2k"],
                     default="step_1k")
     ap.add_argument("--frac", type=float, default=0.25,
                     help="batch8_2k: active fraction of the 2048 positions")
@@ -236,6 +237,7 @@ class Workload:
     logit_rows: int
     default_steps: int
     desc: str
+    schedule: int = 0  # steps of a lock schedule (masks from lock_schedule), 0 = none
 
 
 def make_workload(args) -> Workload:
@@ -252,6 +254,13 @@ def make_workload(args) -> Workload:
                         args.pattern, 0.0, None, 0, 400,
                         f"partial step B{s.B} L{s.L} {s.H}x{s.d} heads, hidden {s.D}, "
                         f"{round(100 * args.frac)}% active ({args.pattern}), no logits")
+    if args.workload == "long_4k_schedule":
+        s = workloads.LONG_4K
+        return Workload("long_4k_schedule", s, s.L, "random", 0.0, "gather", s.L, 64 * 8,
+                        f"64-step schedule B{s.B} L{s.L} {s.H}x{s.d} heads, vocab {s.V}, "
+                        f"locked fraction rising linearly 0 -> 90% (nested locked sets), "
+                        f"logits of the active rows gathered from a [{s.L}, {s.V}] buffer",
+                        schedule=64)
     if args.workload == "long_4k":
         s = workloads.LONG_4K
         n_locked = round(args.locked * s.L)
@@ -301,6 +310,23 @@ def build_set(wl: Workload, seed: int, device):
     return d
 
 
+def lock_schedule(wl: Workload, seed: int):
+    """Nested locked sets of a linear schedule: at step t of T a fraction
+    0.9 t / (T - 1) of the window is locked, the positions locking in one
+    seeded random order.  Returns T uint8 masks [B, Lw] (CPU)."""
+    s = wl.shape
+    g = torch.Generator().manual_seed(seed)
+    order = [torch.randperm(s.Lw, generator=g) for _ in range(s.B)]
+    masks = []
+    for t in range(wl.schedule):
+        n_locked = round(0.9 * t / (wl.schedule - 1) * s.Lw)
+        m = torch.zeros((s.B, s.Lw), dtype=torch.uint8)
+        for b in range(s.B):
+            m[b, order[b][:n_locked]] = 1
+        masks.append(m)
+    return masks
+
+
 def set_bytes(d) -> int:
     return sum(t.numel() * t.element_size() for k, t in d.items()
                if isinstance(t, torch.Tensor) and t.is_cuda)
@@ -331,13 +357,16 @@ class Buffers:
         self.attn_split = aw > 0
 
 
-def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None):
-    """The six calls in order; optional events bracket each call."""
+def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None, locked=None):
+    """The six calls in order; optional events bracket each call.  ``locked``
+    overrides the set's locked mask (schedule steps)."""
     s = wl.shape
     w = s.win_start
     ev = events
+    if locked is None:
+        locked = d["locked"]
     if ev: ev[0].record(stream)
-    dl.dllm_saliency_select(d["cur"][:, w:], d["prev"][:, w:], s.tau, locked=d["locked"],
+    dl.dllm_saliency_select(d["cur"][:, w:], d["prev"][:, w:], s.tau, locked=locked,
                             idx_base=w, cos_out=bf.cos, idx_out=bf.idx, count_out=bf.count,
                             dev_status=bf.dev_status, stream=stream)
     if ev: ev[1].record(stream)
@@ -414,7 +443,7 @@ def algorithmic_work(wl: Workload, counts):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_step(wl: Workload, h, b: int):
+def oracle_step(wl: Workload, h, b: int, locked_mask=None):
     """The float64 oracle over batch row ``b`` of one step (what the GPU step
     computes for that row).  Returns the row's active count."""
     import numpy as np
@@ -423,7 +452,8 @@ def oracle_step(wl: Workload, h, b: int):
     w = s.win_start
     sl = slice(b, b + 1)
     f = lambda k: h[k][sl].double().numpy()  # noqa: E731
-    locked = None if h["locked"] is None else h["locked"][sl].numpy()
+    lk = h["locked"] if locked_mask is None else locked_mask
+    locked = None if lk is None else lk[sl].numpy()
     cur, prev = f("cur"), f("prev")
     cos, idx, count = oracle.saliency_select(cur[:, w:], prev[:, w:], s.tau, locked, idx_base=w)
     kc, vc = oracle.kv_scatter(f("k_cache"), f("v_cache"), f("k_new"), f("v_new"), idx, count)
@@ -456,16 +486,17 @@ def blas_threads():
         return os.cpu_count() or 1
 
 
-def cpu_baseline(wl: Workload, host, seconds, steps_cap=None):
+def cpu_baseline(wl: Workload, host, seconds, steps_cap=None, masks=None):
     """The float64 oracle, as it stands, on the host cores: batch rows of the
-    same step taken in turn until ``seconds`` have passed (or ``steps_cap``
-    batch rows), at least one."""
+    same step (of the schedule's steps in turn) taken in turn until
+    ``seconds`` have passed (or ``steps_cap`` batch rows), at least one."""
     times, rows, units = [], 0, 0
     t_begin = time.perf_counter()
     cpu_begin = time.process_time()
     while True:
         t0 = time.perf_counter()
-        units += oracle_step(wl, host, rows % wl.shape.B)
+        mask = None if masks is None else masks[(rows // wl.shape.B) % len(masks)]
+        units += oracle_step(wl, host, rows % wl.shape.B, mask)
         rows += 1
         times.append(time.perf_counter() - t0)
         if steps_cap is not None and rows >= steps_cap:
@@ -486,13 +517,15 @@ def reference_arm(args, rank):
         return 0
     wl = make_workload(args)
     host = build_set(wl, wl.shape.seed, torch.device("cpu"))["host"]
+    masks = lock_schedule(wl, wl.shape.seed + 5) if wl.schedule else None
     # warm-up rows (at most 3), then as many of the K timed rows as fit in
     # about 90 s of oracle time, at least 3: the run stays within minutes
-    _, wt, _ = cpu_baseline(wl, host, 0, steps_cap=max(1, min(args.warmup, 3)))
+    _, wt, _ = cpu_baseline(wl, host, 0, steps_cap=max(1, min(args.warmup, 3)), masks=masks)
     per_row = sum(wt) / len(wt)
     k = args.steps if args.steps is not None else 10
     res, times, units = cpu_baseline(wl, host, 0,
-                                     steps_cap=max(3, min(k, int(90.0 / max(per_row, 1e-6)))))
+                                     steps_cap=max(3, min(k, int(90.0 / max(per_row, 1e-6)))),
+                                     masks=masks)
     timed = sum(times)
     value = units / timed
     rows_per_step = wl.shape.B
@@ -542,12 +575,17 @@ def main():
         sets.append(build_set(wl, s.seed + 1000 * (rank * 16 + i), device))
     bf = Buffers(dl, wl, device)
     stream = torch.cuda.current_stream(device)
-    counts_per_set = []
-    for d in sets:
-        run_step(dl, wl, bf, d, stream)
+    masks_host = lock_schedule(wl, s.seed + 5) if wl.schedule else None
+    masks = None if masks_host is None else [m.to(device) for m in masks_host]
+    period = wl.schedule if wl.schedule else n_sets  # steps after which the inputs repeat
+    lk = lambda i: None if masks is None else masks[i % wl.schedule]  # noqa: E731
+    counts_per_step = []  # active rows of step i % period
+    for i in range(period):
+        run_step(dl, wl, bf, sets[i % n_sets], stream, locked=lk(i))
         torch.cuda.synchronize()
-        counts_per_set.append(bf.count.cpu().tolist())
+        counts_per_step.append(bf.count.cpu().tolist())
     assert int(bf.dev_status[0]) == 0, "device-side check failed"
+    mean_counts = [sum(c[b] for c in counts_per_step) / period for b in range(s.B)]
 
     # ---------------------------------------------------------------- device-timed
     # A graph of S steps is replayed K / S times back to back: no host launch
@@ -557,24 +595,25 @@ def main():
     # remove that overlap, so its per-call times are conservative) is then
     # replayed for the per-call breakdown.
     K = args.steps if args.steps is not None else wl.default_steps
-    S = min(K, 250)
+    S = wl.schedule if wl.schedule else min(K, 250)
     K = max(S, (K // S) * S)
     cap = torch.cuda.Stream(device)
     g_warm = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_warm, stream=cap):
         for i in range(args.warmup):
-            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream())
+            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream(), locked=lk(i))
     g_timed = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_timed, stream=cap):
         for i in range(S):
-            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream())
+            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream(), locked=lk(i))
     nev = len(ENTRY_ORDER) + 1
     ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)]
           for _ in range(S)]
     g_events = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_events, stream=cap):
         for i in range(S):
-            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream(), ev[i])
+            run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream(), ev[i],
+                     locked=lk(i))
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(torch.cuda.current_device())
@@ -600,7 +639,7 @@ def main():
         for j, n in enumerate(ENTRY_ORDER):
             per_entry[n] += ev[i][j].elapsed_time(ev[i][j + 1])
     events_step_ms = sum(per_entry.values()) / S
-    active_total = sum(sum(counts_per_set[i % n_sets]) for i in range(S)) * (K // S)
+    active_total = sum(sum(counts_per_step[i % period]) for i in range(S)) * (K // S)
     if pg:
         t = torch.tensor([elapsed_ms], device=device)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
@@ -613,7 +652,7 @@ def main():
 
     # ---------------------------------------------------------------- per entry point
     pk = peaks()
-    work = algorithmic_work(wl, counts_per_set[0])
+    work = algorithmic_work(wl, mean_counts)
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     kernels = {}
     for n in ENTRY_ORDER:
@@ -654,7 +693,7 @@ def main():
                            "between every two calls"})
 
     # ---------------------------------------------------------------- end to end
-    e2e = e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K)
+    e2e = e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K, lk, counts_per_step)
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -662,7 +701,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.desc, "name": wl.name, "batch": s.B, "seq_len": s.L,
                        "heads": s.H, "head_dim": s.d, "hidden": s.D, "vocab": s.V,
-                       "active_rows_per_step": sum(counts_per_set[0]),
+                       "active_rows_per_step": sum(mean_counts),
                        "l2": f"{n_sets} rotating input sets of {set_bytes(sets[0]) / 1e6:.0f} MB "
                              f"each (> 126 MB L2)",
                        "parallelism": "replicas (one independent step per GPU)"},
@@ -671,7 +710,7 @@ def main():
             "timing": f"{K} steps as {K // S} replays of a {S}-step CUDA graph",
             "us_per_step_with_call_events": events_step_ms * 1e3, "e2e": e2e}
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cb, _, _ = cpu_baseline(wl, sets[0]["host"], args.cpu_seconds)
+        cb, _, _ = cpu_baseline(wl, sets[0]["host"], args.cpu_seconds, masks=masks_host)
         line["cpu_baseline"] = cb
     if rank == 0:
         print(json.dumps(line), flush=True)
@@ -680,7 +719,7 @@ def main():
     return 0
 
 
-def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev):
+def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev, lk, counts_per_step):
     """Same metric through the public API with pinned host buffers: H2D of the
     step's fresh inputs and D2H of its results inside the timed region."""
     host_in = ["cur", "k_new", "v_new", "q"] + (["logits"] if wl.conf is not None else [])
@@ -703,7 +742,7 @@ def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev):
         for k in host_in:
             dst = d[k][:, :pinned[i % n_sets][k].shape[1]] if k == "logits" else d[k]
             dst.copy_(pinned[i % n_sets][k], non_blocking=True)
-        run_step(dl, wl, bf, d, stream)
+        run_step(dl, wl, bf, d, stream, locked=lk(i))
         for k, src in (("idx", bf.idx), ("count", bf.count), ("o", bf.o), ("lse", bf.lse),
                        ("colsum", bf.colsum), ("score", d["score"]), ("argmax", bf.argmax),
                        ("length", bf.length)):
@@ -726,8 +765,9 @@ def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev):
         t = torch.tensor([ms], device=device)
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
-    active = int(bf.count.sum().item()) * (pg.get_world_size() if pg else 1)
-    return {"value": active * K / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    active = sum(sum(counts_per_step[i % len(counts_per_step)]) for i in range(K))
+    active *= pg.get_world_size() if pg else 1
+    return {"value": active / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": ms / K}
 
 
