@@ -46,7 +46,6 @@ constexpr int kBM = 128;       // query rows per tile
 constexpr int kBN = 128;       // keys per tile
 constexpr int kHD = 128;       // head dim
 constexpr int kStages = 2;     // K/V (forward) or Q (column sums) ring depth
-constexpr int kThreads = 192;  // column-sum kernel: 6 warps
 constexpr uint32_t kBox = 16384;          // one 128-row x 64-dim bf16 box (swizzled)
 constexpr uint32_t kTile = 2 * kBox;      // 128 rows x 128 dims
 constexpr float kRescaleThreshold = 8.0f; // log2 units: P stays below 2^8
@@ -96,12 +95,6 @@ constexpr uint32_t kFwdSmem = kFwdBar + 256 + 1024;
 constexpr uint32_t kTmS = 0;     // + X * 128
 constexpr uint32_t kTmO = 256;   // + X * 128
 
-// shared-memory map of the column-sum kernel
-constexpr uint32_t kCsK = 0;
-constexpr uint32_t kCsQ = kTile;                          // + s * kTile
-constexpr uint32_t kCsLse = kTile + kStages * kTile;      // 2 x 128 floats
-constexpr uint32_t kCsBar = kCsLse + 2 * kBM * 4;
-constexpr uint32_t kCsSmem = kCsBar + 256 + 1024;
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   uint32_t r;
@@ -116,10 +109,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, r);
 }
 
-// Named barrier among the four column-sum warps (ids 2-5).
-__device__ __forceinline__ void epi_bar_sync() {
-  asm volatile("bar.sync 1, 128;" ::: "memory");
-}
 
 // Work plan shared by the forward and merge kernels, computed on the device
 // from the active counts.  A work item is a pair of query tiles of 128
@@ -659,20 +648,39 @@ attn_split_merge_kernel(FwdParams p, int n_ctas) {
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+// Column sums, the second normalised pass.  One CTA per (NK consecutive key
+// tiles of 128 keys, head, batch row); NK in {1, 2, 4} is chosen on the host
+// so that the grid still covers the SMs.  Warps 0..4NK-1 form NK softmax
+// warpgroups (key tile X = warp / 4; thread = one key, its TMEM lane), warp
+// 4NK is the TMA producer (the NK key tiles once, then the query tiles of
+// 128 active rows into a 2-stage ring), warp 4NK+1 issues the MMAs:
+// S_X^T = K_X Q^T for every key tile X of the CTA into its own 128 TMEM
+// columns, so one query tile feeds NK key tiles and NK warps per scheduler
+// hide each other's latency.  A thread reads its S row in chunks of 32
+// queries, releases S_X after the last chunk is read, and adds
+// 2^(s * scale * log2 e - lse * log2 e) over the active rows; -lse (log2
+// units, -inf for padded rows) sits in a warp-private shared buffer,
+// prefetched one query tile ahead.  Each key has one owner thread: no
+// atomics, run-to-run identical.
+template <int NK>
+__global__ void __launch_bounds__((4 * NK + 2) * 32, 1)
 attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                       ColsumParams p) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  const int kt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  constexpr int kSoftWarps = 4 * NK;
+  constexpr uint32_t kTmCols = NK == 1 ? 128 : NK * 128;
+  const int kg = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   int n = __ldca(p.count + b);
   n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
   const int nqt = (n + kBM - 1) / kBM;
-  const int key0 = kt * kBN;
+  const int nkt = (p.L + kBN - 1) / kBN;
+  const int nk = min(NK, nkt - kg * NK);  // key tiles of this CTA
+  const int key_base = kg * NK * kBN;
   float* out = p.colsum + ((int64_t)b * p.H + h) * p.L;
   if (nqt == 0) {
-    for (int j = threadIdx.x; j < kBN; j += blockDim.x)
-      if (key0 + j < p.L) out[key0 + j] = 0.f;
+    for (int j = threadIdx.x; j < NK * kBN; j += blockDim.x)
+      if (key_base + j < p.L) out[key_base + j] = 0.f;
     return;
   }
 
@@ -680,52 +688,59 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw_addr);
-  const uint32_t sK = base + kCsK;
-  float* lse_s = reinterpret_cast<float*>(gbase + kCsLse);  // [2][128]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kCsBar);
+  constexpr uint32_t oQ = NK * kTile;                       // Q ring
+  constexpr uint32_t oL = oQ + kStages * kTile;             // warp-private -lse buffers
+  constexpr uint32_t oBar = oL + kSoftWarps * 2 * kBM * 4;
+  float* lse_w = reinterpret_cast<float*>(gbase + oL);      // [warp][2][128]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + oBar);
   uint64_t* k_full = bars + 0;
-  uint64_t* q_full = bars + 1;   // [kStages]
-  uint64_t* q_empty = bars + 3;  // [kStages]
-  uint64_t* s_full = bars + 5;   // [2]
-  uint64_t* s_free = bars + 7;   // [2]
-  uint64_t* mma_done = bars + 9;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 10);
-  int* abort_flag = reinterpret_cast<int*>(bars + 11);
+  uint64_t* q_full = bars + 1;             // [kStages]
+  uint64_t* q_empty = bars + 1 + kStages;  // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;        // [NK]
+  uint64_t* s_free = bars + 1 + 2 * kStages + NK;   // [NK]
+  uint64_t* mma_done = bars + 1 + 2 * kStages + 2 * NK;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mma_done + 1);
+  int* abort_flag = reinterpret_cast<int*>(mma_done + 2);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int kWarpT = kSoftWarps, kWarpM = kSoftWarps + 1;
   if (threadIdx.x == 0) {
     mbar_init(k_full, 1);
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&q_full[s], 1);
       mbar_init(&q_empty[s], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+    for (int x = 0; x < NK; ++x) {
+      mbar_init(&s_full[x], 1);
+      mbar_init(&s_free[x], 4);
     }
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
-  if (warp == 0) tmem_alloc(tmem_slot, 256);
+  if (warp == kWarpT) tmem_alloc(tmem_slot, kTmCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort = abort_flag;
 
-  if (warp == 0) {
+  if (warp == kWarpT) {
+    // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
-      mbar_expect_tx(k_full, kTile);
-      tma_load_4d(gbase + kCsK, &tk, k_full, 0, h, key0, b);
-      tma_load_4d(gbase + kCsK + kBox, &tk, k_full, 64, h, key0, b);
+      mbar_expect_tx(k_full, (uint32_t)nk * kTile);
+      for (int x = 0; x < nk; ++x) {
+        const int key0 = key_base + x * kBN;
+        tma_load_4d(gbase + x * kTile, &tk, k_full, 0, h, key0, b);
+        tma_load_4d(gbase + x * kTile + kBox, &tk, k_full, 64, h, key0, b);
+      }
       int issued = 0;
       for (int it = 0; it < nqt; ++it) {
         const int s = it % kStages;
         if (it >= kStages && !mbar_wait(&q_empty[s], ((it / kStages) - 1) & 1, abort)) break;
-        uint8_t* qdst = gbase + kCsQ + s * kTile;
+        uint8_t* qdst = gbase + oQ + s * kTile;
         mbar_expect_tx(&q_full[s], kTile);
         tma_load_4d(qdst, &tq, &q_full[s], 0, h, it * kBM, b);
         tma_load_4d(qdst + kBox, &tq, &q_full[s], 64, h, it * kBM, b);
@@ -737,106 +752,122 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         mbar_wait(&q_full[it % kStages], (it / kStages) & 1, &none);
       if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
-  } else if (warp == 1) {
+  } else if (warp == kWarpM) {
+    // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc_bf16_f32(kBN, kBM, false, false);
       bool ok = mbar_wait(k_full, 0, abort);
       for (int it = 0; ok && it < nqt; ++it) {
-        const int s = it % kStages, sb = it & 1;
+        const int s = it % kStages;
         if (!mbar_wait(&q_full[s], (it / kStages) & 1, abort)) break;
-        if (it >= 2 && !mbar_wait(&s_free[sb], ((it >> 1) - 1) & 1, abort)) break;
-        tc_fence_after();
-        const uint32_t sQ = base + kCsQ + s * kTile;
+        const uint32_t sQ = base + oQ + s * kTile;
+        for (int x = 0; x < nk; ++x) {
+          if (it > 0 && !mbar_wait(&s_free[x], (it - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sK = base + x * kTile;
 #pragma unroll
-        for (int kk = 0; kk < kHD / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          mma_bf16_ss(tmem + sb * kBM, smem_desc_sw128(sK + off, 16, 1024),
-                      smem_desc_sw128(sQ + off, 16, 1024), id, kk > 0);
+          for (int kk = 0; kk < kHD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_bf16_ss(tmem + x * kBN, smem_desc_sw128(sK + off, 16, 1024),
+                        smem_desc_sw128(sQ + off, 16, 1024), id, kk > 0);
+          }
+          mma_commit(&s_full[x]);
         }
-        mma_commit(&s_full[sb]);
-        mma_commit(&q_empty[s]);
+        if (ok) mma_commit(&q_empty[s]);
       }
       mma_commit(mma_done);
       int none = 0;
       mbar_wait(mma_done, 0, &none);
       if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
-  } else {
+  } else if (warp / 4 < nk) {
+    // ------------------------------------------------------------ softmax warps
+    const int x = warp >> 2;
     const int quarter = warp & 3;
-    const int j = quarter * 32 + lane;  // key row of this thread
-    const int t = threadIdx.x - 64;     // 0..127 for the lse loads
-    const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+    const int j = quarter * 32 + lane;  // key of this thread within its tile
+    const uint32_t tS = tmem + ((uint32_t)(quarter * 32) << 16) + x * kBN;
     const float* lse_g = p.lse + ((int64_t)b * p.H + h) * p.M_max;
+    float* lbuf = lse_w + warp * 2 * kBM;
     const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+    // -lse (log2 units) of query rows lane + 32 q of tile it, -inf past the count
+    auto load_lse = [&](int it, float (&v)[4]) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int i = it * kBM + q * 32 + lane;
+        v[q] = (it < nqt && i < n) ? -__ldca(lse_g + i) * kLog2e : -INFINITY;
+      }
+    };
+    float nl[4];
+    load_lse(0, nl);
     bool ok = true;
-    // -lse in log2 units of query row it * 128 + t; padded rows get -inf, so
-    // their terms vanish.  Loaded one query tile ahead, so that the load
-    // latency overlaps the previous tile's work.
-    float nlse = t < n ? -__ldca(lse_g + t) * kLog2e : -INFINITY;
-    for (int it = 0; it < nqt; ++it) {
-      // every epilogue thread passes the named barrier on every iteration,
-      // also after an abort, so the barrier can never wait for a thread that left
-      const int sb = it & 1;
-      lse_s[sb * kBM + t] = nlse;
-      epi_bar_sync();
-      const int inext = (it + 1) * kBM + t;
-      nlse = (it + 1 < nqt && inext < n) ? -__ldca(lse_g + inext) * kLog2e : -INFINITY;
-      if (!ok) continue;
-      if (!warp_wait(&s_full[sb], (it >> 1) & 1, abort)) {
+    for (int it = 0; ok && it < nqt; ++it) {
+      float* lb = lbuf + (it & 1) * kBM;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) lb[q * 32 + lane] = nl[q];
+      __syncwarp();
+      load_lse(it + 1, nl);  // the next tile's values, while this tile is worked on
+      if (!warp_wait(&s_full[x], it & 1, abort)) {
         ok = false;
-        continue;
+        break;
       }
       tc_fence_after();
-      uint32_t raw[kBM];
 #pragma unroll
-      for (int c = 0; c < kBM / 32; ++c)
-        tmem_ld_32x32b_x32(tmem + lane_base + sb * kBM + c * 32,
-                           *reinterpret_cast<uint32_t(*)[32]>(&raw[c * 32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[sb]);
-      // sum over the tile's query rows of 2^(s * scale * log2 e - lse log2 e):
-      // packed f32x2 FMA and adds, -lse read as broadcast 16-byte vectors,
-      // and 3 of every 8 exponential pairs on the FMA pipe (kColsumPoly) so
-      // that MUFU is not the only pipe doing the work
-      const float4* nl = reinterpret_cast<const float4*>(lse_s + sb * kBM);
-      const float2 sl2x2 = make_float2(sl2, sl2);
+      for (int c = 0; c < kBM / 32; ++c) {
+        uint32_t raw[32];
+        tmem_ld_32x32b_x32(tS + c * 32, raw);
+        tmem_ld_wait();
+        if (c == kBM / 32 - 1) {  // S_X is read: the next query tile may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[x]);
+        }
+        const float4* nl4 = reinterpret_cast<const float4*>(lb + c * 32);
 #pragma unroll
-      for (int q4 = 0; q4 < kBM / 4; ++q4) {
-        const float4 L4 = nl[q4];
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 L4 = nl4[q4];
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int q = q4 * 4 + hh * 2;
-          const float2 a = __ffma2_rn(
-              make_float2(__uint_as_float(raw[q]), __uint_as_float(raw[q + 1])), sl2x2,
-              hh ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y));
-          float2 e;
-          if (((q >> 1) & 7) >= 8 - kColsumPoly) {
-            e = exp2_poly2(a);
-          } else {
-            e.x = ex2_approx(a.x);
-            e.y = ex2_approx(a.y);
+          for (int hh = 0; hh < 2; ++hh) {
+            const int q = q4 * 4 + hh * 2;
+            const float2 a = __ffma2_rn(
+                make_float2(__uint_as_float(raw[q]), __uint_as_float(raw[q + 1])), sl2x2,
+                hh ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y));
+            float2 e;
+            if (((q >> 1) & 7) >= 8 - kColsumPoly) {
+              e = exp2_poly2(a);
+            } else {
+              e.x = ex2_approx(a.x);
+              e.y = ex2_approx(a.y);
+            }
+            if (hh)
+              acc1 = __fadd2_rn(acc1, e);
+            else
+              acc0 = __fadd2_rn(acc0, e);
           }
-          if (hh)
-            acc1 = __fadd2_rn(acc1, e);
-          else
-            acc0 = __fadd2_rn(acc0, e);
         }
       }
+      __syncwarp();  // lb is rewritten two tiles later
     }
-    const float acc = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-    if (ok && key0 + j < p.L) out[key0 + j] = acc;
+    const int key = key_base + x * kBN + j;
+    if (ok && key < p.L) out[key] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kWarpT) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, kTmCols);
   }
   if (threadIdx.x == 0 && *abort) report(p.dev_status, DLLM_ERR_TIMEOUT);
+}
+
+template <int NK>
+constexpr uint32_t colsum_smem_bytes() {
+  return NK * kTile + kStages * kTile + 4 * NK * 2 * kBM * 4 + 256 + 1024;
 }
 
 // ------------------------------------------------------------------ host side
@@ -929,15 +960,35 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
 cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, int M_max,
                              const int32_t* count, float scale, const float* lse, float* colsum,
                              int32_t* dev_status, cudaStream_t stream) {
-  cudaError_t e =
-      ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel), (int)kCsSmem);
-  if (e != cudaSuccess) return e;
   CUtensorMap tq, tk;
   if (!make_rows_map(&tq, q, B, M_max, H) || !make_rows_map(&tk, k, B, L, H))
     return cudaErrorInvalidValue;
   ColsumParams cp{count, lse, colsum, L, H, M_max, scale * kLog2e, dev_status};
-  dim3 cgrid((L + kBN - 1) / kBN, H, B);
-  launch_pdl(attn_colsum_tc_kernel, cgrid, kThreads, kCsSmem, stream, tq, tk, cp);
+  // Key tiles per CTA: 4 (one query tile feeds four key tiles, four warps
+  // per scheduler) while that still leaves two CTAs per SM, else fewer.
+  const int nkt = (L + kBN - 1) / kBN;
+  const int64_t bh = (int64_t)B * H;
+  const int sms = num_sms();
+  cudaError_t e;
+  if (bh * ((nkt + 3) / 4) >= 2 * sms) {
+    e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel<4>),
+                          (int)colsum_smem_bytes<4>());
+    if (e != cudaSuccess) return e;
+    dim3 grid((nkt + 3) / 4, H, B);
+    launch_pdl(attn_colsum_tc_kernel<4>, grid, 18 * 32, colsum_smem_bytes<4>(), stream, tq, tk, cp);
+  } else if (bh * ((nkt + 1) / 2) >= sms) {
+    e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel<2>),
+                          (int)colsum_smem_bytes<2>());
+    if (e != cudaSuccess) return e;
+    dim3 grid((nkt + 1) / 2, H, B);
+    launch_pdl(attn_colsum_tc_kernel<2>, grid, 10 * 32, colsum_smem_bytes<2>(), stream, tq, tk, cp);
+  } else {
+    e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel<1>),
+                          (int)colsum_smem_bytes<1>());
+    if (e != cudaSuccess) return e;
+    dim3 grid(nkt, H, B);
+    launch_pdl(attn_colsum_tc_kernel<1>, grid, 6 * 32, colsum_smem_bytes<1>(), stream, tq, tk, cp);
+  }
   return cudaGetLastError();
 }
 
