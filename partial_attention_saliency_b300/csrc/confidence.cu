@@ -372,93 +372,80 @@ __device__ __forceinline__ bool vec_contains(const uint4& v, float m) {
   }
 }
 
-struct Top2Sum {
-  float m1, m2, l;
-};
-
-__device__ __forceinline__ Top2Sum merge_t2s(const Top2Sum& a, const Top2Sum& b) {
-  Top2Sum r;
-  r.m1 = fmaxf(a.m1, b.m1);
-  r.m2 = fmaxf(fminf(a.m1, b.m1), fmaxf(a.m2, b.m2));
-  if (r.m1 == -INFINITY) {
-    r.l = 0.f;
-  } else {
-    r.l = a.l * ex2_approx((a.m1 - r.m1) * kLog2e) + b.l * ex2_approx((b.m1 - r.m1) * kLog2e);
-  }
-  return r;
-}
-
-// Lane-local top-2 and sum of exp(z - own max) over the lane's vectors.
+// Lane top-1 and top-2 over the lane's vectors (packed bf16x2 pairs of
+// (max, second) in four independent chains for bf16).
 template <typename T>
-__device__ __forceinline__ Top2Sum lane_reduce(const uint4 (&x)[kStreamVPL]) {
+__device__ __forceinline__ void lane_top2(const uint4 (&x)[kStreamVPL], float* m1, float* m2) {
   constexpr int E = vec_elems<T>();
-  Top2Sum t;
   if constexpr (std::is_same<T, float>::value) {
-    t.m1 = -INFINITY;
-    t.m2 = -INFINITY;
+    float t1 = -INFINITY, t2 = -INFINITY;
 #pragma unroll
     for (int u = 0; u < kStreamVPL; ++u)
 #pragma unroll
       for (int e = 0; e < E; ++e) {
         const float z = elem_of<T>(x[u], e);
-        t.m2 = fmaxf(t.m2, fminf(t.m1, z));
-        t.m1 = fmaxf(t.m1, z);
+        t2 = fmaxf(t2, fminf(t1, z));
+        t1 = fmaxf(t1, z);
       }
-    float lacc[4] = {0.f, 0.f, 0.f, 0.f};
-    if (t.m1 != -INFINITY) {
-      const float neg = -t.m1 * kLog2e;
-#pragma unroll
-      for (int u = 0; u < kStreamVPL; ++u)
-#pragma unroll
-        for (int e = 0; e < E; ++e)
-          lacc[e & 3] += ex2_approx(fmaf(elem_of<T>(x[u], e), kLog2e, neg));
-    }
-    t.l = (lacc[0] + lacc[1]) + (lacc[2] + lacc[3]);
+    *m1 = t1;
+    *m2 = t2;
   } else {
-    // packed bf16x2 (max, second) in four independent chains
     const __nv_bfloat162 ninf =
         __halves2bfloat162(__ushort_as_bfloat16(0xff80), __ushort_as_bfloat16(0xff80));
-    __nv_bfloat162 m1[4] = {ninf, ninf, ninf, ninf}, m2[4] = {ninf, ninf, ninf, ninf};
+    __nv_bfloat162 a1[4] = {ninf, ninf, ninf, ninf}, a2[4] = {ninf, ninf, ninf, ninf};
 #pragma unroll
     for (int u = 0; u < kStreamVPL; ++u) {
       const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const __nv_bfloat162 z = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-        m2[k] = __hmax2(m2[k], __hmin2(m1[k], z));
-        m1[k] = __hmax2(m1[k], z);
+        a2[k] = __hmax2(a2[k], __hmin2(a1[k], z));
+        a1[k] = __hmax2(a1[k], z);
       }
     }
 #pragma unroll
     for (int k = 1; k < 4; ++k) {
-      m2[0] = __hmax2(__hmax2(m2[0], m2[k]), __hmin2(m1[0], m1[k]));
-      m1[0] = __hmax2(m1[0], m1[k]);
+      a2[0] = __hmax2(__hmax2(a2[0], a2[k]), __hmin2(a1[0], a1[k]));
+      a1[0] = __hmax2(a1[0], a1[k]);
     }
-    const float a = __bfloat162float(m1[0].x), c = __bfloat162float(m1[0].y);
-    t.m1 = fmaxf(a, c);
-    t.m2 = fmaxf(fminf(a, c), fmaxf(__bfloat162float(m2[0].x), __bfloat162float(m2[0].y)));
+    const float p = __bfloat162float(a1[0].x), q = __bfloat162float(a1[0].y);
+    *m1 = fmaxf(p, q);
+    *m2 = fmaxf(fminf(p, q), fmaxf(__bfloat162float(a2[0].x), __bfloat162float(a2[0].y)));
+  }
+}
+
+// Lane sum of 2^(z log2 e + nm) over the lane's vectors (nm = -M log2 e).
+template <typename T>
+__device__ __forceinline__ float lane_sumexp(const uint4 (&x)[kStreamVPL], float nm) {
+  if constexpr (std::is_same<T, float>::value) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int u = 0; u < kStreamVPL; ++u) {
+      acc[0] += ex2_approx(fmaf(__uint_as_float(x[u].x), kLog2e, nm));
+      acc[1] += ex2_approx(fmaf(__uint_as_float(x[u].y), kLog2e, nm));
+      acc[2] += ex2_approx(fmaf(__uint_as_float(x[u].z), kLog2e, nm));
+      acc[3] += ex2_approx(fmaf(__uint_as_float(x[u].w), kLog2e, nm));
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+  } else {
+    const float2 l2e = make_float2(kLog2e, kLog2e);
+    const float2 n2 = make_float2(nm, nm);
     float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-    if (t.m1 != -INFINITY) {
-      const float2 l2e = make_float2(kLog2e, kLog2e);
-      const float2 neg = make_float2(-t.m1 * kLog2e, -t.m1 * kLog2e);
 #pragma unroll
-      for (int u = 0; u < kStreamVPL; ++u) {
-        const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+    for (int u = 0; u < kStreamVPL; ++u) {
+      const uint32_t w[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const float2 z = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
-          const float2 arg = __ffma2_rn(z, l2e, neg);
-          const float2 e = make_float2(ex2_approx(arg.x), ex2_approx(arg.y));
-          if (k & 1)
-            acc1 = __fadd2_rn(acc1, e);
-          else
-            acc0 = __fadd2_rn(acc0, e);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const float2 a = __ffma2_rn(make_float2(bf16_lo(w[k]), bf16_hi(w[k])), l2e, n2);
+        const float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+        if (k & 1)
+          acc1 = __fadd2_rn(acc1, e);
+        else
+          acc0 = __fadd2_rn(acc0, e);
       }
     }
-    t.l = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    return (acc0.x + acc0.y) + (acc1.x + acc1.y);
   }
-  return t;
 }
 
 template <typename T>
@@ -574,36 +561,39 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[stage]);  // this warp's slice is in registers
-    Top2Sum t = lane_reduce<T>(x);
-    const float own_max = t.m1;
+    // Slice top-2 first (lane chains, then a shuffle tree), then the sum of
+    // exp(z - M) relative to the slice maximum M directly, so no partial
+    // sums need rescaling; lanes holding M find its lowest position.
+    float own_max, own_2;
+    lane_top2<T>(x, &own_max, &own_2);
+    float t1 = own_max, t2 = own_2;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
-      Top2Sum q;
-      q.m1 = __shfl_xor_sync(0xffffffffu, t.m1, o);
-      q.m2 = __shfl_xor_sync(0xffffffffu, t.m2, o);
-      q.l = __shfl_xor_sync(0xffffffffu, t.l, o);
-      t = merge_t2s(t, q);
+      const float o1 = __shfl_xor_sync(0xffffffffu, t1, o);
+      const float o2 = __shfl_xor_sync(0xffffffffu, t2, o);
+      t2 = fmaxf(fminf(t1, o1), fmaxf(t2, o2));
+      t1 = fmaxf(t1, o1);
     }
+    const float lsum = t1 == -INFINITY ? 0.f : warp_sum(lane_sumexp<T>(x, -t1 * kLog2e));
     int arg = INT_MAX;
-    if (own_max == t.m1 && own_max != -INFINITY) {
-      // Only lanes holding the slice maximum search (usually one lane): find
-      // the first vector containing it with a cheap per-vector test, then
-      // the first element in that vector.  Indices ascend with u, then e.
+    if (own_max == t1 && own_max != -INFINITY) {
+      // usually one lane: the first vector containing the maximum, then the
+      // first element in it (indices ascend with u, then e)
 #pragma unroll
       for (int u = 0; u < kStreamVPL; ++u) {
-        if (arg == INT_MAX && vec_contains<T>(x[u], t.m1)) {
+        if (arg == INT_MAX && vec_contains<T>(x[u], t1)) {
 #pragma unroll
           for (int e = E - 1; e >= 0; --e)
-            if (elem_of<T>(x[u], e) == t.m1) arg = s0 + (u * 32 + lane) * E + e;
+            if (elem_of<T>(x[u], e) == t1) arg = s0 + (u * 32 + lane) * E + e;
         }
       }
     }
     arg = __reduce_min_sync(0xffffffffu, arg);
     if (lane == 0) {
       ConfPartial out;
-      out.m1 = t.m1;
-      out.m2 = t.m2;
-      out.l = t.l;
+      out.m1 = t1;
+      out.m2 = t2;
+      out.l = lsum;
       out.arg = arg;
       ws[((int64_t)br * nchunks + c) * kStreamWarps + warp] = out;
     }
