@@ -331,7 +331,9 @@ __global__ void conf_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
 // kernel folds the 16 slices x chunks of a row.  The exponentials run on
 // packed f32x2 FMA/add with MUFU ex2 (the MUFU pipe is far from saturated
 // here; the limit is latency, hence four consumer warps per scheduler).
-// Work items are (row, chunk) pairs dealt round-robin to the CTAs.
+// Work items are the valid (row, chunk) pairs in row-major order, dealt
+// round-robin to the CTAs (neighbouring chunks stream at the same time).
+constexpr int kStreamMaxB = 64;  // batch rows whose counts are staged in shared memory
 constexpr int kStreamWarps = 16;                         // consumer warps
 constexpr int kStreamThreads = (kStreamWarps + 1) * 32;
 constexpr int kStreamStages = 3;
@@ -470,6 +472,7 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
   // (batch row * R_max + row, chunk) of each staged chunk; br < 0 ends the stream
   int2* stage_info = reinterpret_cast<int2*>(abort_flag + 2);
 
+  __shared__ int s_cnt[kStreamMaxB];  // clamped counts of the first batch rows
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) {
     for (int s = 0; s < kStreamStages; ++s) {
@@ -479,6 +482,10 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
     *abort_flag = 0;
     fence_barrier_init();
   }
+  for (int b = tid; b < B && b < kStreamMaxB; b += blockDim.x) {
+    const int n = count ? __ldca(count + b) : R_max;
+    s_cnt[b] = n < 0 ? 0 : (n > R_max ? R_max : n);
+  }
   __syncthreads();
   volatile int* abort = abort_flag;
 
@@ -487,18 +494,25 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
     // The producer alone reads counts and row indices; the consumers learn
     // which row and chunk each stage holds from stage_info.
     if (lane == 0) {
-      const int total = B * R_max * nchunks;  // < 2^31 (checked on the host)
-      int j = 0, cached_b = -1, n_b = 0;
+      // Valid items only, in row-major order ((b, r < count[b], chunk)),
+      // dealt round-robin: at any time the CTAs stream neighbouring chunks.
+      auto cnt = [&](int b) {
+        if (b < kStreamMaxB) return s_cnt[b];
+        int n = count ? __ldca(count + b) : R_max;
+        return n < 0 ? 0 : (n > R_max ? R_max : n);  // out of range: reported by the merge kernel
+      };
+      int64_t rows = 0;
+      for (int b = 0; b < B; ++b) rows += cnt(b);
+      const int64_t total = rows * nchunks;
+      int j = 0, b = 0;
+      int64_t row_base = 0;  // valid rows before batch row b
       bool ok = true;
-      for (int v = blockIdx.x; v < total; v += gridDim.x) {
-        const int br = v / nchunks, c = v - br * nchunks;
-        const int b = br / R_max, r = br - b * R_max;
-        if (b != cached_b) {
-          cached_b = b;
-          n_b = count ? __ldca(count + b) : R_max;
-          n_b = n_b < 0 ? 0 : (n_b > R_max ? R_max : n_b);  // the merge kernel reports it
-        }
-        if (r >= n_b) continue;
+      for (int64_t v = blockIdx.x; v < total; v += gridDim.x) {
+        const int64_t vr = v / nchunks;
+        const int c = (int)(v - vr * nchunks);
+        while (vr >= row_base + cnt(b)) row_base += cnt(b++);
+        const int r = (int)(vr - row_base);
+        const int br = b * R_max + r;
         const int row = row_idx ? __ldca(row_idx + br) : r;
         if (row < 0 || row >= R_src) continue;  // the merge kernel reports it
         const int stage = j % kStreamStages;
