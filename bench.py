@@ -65,11 +65,11 @@ KERNELS = {  # kernels each entry point launches, and the source they come from
 # it was captured with; otherwise traffic is null.
 TRAFFIC = {
     # (workload, entry point): {"bytes": ..., "src_sha": first 16 hex of sha256}
-    ("step_1k", "dllm_confidence"): {"bytes": 133093376, "src_sha": "c08e7746f3bdce9b"},
-    ("batch8_2k_f50_random", "dllm_partial_attention"): {"bytes": 386689792,
-                                                          "src_sha": "17d490fa7390867e"},
-    ("batch8_2k_f05_random", "dllm_partial_attention"): {"bytes": 284424192,
-                                                          "src_sha": "17d490fa7390867e"},
+    ("step_1k", "dllm_confidence"): {"bytes": 133703936, "src_sha": "8852f06b7bb1aac3"},
+    ("batch8_2k_f50_random", "dllm_partial_attention"): {"bytes": 386810368,
+                                                          "src_sha": "e7e48f69adabdd83"},
+    ("batch8_2k_f05_random", "dllm_partial_attention"): {"bytes": 284102912,
+                                                          "src_sha": "e7e48f69adabdd83"},
 }
 
 
