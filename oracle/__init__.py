@@ -18,5 +18,8 @@ from .dllm_oracle import (  # noqa: F401
     kv_scatter,
     partial_attention,
     stable_prefix,
+    lock_kl,
+    lock_decision,
+    adaptive_prefix,
     step,
 )

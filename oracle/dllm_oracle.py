@@ -46,6 +46,9 @@ __all__ = [
     "kv_scatter",
     "partial_attention",
     "stable_prefix",
+    "lock_kl",
+    "lock_decision",
+    "adaptive_prefix",
     "step",
 ]
 
@@ -273,6 +276,122 @@ def stable_prefix(score, start, tau: float, min_commit: bool = True):
             k = 1
         out[b] = k
     return out
+
+
+# --------------------------------------------------------------------------
+# Lock criterion (SureLock) and adaptive prefix threshold (LSP)
+# --------------------------------------------------------------------------
+
+def lock_kl(logits_cur, logits_prev, count=None, row_idx=None):
+    """Local KL divergence between consecutive steps and the uncertainty.
+
+    SureLock, technical summary section 2, locking criterion 1: the local
+    divergence D = KL(p_t || p_{t-1}) between the current and the previous
+    step's predictive distribution of a position; criterion 2: its
+    uncertainty 1 - max_v p_t(v).
+
+    ``logits_cur``/``logits_prev`` [B, R, V] (same row layout); row r of batch
+    b reads row ``row_idx[b, r]`` when given, else row r; rows r >= count[b]
+    are skipped (NaN).  p = softmax(z), q = softmax(y), and with the
+    log-softmax log p_j = z_j - logsumexp(z):
+    KL = sum_j p_j (log p_j - log q_j).  Returns kl, unc, each [B, R_max].
+    """
+    z_all, y_all = _f64(logits_cur), _f64(logits_prev)
+    B, R, V = z_all.shape
+    R_max = R if row_idx is None else np.asarray(row_idx).shape[1]
+    if count is None:
+        count = np.full(B, R_max, dtype=np.int64)
+    kl = np.full((B, R_max), np.nan)
+    unc = np.full((B, R_max), np.nan)
+    for b in range(B):
+        for r in range(int(count[b])):
+            row = r if row_idx is None else int(row_idx[b][r])
+            z, y = z_all[b, row], y_all[b, row]
+            mz, my = np.max(z), np.max(y)
+            log_p = z - (mz + np.log(np.sum(np.exp(z - mz))))
+            log_q = y - (my + np.log(np.sum(np.exp(y - my))))
+            p = np.exp(log_p)
+            kl[b, r] = np.sum(p * (log_p - log_q))
+            unc[b, r] = 1.0 - np.max(p)
+    return kl, unc
+
+
+def lock_decision(kl, unc, count, eps: float, gate_q: float):
+    """Which active rows lock at this step.
+
+    SureLock, technical summary section 2: a position locks when its local
+    KL divergence is below eps (criterion 1) and, with the optional gate
+    (criterion 2), its uncertainty lies below a percentile of the
+    uncertainties.  Reading: the percentile is taken over the active rows of
+    the same batch row; with n of them and gate fraction q in (0, 1), the gate
+    passes iff unc <= the k-th smallest uncertainty, k = max(1, ceil(q n));
+    q <= 0 or q >= 1 disables the gate.  Decisions compare float32 values
+    (kl < eps, unc <= threshold); NaN never locks.  Returns lock [B, R_max]
+    (bool).
+    """
+    kl32 = np.asarray(kl, dtype=np.float32)
+    unc32 = np.asarray(unc, dtype=np.float32)
+    B, R_max = kl32.shape
+    lock = np.zeros((B, R_max), dtype=bool)
+    for b in range(B):
+        n = int(count[b])
+        if n == 0:
+            continue
+        gate = np.ones(n, dtype=bool)
+        if 0.0 < gate_q < 1.0:
+            u = unc32[b, :n]
+            k = max(1, int(math.ceil(gate_q * n)))
+            finite = np.sort(u[~np.isnan(u)])
+            t = finite[k - 1] if k <= len(finite) else np.float32(np.inf)
+            gate = u <= t
+        lock[b, :n] = (kl32[b, :n] < np.float32(eps)) & gate
+    return lock
+
+
+def adaptive_prefix(score, start, lo: float, hi: float):
+    """Longest stable prefix with an adaptive threshold.
+
+    LSP, technical summary section 2, step 2 (adaptive sizing): instead of a
+    fixed threshold, tau is chosen so that the committed stable block covers
+    a fraction [lo, hi] of the current active length A = L - start; step 4
+    (fallback): at least one token.  Reading: with the prefix minima
+    m_k = min(score[start .. start + k - 1]) (NaN counts as unstable, -inf),
+    k_lo = max(1, ceil(lo A)) and k_hi = max(k_lo, floor(hi A)):
+    tau = m_{k_lo}, len = min(k_hi, #{k : m_k >= tau}), never past the first
+    NaN score, and at least 1 when A > 0.  Scores are compared as float32.
+    Returns (len [B] int32, tau [B] float32; +inf when A = 0).
+    """
+    s32 = np.asarray(score).astype(np.float32)
+    B, L = s32.shape
+    lens = np.zeros(B, dtype=np.int32)
+    taus = np.full(B, np.inf, dtype=np.float32)
+    for b in range(B):
+        st = int(start[b])
+        A = L - st
+        if A <= 0:
+            continue
+        seg = s32[b, st:]
+        m = np.empty(A, dtype=np.float32)
+        cur = np.float32(np.inf)
+        first_nan = A
+        for k in range(A):
+            v = seg[k]
+            if np.isnan(v):
+                v = np.float32(-np.inf)
+                first_nan = min(first_nan, k)
+            cur = min(cur, v)
+            m[k] = cur
+        k_lo = max(1, int(math.ceil(lo * A)))
+        k_lo = min(k_lo, A)
+        k_hi = max(k_lo, int(math.floor(hi * A)))
+        tau = m[k_lo - 1]
+        n_ge = 0
+        while n_ge < A and m[n_ge] >= tau:
+            n_ge += 1
+        ln = min(k_hi, n_ge, first_nan)
+        lens[b] = max(ln, 1)
+        taus[b] = tau
+    return lens, taus
 
 
 # --------------------------------------------------------------------------

@@ -264,9 +264,9 @@ def test_attention_all_active_equals_torch_sdpa():
     tk = torch.from_numpy(k).permute(0, 2, 1, 3)
     tv = torch.from_numpy(v).permute(0, 2, 1, 3)
     ref = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv).permute(0, 2, 1, 3)
-    assert np.allclose(o, ref.numpy(), atol=1e-13, rtol=0)
+    assert np.allclose(o, ref.numpy(), atol=1e-12, rtol=0)
     s = torch.matmul(tq, tk.transpose(-1, -2)) / math.sqrt(d)
-    assert np.allclose(lse, torch.logsumexp(s, -1).numpy(), atol=1e-13, rtol=0)
+    assert np.allclose(lse, torch.logsumexp(s, -1).numpy(), atol=1e-12, rtol=0)
     # full-matrix column sums when every row is active
     assert np.allclose(cs, torch.softmax(s, -1).sum(-2).numpy(), atol=1e-12, rtol=0)
 
@@ -403,3 +403,125 @@ def test_step_nothing_salient():
     assert np.array_equal(out["k_cache"], d["k_cache"])
     assert np.all(out["colsum"] == 0)
     assert np.all(np.isnan(out["o"]))
+
+
+# ---------------------------------------------------------------- lock criterion
+
+def test_lock_kl_golden(golden):
+    for case in golden["lock_kl"]:
+        kl, unc = oracle.lock_kl(np.array([[case["cur"]]]), np.array([[case["prev"]]]))
+        assert abs(kl[0, 0] - case["kl"]) < 1e-14, case
+        assert abs(unc[0, 0] - case["unc"]) < 1e-14, case
+
+
+def test_lock_kl_matches_scipy_entropy():
+    from scipy.special import softmax
+    from scipy.stats import entropy
+    z = RNG.standard_normal((2, 5, 300)) * 2.0
+    y = z + RNG.standard_normal((2, 5, 300)) * 0.3
+    kl, unc = oracle.lock_kl(z, y)
+    for b in range(2):
+        for r in range(5):
+            p, q = softmax(z[b, r]), softmax(y[b, r])
+            assert abs(kl[b, r] - entropy(p, q)) < 1e-12
+            assert abs(unc[b, r] - (1.0 - p.max())) < 1e-14
+
+
+def test_lock_kl_identity_shift_and_gibbs():
+    z = RNG.standard_normal((1, 6, 50))
+    kl, _ = oracle.lock_kl(z, z + 7.5)  # same distribution
+    assert np.max(np.abs(kl)) < 1e-13
+    y = RNG.standard_normal((1, 6, 50))
+    kl, _ = oracle.lock_kl(z, y)
+    assert np.all(kl > 0)
+
+
+def test_lock_kl_brute_force_small_vocab():
+    for V in (2, 3, 4):
+        z = RNG.standard_normal((1, 3, V)) * 3
+        y = RNG.standard_normal((1, 3, V)) * 3
+        kl, unc = oracle.lock_kl(z, y)
+        for r in range(3):
+            ez = [math.exp(v) for v in z[0, r]]
+            ey = [math.exp(v) for v in y[0, r]]
+            p = [e / sum(ez) for e in ez]
+            q = [e / sum(ey) for e in ey]
+            ref = sum(pj * math.log(pj / qj) for pj, qj in zip(p, q))
+            assert abs(kl[0, r] - ref) < 1e-12
+            assert abs(unc[0, r] - (1 - max(p))) < 1e-14
+
+
+def test_lock_kl_row_idx_and_count():
+    z = RNG.standard_normal((2, 6, 40))
+    y = RNG.standard_normal((2, 6, 40))
+    row_idx = np.array([[5, 0, 3], [1, 1, 2]])
+    kl, unc = oracle.lock_kl(z, y, count=[3, 1], row_idx=row_idx)
+    full, ufull = oracle.lock_kl(z, y)
+    assert np.allclose(kl[0], full[0, [5, 0, 3]], rtol=0, atol=0)
+    assert kl[1, 0] == full[1, 1] and np.all(np.isnan(kl[1, 1:]))
+
+
+def test_lock_decision_without_gate_and_with_numpy_quantile():
+    kl = RNG.random((3, 40)).astype(np.float32) * 1e-2
+    unc = RNG.random((3, 40)).astype(np.float32)
+    count = [40, 17, 0]
+    lock = oracle.lock_decision(kl, unc, count, 5e-3, 0.0)
+    for b, n in enumerate(count):
+        assert np.array_equal(lock[b, :n], kl[b, :n] < np.float32(5e-3))
+        assert not lock[b, n:].any()
+    for q in (0.1, 0.25, 0.5, 0.9):
+        lock = oracle.lock_decision(kl, unc, count, 5e-3, q)
+        for b, n in enumerate(count[:2]):
+            t = np.quantile(unc[b, :n], q, method="inverted_cdf")
+            assert np.array_equal(lock[b, :n], (kl[b, :n] < np.float32(5e-3)) & (unc[b, :n] <= t))
+
+
+def test_lock_decision_gate_extremes_and_nan():
+    kl = np.zeros((1, 8), dtype=np.float32)
+    unc = np.array([[0.5, 0.1, 0.3, 0.1, 0.9, 0.2, 0.7, 0.4]], dtype=np.float32)
+    lock = oracle.lock_decision(kl, unc, [8], 1.0, 1.0 / 8)
+    assert lock[0].tolist() == [False, True, False, True, False, False, False, False]  # tie at the minimum
+    assert oracle.lock_decision(kl, unc, [8], 1.0, 1.0).all()  # q >= 1: no gate
+    kl[0, 2] = np.nan
+    assert not oracle.lock_decision(kl, unc, [8], 1.0, 0.0)[0, 2]
+
+
+# ---------------------------------------------------------------- adaptive prefix
+
+def test_adaptive_prefix_golden(golden):
+    for case in golden["adaptive_prefix"]:
+        ln, tau = oracle.adaptive_prefix(np.array([case["score"]]), [case["start"]], case["lo"],
+                                         case["hi"])
+        assert ln[0] == case["len"], case
+        assert tau[0] == np.float32(case["tau"]), case
+
+
+def test_adaptive_prefix_brute_force_characterisation():
+    # For every pattern: tau is the minimum of the first k_lo active scores
+    # (numpy), every committed score is >= tau, and len is the largest k <=
+    # k_hi with that property, at least 1.
+    vals = np.array([0.2, 0.5, 0.8], dtype=np.float32)
+    for n in (1, 2, 3, 5, 6):
+        for pat in itertools.product(range(3), repeat=n):
+            score = vals[list(pat)][None, :]
+            for start in range(n + 1):
+                for lo, hi in ((0.25, 0.5), (0.1, 0.9), (0.5, 0.5)):
+                    ln, tau = oracle.adaptive_prefix(score, [start], lo, hi)
+                    A = n - start
+                    if A == 0:
+                        assert ln[0] == 0 and np.isinf(tau[0])
+                        continue
+                    k_lo = min(A, max(1, math.ceil(lo * A)))
+                    k_hi = max(k_lo, math.floor(hi * A))
+                    seg = score[0, start:]
+                    assert tau[0] == np.min(seg[:k_lo])
+                    feasible = [k for k in range(1, k_hi + 1) if np.all(seg[:k] >= tau[0])]
+                    assert ln[0] == max(feasible + [1])
+                    assert np.array_equal(np.minimum.accumulate(seg)[:ln[0]] >= tau[0],
+                                          np.ones(ln[0], dtype=bool))
+
+
+def test_adaptive_prefix_nan_stops_and_fallback():
+    score = np.array([[0.9, np.nan, 0.9, 0.9], [np.nan, 0.9, 0.9, 0.9]], dtype=np.float32)
+    ln, tau = oracle.adaptive_prefix(score, [0, 0], 0.25, 1.0)
+    assert ln.tolist() == [1, 1]
