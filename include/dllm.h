@@ -291,6 +291,79 @@ dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start,
                                int32_t* len_out, int32_t* dev_status,
                                void* stream);
 
+/*
+ * dllm_lock_criterion -- SureLock's locking criterion: the local KL
+ * divergence of each row's predictive distribution between the previous and
+ * the current step, its uncertainty, and the lock flags.
+ *
+ * SureLock, technical summary section 2, locking criterion 1: a position
+ * locks when D = KL(p_t || p_{t-1}) falls below eps; criterion 2 (optional
+ * gate): its uncertainty 1 - max_v p_t(v) must lie below a percentile.  The
+ * percentile is taken over the active rows of the same batch row: with n
+ * active rows and gate fraction q in (0, 1) the gate passes iff the
+ * uncertainty is at most the k-th smallest one, k = max(1, ceil(q n)) (q as
+ * float32, the product exact); q <= 0 or q >= 1 disables the gate.
+ *
+ *   logits_cur, logits_prev  [B, R_src, V] of `dtype`, the same layout
+ *               (row r of batch b at b*batch_stride + r*row_stride): the
+ *               current and the previous step's logits of the same rows.
+ *   R_max, row_idx, count, out_idx, out_cols  as in dllm_confidence.
+ *   eps         KL threshold: a row locks iff kl < eps (float32 compare) and
+ *               the gate passes; NaN never locks.
+ *   kl_out      [B, out_cols] float32: sum_j p_j (log p_j - log q_j),
+ *               p = softmax(current row), q = softmax(previous row).
+ *   unc_out     [B, out_cols] float32: 1 - max_j p_j.
+ *   locked_inout [B, out_cols] uint8 or NULL: set to 1 at the columns of the
+ *               rows that lock (never cleared: a lock is permanent); usable
+ *               as the `locked` mask of dllm_saliency_select.  R_max must be
+ *               at most 16384 when it is given.
+ *   ws          workspace of dllm_lock_workspace_bytes() bytes (16-byte
+ *               aligned); its contents need no initialisation.
+ * Logits must be finite.  Errors: INVALID_ARG (NULLs, sizes, strides, small
+ * workspace, R_max above 16384 with lock flags); dev_status gets
+ * DEVICE_CHECK for counts/indices out of range (row skipped).
+ */
+size_t dllm_lock_workspace_bytes(int B, int R_max, int V, int dtype);
+
+dllm_status dllm_lock_criterion(const void* logits_cur, const void* logits_prev,
+                                int dtype, int B, int R_src, int V,
+                                int64_t row_stride, int64_t batch_stride,
+                                int R_max, const int32_t* row_idx,
+                                const int32_t* count, const int32_t* out_idx,
+                                int out_cols, float eps, float gate_q,
+                                float* kl_out, float* unc_out,
+                                uint8_t* locked_inout, void* ws,
+                                size_t ws_bytes, int32_t* dev_status,
+                                void* stream);
+
+/*
+ * dllm_adaptive_prefix -- the longest stable prefix with an adaptive
+ * threshold.
+ *
+ * LSP, technical summary section 2, step 2 (adaptive sizing): instead of a
+ * fixed threshold, tau is chosen so that the committed stable block covers a
+ * fraction [lo, hi] of the current active length A = L - start; step 4
+ * (fallback): at least one token.  With the prefix minima
+ * m_k = min(score[start .. start + k - 1]) (NaN counts as -inf),
+ * k_lo = max(1, ceil(lo A)), k_hi = max(k_lo, floor(hi A)) (float32 lo, hi;
+ * exact products): tau = m_{k_lo}; len = min(k_hi, #{k : m_k >= tau}),
+ * never past the first NaN score, at least 1 when A > 0.
+ *
+ *   score       [B, L] float32, contiguous (e.g. the logit margin of
+ *               dllm_confidence, +inf at committed positions).
+ *   start       [B] int32 in [0, L]; advance_start nonzero: start += len.
+ *   lo, hi      fractions in [0, 1].
+ *   len_out     [B] int32 (0 when A = 0).
+ *   tau_out     [B] float32: the threshold chosen (+inf when A = 0).
+ * Errors: INVALID_ARG; dev_status gets DEVICE_CHECK for start outside
+ * [0, L] (len 0).
+ */
+dllm_status dllm_adaptive_prefix(const float* score, int B, int L,
+                                 int32_t* start, float lo, float hi,
+                                 int advance_start, int32_t* len_out,
+                                 float* tau_out, int32_t* dev_status,
+                                 void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

@@ -325,8 +325,9 @@ def lock_decision(kl, unc, count, eps: float, gate_q: float):
     uncertainties.  Reading: the percentile is taken over the active rows of
     the same batch row; with n of them and gate fraction q in (0, 1), the gate
     passes iff unc <= the k-th smallest uncertainty, k = max(1, ceil(q n));
-    q <= 0 or q >= 1 disables the gate.  Decisions compare float32 values
-    (kl < eps, unc <= threshold); NaN never locks.  Returns lock [B, R_max]
+    q <= 0 or q >= 1 disables the gate; q is taken as a float32 and q n is
+    the exact product.  Decisions compare float32 values (kl < eps, unc <=
+    threshold); NaN never locks.  Returns lock [B, R_max]
     (bool).
     """
     kl32 = np.asarray(kl, dtype=np.float32)
@@ -340,7 +341,7 @@ def lock_decision(kl, unc, count, eps: float, gate_q: float):
         gate = np.ones(n, dtype=bool)
         if 0.0 < gate_q < 1.0:
             u = unc32[b, :n]
-            k = max(1, int(math.ceil(gate_q * n)))
+            k = max(1, int(math.ceil(float(np.float32(gate_q)) * n)))
             finite = np.sort(u[~np.isnan(u)])
             t = finite[k - 1] if k <= len(finite) else np.float32(np.inf)
             gate = u <= t
@@ -356,7 +357,8 @@ def adaptive_prefix(score, start, lo: float, hi: float):
     a fraction [lo, hi] of the current active length A = L - start; step 4
     (fallback): at least one token.  Reading: with the prefix minima
     m_k = min(score[start .. start + k - 1]) (NaN counts as unstable, -inf),
-    k_lo = max(1, ceil(lo A)) and k_hi = max(k_lo, floor(hi A)):
+    k_lo = max(1, ceil(lo A)) and k_hi = max(k_lo, floor(hi A)) (lo, hi taken
+    as float32, the products exact):
     tau = m_{k_lo}, len = min(k_hi, #{k : m_k >= tau}), never past the first
     NaN score, and at least 1 when A > 0.  Scores are compared as float32.
     Returns (len [B] int32, tau [B] float32; +inf when A = 0).
@@ -381,9 +383,9 @@ def adaptive_prefix(score, start, lo: float, hi: float):
                 first_nan = min(first_nan, k)
             cur = min(cur, v)
             m[k] = cur
-        k_lo = max(1, int(math.ceil(lo * A)))
+        k_lo = max(1, int(math.ceil(float(np.float32(lo)) * A)))
         k_lo = min(k_lo, A)
-        k_hi = max(k_lo, int(math.floor(hi * A)))
+        k_hi = max(k_lo, int(math.floor(float(np.float32(hi)) * A)))
         tau = m[k_lo - 1]
         n_ge = 0
         while n_ge < A and m[n_ge] >= tau:

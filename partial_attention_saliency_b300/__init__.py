@@ -11,11 +11,14 @@ from ._lib import (  # noqa: F401
     DllmError,
     LIB_PATH,
     SIGNATURES,
+    dllm_adaptive_prefix,
     dllm_attention_colsum,
     dllm_attention_workspace_bytes,
     dllm_confidence,
     dllm_confidence_workspace_bytes,
     dllm_kv_scatter,
+    dllm_lock_criterion,
+    dllm_lock_workspace_bytes,
     dllm_partial_attention,
     dllm_saliency_select,
     dllm_stable_prefix,

@@ -44,6 +44,10 @@ SIGNATURES = {
                                     _SZ, _P, _P]),
     "dllm_attention_colsum": (_I, [_P, _P, _I, _I, _I, _I, _I, _I, _P, _F, _P, _P, _P, _P]),
     "dllm_stable_prefix": (_I, [_P, _I, _I, _P, _F, _I, _I, _P, _P, _P]),
+    "dllm_lock_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
+    "dllm_lock_criterion": (_I, [_P, _P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _F, _F,
+                                 _P, _P, _P, _P, _SZ, _P, _P]),
+    "dllm_adaptive_prefix": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
 }
 
 
@@ -289,3 +293,67 @@ def dllm_stable_prefix(score, start, tau: float, *, min_commit: bool = True,
                                   int(advance_start), _ptr(len_out), _ptr(dev_status),
                                   _stream(stream)))
     return len_out
+
+
+def dllm_lock_workspace_bytes(B: int, R_max: int, V: int, dtype: torch.dtype) -> int:
+    return int(load_library().dllm_lock_workspace_bytes(B, R_max, V, DTYPES[dtype]))
+
+
+def dllm_lock_criterion(logits_cur, logits_prev, eps: float, *, gate_q: float = 0.0,
+                        R_max: Optional[int] = None, row_idx=None, count=None, out_idx=None,
+                        out_cols: Optional[int] = None, kl_out=None, unc_out=None,
+                        locked_inout=None, ws=None, dev_status=None, stream=None):
+    """Local KL divergence between two steps, uncertainty and lock flags.
+
+    ``logits_cur``/``logits_prev`` [B, R_src, V] with identical strides.
+    Returns (kl [B, out_cols], unc [B, out_cols], locked_inout or None).
+    """
+    lib = load_library()
+    dt = _dtype(logits_cur, logits_prev)
+    if logits_cur.dim() != 3 or logits_cur.shape != logits_prev.shape \
+            or logits_cur.stride() != logits_prev.stride() or logits_cur.stride(2) != 1:
+        raise ValueError("logits must be [B, R_src, V] with identical strides, vocabulary contiguous")
+    B, R_src, V = logits_cur.shape
+    R_max = R_src if R_max is None else int(R_max)
+    out_cols = R_max if out_cols is None else int(out_cols)
+    dev = logits_cur.device
+    kl_out = torch.empty((B, out_cols), dtype=torch.float32, device=dev) if kl_out is None else kl_out
+    unc_out = torch.empty((B, out_cols), dtype=torch.float32, device=dev) if unc_out is None else unc_out
+    _need(kl_out, torch.float32, (B, out_cols), "kl_out")
+    _need(unc_out, torch.float32, (B, out_cols), "unc_out")
+    if locked_inout is not None:
+        _need(locked_inout, torch.uint8, (B, out_cols), "locked_inout")
+    for t, n in ((row_idx, "row_idx"), (out_idx, "out_idx")):
+        if t is not None:
+            _need(t, torch.int32, (B, R_max), n)
+    if count is not None:
+        _need(count, torch.int32, (B,), "count")
+    need = lib.dllm_lock_workspace_bytes(B, R_max, V, dt)
+    if ws is None:
+        ws = torch.empty((max(int(need), 16),), dtype=torch.uint8, device=dev)
+    _check(lib.dllm_lock_criterion(_ptr(logits_cur), _ptr(logits_prev), dt, B, R_src, V,
+                                   logits_cur.stride(1), logits_cur.stride(0), R_max,
+                                   _ptr(row_idx), _ptr(count), _ptr(out_idx), out_cols,
+                                   float(eps), float(gate_q), _ptr(kl_out), _ptr(unc_out),
+                                   _ptr(locked_inout), _ptr(ws), ws.numel() * ws.element_size(),
+                                   _ptr(dev_status), _stream(stream)))
+    return kl_out, unc_out, locked_inout
+
+
+def dllm_adaptive_prefix(score, start, lo: float, hi: float, *, advance_start: bool = False,
+                         len_out=None, tau_out=None, dev_status=None, stream=None):
+    """Longest stable prefix whose threshold adapts to a fraction [lo, hi] of
+    the active length.  Returns (len [B] int32, tau [B] float32)."""
+    lib = load_library()
+    B, L = score.shape
+    _need(score, torch.float32, (B, L), "score")
+    _need(start, torch.int32, (B,), "start")
+    dev = score.device
+    len_out = torch.empty((B,), dtype=torch.int32, device=dev) if len_out is None else len_out
+    tau_out = torch.empty((B,), dtype=torch.float32, device=dev) if tau_out is None else tau_out
+    _need(len_out, torch.int32, (B,), "len_out")
+    _need(tau_out, torch.float32, (B,), "tau_out")
+    _check(lib.dllm_adaptive_prefix(_ptr(score), B, L, _ptr(start), float(lo), float(hi),
+                                    int(advance_start), _ptr(len_out), _ptr(tau_out),
+                                    _ptr(dev_status), _stream(stream)))
+    return len_out, tau_out

@@ -227,6 +227,60 @@ dllm_status dllm_stable_prefix(const float* score, int B, int L, int32_t* start,
                    "dllm_stable_prefix launch");
 }
 
+size_t dllm_lock_workspace_bytes(int B, int R_max, int V, int dtype) {
+  if (B < 1 || R_max < 1 || V < 1 || !valid_dtype(dtype)) return 0;
+  return dllm::lock_workspace_bytes(B, R_max, V, dtype);
+}
+
+dllm_status dllm_lock_criterion(const void* logits_cur, const void* logits_prev, int dtype,
+                                int B, int R_src, int V, int64_t row_stride,
+                                int64_t batch_stride, int R_max, const int32_t* row_idx,
+                                const int32_t* count, const int32_t* out_idx, int out_cols,
+                                float eps, float gate_q, float* kl_out, float* unc_out,
+                                uint8_t* locked_inout, void* ws, size_t ws_bytes,
+                                int32_t* dev_status, void* stream) {
+  REQUIRE(logits_cur && logits_prev && kl_out && unc_out,
+          "dllm_lock_criterion: NULL logits or output pointer");
+  REQUIRE(valid_dtype(dtype), "dllm_lock_criterion: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && R_src >= 1 && R_max >= 1, "dllm_lock_criterion: B=%d R_src=%d R_max=%d", B,
+          R_src, R_max);
+  REQUIRE(V >= 1, "dllm_lock_criterion: V=%d must be >= 1", V);
+  REQUIRE(row_stride >= V, "dllm_lock_criterion: row_stride %lld < V", (long long)row_stride);
+  REQUIRE(B == 1 || batch_stride >= (int64_t)R_src * row_stride,
+          "dllm_lock_criterion: batch_stride too small");
+  REQUIRE(row_idx != nullptr || R_max <= R_src,
+          "dllm_lock_criterion: R_max > R_src without row_idx");
+  REQUIRE(out_cols >= 1 && (out_idx != nullptr || R_max <= out_cols),
+          "dllm_lock_criterion: out_cols %d too small", out_cols);
+  REQUIRE(locked_inout == nullptr || R_max <= 16384,
+          "dllm_lock_criterion: R_max %d above 16384 with lock flags", R_max);
+  REQUIRE((int64_t)B * R_max <= 2147483647, "dllm_lock_criterion: B*R_max too large");
+  const size_t need = dllm::lock_workspace_bytes(B, R_max, V, dtype);
+  REQUIRE(ws != nullptr && ws_bytes >= need,
+          "dllm_lock_criterion: workspace %zu bytes < %zu required", ws_bytes, need);
+  REQUIRE(reinterpret_cast<uintptr_t>(ws) % 16 == 0, "dllm_lock_criterion: workspace misaligned");
+  return from_cuda(dllm::launch_lock_criterion(logits_cur, logits_prev, dtype, B, R_src, V,
+                                               row_stride, batch_stride, R_max, row_idx, count,
+                                               out_idx, out_cols, eps, gate_q, kl_out, unc_out,
+                                               locked_inout, ws, dev_status,
+                                               static_cast<cudaStream_t>(stream)),
+                   "dllm_lock_criterion launch");
+}
+
+dllm_status dllm_adaptive_prefix(const float* score, int B, int L, int32_t* start, float lo,
+                                 float hi, int advance_start, int32_t* len_out, float* tau_out,
+                                 int32_t* dev_status, void* stream) {
+  REQUIRE(score && start && len_out && tau_out, "dllm_adaptive_prefix: NULL pointer argument");
+  REQUIRE(B >= 1 && L >= 1, "dllm_adaptive_prefix: B=%d L=%d must be >= 1", B, L);
+  REQUIRE(L < (1 << 29), "dllm_adaptive_prefix: L=%d too large", L);
+  REQUIRE(lo >= 0.0f && lo <= 1.0f && hi >= 0.0f && hi <= 1.0f,
+          "dllm_adaptive_prefix: fractions lo=%g hi=%g outside [0, 1]", lo, hi);
+  return from_cuda(dllm::launch_adaptive_prefix(score, B, L, start, lo, hi, advance_start,
+                                                len_out, tau_out, dev_status,
+                                                static_cast<cudaStream_t>(stream)),
+                   "dllm_adaptive_prefix launch");
+}
+
 }  // extern "C"
 
 namespace dllm {

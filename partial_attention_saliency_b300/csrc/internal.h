@@ -58,10 +58,24 @@ cudaError_t launch_stable_prefix(const float* score, int B, int L, int32_t* star
                                  int min_commit, int advance_start, int32_t* len_out,
                                  int32_t* dev_status, cudaStream_t stream);
 
+size_t lock_workspace_bytes(int B, int R_max, int V, int dtype);
+
+cudaError_t launch_lock_criterion(const void* z, const void* y, int dtype, int B, int R_src,
+                                  int V, int64_t rs, int64_t bs, int R_max,
+                                  const int32_t* row_idx, const int32_t* count,
+                                  const int32_t* out_idx, int out_cols, float eps, float gate_q,
+                                  float* kl_out, float* unc_out, uint8_t* locked, void* ws,
+                                  int32_t* dev_status, cudaStream_t stream);
+
+cudaError_t launch_adaptive_prefix(const float* score, int B, int L, int32_t* start, float lo,
+                                   float hi, int advance_start, int32_t* len_out, float* tau_out,
+                                   int32_t* dev_status, cudaStream_t stream);
+
 int num_sms();
 
 // Raises the dynamic shared-memory limit of `func` to `bytes` on the current
-// device (once per function and device).
+// device (once per function and device: later calls keep the first value, so
+// a kernel whose size varies passes its largest size).
 cudaError_t ensure_smem_limit(const void* func, int bytes);
 
 // Records `message` as the thread's dllm_last_error() text and returns `code`.

@@ -1,0 +1,507 @@
+// Lock criterion between consecutive steps, and the adaptive prefix threshold.
+//
+// SureLock ("Stopping Computation for Converged Tokens in Masked Diffusion-LM
+// Decoding"), technical summary section 2, locking criterion 1: a position
+// locks when the local divergence D = KL(p_t || p_{t-1}) of its predictive
+// distribution between two steps falls below eps; criterion 2 (optional):
+// its uncertainty 1 - max p_t must lie below a percentile.  LSP ("Beyond
+// Scattered Acceptance ..."), technical summary section 2, step 2: the
+// threshold of the stable prefix is chosen so that the committed block
+// covers a fraction [lo, hi] of the active length.
+//
+// lock_partial_kernel  one CTA per (row, 32 KB chunk of each of the two
+//                      logit rows): block maxima of z and y first, then
+//                      sum exp(z - Mz), sum exp(z - Mz)(z - y) and
+//                      sum exp(y - My); HBM bound, 2 V sizeof(T) per row.
+// lock_merge_kernel    one warp per row folds the chunks in a fixed order and
+//                      evaluates KL = A / lz - (Mz + ln lz) + (My + ln ly) in
+//                      double; the uncertainty is 1 - 1 / lz.
+// lock_gate_kernel     one CTA per batch row: radix select of the k-th
+//                      smallest uncertainty among the active rows (the
+//                      percentile gate), then the lock flags (only ever set).
+// adaptive_prefix_kernel one CTA per batch row: block-wide prefix-minimum scan
+//                      of the active suffix, tau at ceil(lo A), the run of
+//                      prefix minima >= tau capped at floor(hi A).
+#include <climits>
+#include <type_traits>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dllm {
+namespace {
+
+constexpr int kLockThreads = 256;
+constexpr int kLockU = 8;  // 16-byte vectors per thread per chunk and input
+constexpr int kGateThreads = 1024;
+constexpr int kGateMaxRows = 16384;  // uncertainty keys held in shared memory (64 KB)
+
+struct LockPartial {
+  float mz, lz, a, my, ly, pad0, pad1, pad2;  // 32 bytes
+};
+
+template <typename T> __host__ __device__ constexpr int lvec() { return 16 / (int)sizeof(T); }
+template <typename T> __host__ __device__ constexpr int lock_chunk_elems() {
+  return kLockThreads * kLockU * lvec<T>();
+}
+
+template <typename T>
+__device__ __forceinline__ float lelem(const uint4& v, int e) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  if constexpr (std::is_same<T, float>::value) {
+    return __uint_as_float(w[e]);
+  } else {
+    return (e & 1) ? bf16_hi(w[e >> 1]) : bf16_lo(w[e >> 1]);
+  }
+}
+
+template <typename T, bool VEC>
+__device__ __forceinline__ uint4 lload(const T* row, int vi, int V) {
+  constexpr int E = lvec<T>();
+  if (VEC && (vi + 1) * E <= V) return ld_stream16(row + (int64_t)vi * E);
+  uint32_t w[4];
+  if constexpr (std::is_same<T, float>::value) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i = vi * E + k;
+      w[k] = i < V ? __float_as_uint(row[i]) : 0xff800000u;
+    }
+  } else {
+    const uint16_t* hh = reinterpret_cast<const uint16_t*>(row);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int i0 = vi * E + 2 * k, i1 = i0 + 1;
+      const uint32_t lo = i0 < V ? hh[i0] : 0xff80u;
+      const uint32_t hi = i1 < V ? hh[i1] : 0xff80u;
+      w[k] = lo | (hi << 16);
+    }
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ bool lock_row(int b, int r, int R_max, int R_src,
+                                         const int32_t* row_idx, const int32_t* count, int* row,
+                                         bool* bad) {
+  int n = count ? __ldca(count + b) : R_max;
+  *bad = false;
+  if (n < 0 || n > R_max) {
+    *bad = true;
+    n = n < 0 ? 0 : R_max;
+  }
+  if (r >= n) return false;
+  const int rr = row_idx ? __ldca(row_idx + (int64_t)b * R_max + r) : r;
+  if (rr < 0 || rr >= R_src) {
+    *bad = true;
+    return false;
+  }
+  *row = rr;
+  return true;
+}
+
+__device__ __forceinline__ float block_max(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_max(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float m = red[0];
+  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
+  __syncthreads();
+  return m;
+}
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  v = warp_sum(v);
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float s = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];  // fixed order
+  __syncthreads();
+  return s;
+}
+
+template <typename T, bool VEC>
+__global__ void __launch_bounds__(kLockThreads)
+lock_partial_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs, int64_t bs, int R_max,
+                    const int32_t* row_idx, const int32_t* count, int nchunks, LockPartial* ws) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
+  __shared__ float red[kLockThreads / 32];
+  constexpr int E = lvec<T>();
+  const int br = blockIdx.x, chunk = blockIdx.y;
+  const int b = br / R_max, r = br - b * R_max;
+  int row;
+  bool bad;
+  if (!lock_row(b, r, R_max, R_src, row_idx, count, &row, &bad)) return;
+  const T* zrow = zs + (int64_t)b * bs + (int64_t)row * rs;
+  const T* yrow = ys + (int64_t)b * bs + (int64_t)row * rs;
+  const int vbase = chunk * (kLockThreads * kLockU);
+  const int nvec = (V + E - 1) / E;
+  const uint32_t sent = std::is_same<T, float>::value ? 0xff800000u : 0xff80ff80u;
+  uint4 vz[kLockU], vy[kLockU];
+#pragma unroll
+  for (int u = 0; u < kLockU; ++u) {
+    const int vi = vbase + u * kLockThreads + threadIdx.x;
+    vz[u] = vi < nvec ? lload<T, VEC>(zrow, vi, V) : make_uint4(sent, sent, sent, sent);
+    vy[u] = vi < nvec ? lload<T, VEC>(yrow, vi, V) : make_uint4(sent, sent, sent, sent);
+  }
+  float mz = -INFINITY, my = -INFINITY;
+#pragma unroll
+  for (int u = 0; u < kLockU; ++u)
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      mz = fmaxf(mz, lelem<T>(vz[u], e));
+      my = fmaxf(my, lelem<T>(vy[u], e));
+    }
+  const float Mz = block_max(mz, red);
+  const float My = block_max(my, red);
+  float lz = 0.f, a = 0.f, ly = 0.f;
+  if (Mz != -INFINITY) {
+    const float nz = -Mz * kLog2e, ny = -My * kLog2e;
+#pragma unroll
+    for (int u = 0; u < kLockU; ++u)
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        const float z = lelem<T>(vz[u], e), y = lelem<T>(vy[u], e);
+        if (z != -INFINITY) {  // padding past the row end
+          const float pz = ex2_approx(fmaf(z, kLog2e, nz));
+          lz += pz;
+          a = fmaf(pz, z - y, a);
+          ly += ex2_approx(fmaf(y, kLog2e, ny));
+        }
+      }
+  }
+  lz = block_sum(lz, red);
+  a = block_sum(a, red);
+  ly = block_sum(ly, red);
+  if (threadIdx.x == 0) {
+    LockPartial out;
+    out.mz = Mz;
+    out.lz = lz;
+    out.a = a;
+    out.my = My;
+    out.ly = ly;
+    out.pad0 = out.pad1 = out.pad2 = 0.f;
+    ws[(int64_t)br * nchunks + chunk] = out;
+  }
+}
+
+struct LockAcc {
+  float mz, lz, a, my, ly;
+};
+
+__device__ __forceinline__ LockAcc lock_fold(const LockAcc& p, const LockAcc& q) {
+  LockAcc r;
+  r.mz = fmaxf(p.mz, q.mz);
+  r.my = fmaxf(p.my, q.my);
+  const float cp = p.mz == -INFINITY ? 0.f : ex2_approx((p.mz - r.mz) * kLog2e);
+  const float cq = q.mz == -INFINITY ? 0.f : ex2_approx((q.mz - r.mz) * kLog2e);
+  const float dp = p.my == -INFINITY ? 0.f : ex2_approx((p.my - r.my) * kLog2e);
+  const float dq = q.my == -INFINITY ? 0.f : ex2_approx((q.my - r.my) * kLog2e);
+  r.lz = p.lz * cp + q.lz * cq;
+  r.a = p.a * cp + q.a * cq;
+  r.ly = p.ly * dp + q.ly * dq;
+  return r;
+}
+
+__global__ void lock_merge_kernel(int B, int R_src, int R_max, const int32_t* row_idx,
+                                  const int32_t* count, const int32_t* out_idx, int out_cols,
+                                  int nchunks, const LockPartial* ws, float* kl_out,
+                                  float* unc_out, int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
+  const int lane = threadIdx.x & 31;
+  const int64_t br = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (br >= (int64_t)B * R_max) return;
+  const int b = (int)(br / R_max), r = (int)(br - (int64_t)b * R_max);
+  int row;
+  bool bad;
+  const bool ok = lock_row(b, r, R_max, R_src, row_idx, count, &row, &bad);
+  if (bad && lane == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
+  if (!ok) return;
+  int col = r;
+  if (out_idx != nullptr) {
+    col = __ldca(out_idx + br);
+    if (col < 0 || col >= out_cols) {
+      if (lane == 0) report(dev_status, DLLM_ERR_DEVICE_CHECK);
+      return;
+    }
+  }
+  LockAcc acc{-INFINITY, 0.f, 0.f, -INFINITY, 0.f};
+  for (int c = lane; c < nchunks; c += 32) {
+    const float4* src = reinterpret_cast<const float4*>(ws + br * nchunks + c);
+    const float4 p0 = __ldca(src), p1 = __ldca(src + 1);
+    acc = lock_fold(acc, LockAcc{p0.x, p0.y, p0.z, p0.w, p1.x});
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    LockAcc o;
+    o.mz = __shfl_xor_sync(0xffffffffu, acc.mz, off);
+    o.lz = __shfl_xor_sync(0xffffffffu, acc.lz, off);
+    o.a = __shfl_xor_sync(0xffffffffu, acc.a, off);
+    o.my = __shfl_xor_sync(0xffffffffu, acc.my, off);
+    o.ly = __shfl_xor_sync(0xffffffffu, acc.ly, off);
+    acc = lock_fold(acc, o);
+  }
+  if (lane == 0) {
+    const double lse_z = (double)acc.mz + log((double)acc.lz);
+    const double lse_y = (double)acc.my + log((double)acc.ly);
+    const double kl = (double)acc.a / (double)acc.lz - lse_z + lse_y;
+    const int64_t o = (int64_t)b * out_cols + col;
+    kl_out[o] = (float)kl;
+    unc_out[o] = 1.0f - 1.0f / acc.lz;
+  }
+}
+
+// Order-preserving key of a non-negative float (NaN sorts last).
+__device__ __forceinline__ uint32_t ukey(float u) {
+  return isnan(u) ? 0xffffffffu : __float_as_uint(u);
+}
+
+__global__ void __launch_bounds__(kGateThreads)
+lock_gate_kernel(int R_max, const int32_t* count, const int32_t* out_idx, int out_cols,
+                 const float* kl, const float* unc, float eps, float gate_q, uint8_t* locked,
+                 int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
+  extern __shared__ uint32_t keys[];  // [R_max] uncertainty keys of the active rows
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_prefix, s_k;
+  const int b = blockIdx.x;
+  int n = count ? __ldca(count + b) : R_max;
+  n = n < 0 ? 0 : (n > R_max ? R_max : n);
+  auto col_of = [&](int r) { return out_idx ? __ldca(out_idx + (int64_t)b * R_max + r) : r; };
+  const bool gate = gate_q > 0.f && gate_q < 1.f;
+  float t = INFINITY;
+  if (gate && n > 0) {
+    for (int r = threadIdx.x; r < n; r += blockDim.x) {
+      const int c = col_of(r);
+      keys[r] = (c >= 0 && c < out_cols) ? ukey(__ldca(unc + (int64_t)b * out_cols + c))
+                                         : 0xffffffffu;
+    }
+    if (threadIdx.x == 0) {
+      s_prefix = 0;
+      // k = max(1, ceil(q n)), the product of the float32 q and n taken exactly in double
+      int k = (int)ceil((double)gate_q * (double)n);
+      s_k = (uint32_t)(k < 1 ? 1 : (k > n ? n : k));
+    }
+    uint32_t mask = 0;
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += blockDim.x) hist[i] = 0;
+      __syncthreads();
+      const uint32_t prefix = s_prefix;
+      for (int r = threadIdx.x; r < n; r += blockDim.x) {
+        const uint32_t key = keys[r];
+        if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        uint32_t k = s_k, cum = 0;
+        int d = 0;
+        for (; d < 256; ++d) {
+          if (cum + hist[d] >= k) break;
+          cum += hist[d];
+        }
+        s_k = k - cum;
+        s_prefix = prefix | ((uint32_t)d << shift);
+      }
+      mask |= 255u << shift;
+      __syncthreads();
+    }
+    const uint32_t tk = s_prefix;
+    t = tk == 0xffffffffu ? INFINITY : __uint_as_float(tk);
+  }
+  if (locked == nullptr) return;
+  const float e32 = eps;
+  for (int r = threadIdx.x; r < n; r += blockDim.x) {
+    const int c = col_of(r);
+    if (c < 0 || c >= out_cols) continue;  // reported by the merge kernel
+    const int64_t o = (int64_t)b * out_cols + c;
+    const float d = __ldca(kl + o), u = __ldca(unc + o);
+    if (d < e32 && (!gate || u <= t)) locked[o] = 1;
+  }
+}
+
+constexpr int kPrefixScanThreads = 1024;
+
+__global__ void __launch_bounds__(kPrefixScanThreads)
+adaptive_prefix_kernel(const float* score, int L, int32_t* start, float lo, float hi,
+                       int advance, int32_t* len_out, float* tau_out, int32_t* dev_status) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
+  __shared__ float warp_min[kPrefixScanThreads / 32];
+  __shared__ float s_tau;
+  __shared__ int s_fail[kPrefixScanThreads / 32], s_nan[kPrefixScanThreads / 32];
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int s = __ldca(start + b);
+  if (s < 0 || s > L) {
+    if (tid == 0) {
+      report(dev_status, DLLM_ERR_DEVICE_CHECK);
+      len_out[b] = 0;
+      tau_out[b] = INFINITY;
+    }
+    return;
+  }
+  const int A = L - s;
+  if (A == 0) {
+    if (tid == 0) {
+      len_out[b] = 0;
+      tau_out[b] = INFINITY;
+    }
+    return;
+  }
+  const float* row = score + (int64_t)b * L + s;
+  const int seg = (A + kPrefixScanThreads - 1) / kPrefixScanThreads;
+  const int p0 = tid * seg, p1 = min(A, p0 + seg);
+  // 1. segment minimum (NaN counts as -inf) and first NaN
+  float smin = INFINITY;
+  int first_nan = A;
+  for (int p = p0; p < p1; ++p) {
+    const float v = __ldca(row + p);
+    if (isnan(v)) {
+      smin = -INFINITY;
+      first_nan = min(first_nan, p);
+    } else {
+      smin = fminf(smin, v);
+    }
+  }
+  // 2. exclusive block min-scan of the segment minima
+  float incl = smin;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl = fminf(incl, t);
+  }
+  if (lane == 31) warp_min[warp] = incl;
+  __syncthreads();
+  float before_warp = INFINITY;
+  for (int w = 0; w < warp; ++w) before_warp = fminf(before_warp, warp_min[w]);
+  const float excl_lane = __shfl_up_sync(0xffffffffu, incl, 1);
+  const float before = fminf(before_warp, lane == 0 ? INFINITY : excl_lane);
+  // 3. tau = prefix minimum at k_lo
+  // ceil(lo A) and floor(hi A) of the float32 fractions, products exact in double
+  int k_lo = (int)ceil((double)lo * (double)A);
+  k_lo = k_lo < 1 ? 1 : (k_lo > A ? A : k_lo);
+  int k_hi = (int)floor((double)hi * (double)A);
+  k_hi = k_hi < k_lo ? k_lo : k_hi;
+  if (k_lo - 1 >= p0 && k_lo - 1 < p1) {
+    float m = before;
+    for (int p = p0; p < k_lo; ++p) {
+      const float v = __ldca(row + p);
+      m = fminf(m, isnan(v) ? -INFINITY : v);
+    }
+    s_tau = m;
+  }
+  __syncthreads();
+  const float tau = s_tau;
+  // 4. first position whose prefix minimum falls below tau
+  int fail = A;
+  {
+    float m = before;
+    for (int p = p0; p < p1; ++p) {
+      const float v = __ldca(row + p);
+      m = fminf(m, isnan(v) ? -INFINITY : v);
+      if (!(m >= tau)) {
+        fail = p;
+        break;
+      }
+    }
+  }
+  fail = warp_min_int(fail);
+  first_nan = warp_min_int(first_nan);
+  if (lane == 0) {
+    s_fail[warp] = fail;
+    s_nan[warp] = first_nan;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int f = A, fn = A;
+    for (int w = 0; w < kPrefixScanThreads / 32; ++w) {
+      f = min(f, s_fail[w]);
+      fn = min(fn, s_nan[w]);
+    }
+    int len = min(k_hi, min(f, fn));
+    if (len < 1) len = 1;
+    len_out[b] = len;
+    tau_out[b] = tau;
+    if (advance) start[b] = s + len;
+  }
+}
+
+template <typename T>
+int lock_nchunks(int V) {
+  const int n = (V + lock_chunk_elems<T>() - 1) / lock_chunk_elems<T>();
+  return n < 1 ? 1 : n;
+}
+
+template <typename T>
+cudaError_t launch_lock_typed(const T* z, const T* y, int B, int R_src, int V, int64_t rs,
+                              int64_t bs, int R_max, const int32_t* row_idx,
+                              const int32_t* count, const int32_t* out_idx, int out_cols,
+                              float eps, float gate_q, float* kl_out, float* unc_out,
+                              uint8_t* locked, void* ws, int32_t* dev_status,
+                              cudaStream_t stream) {
+  constexpr int E = lvec<T>();
+  const int nchunks = lock_nchunks<T>(V);
+  if (nchunks > 65535 || (int64_t)B * R_max > INT_MAX) return cudaErrorInvalidConfiguration;
+  const bool vec = (reinterpret_cast<uintptr_t>(z) % 16 == 0) &&
+                   (reinterpret_cast<uintptr_t>(y) % 16 == 0) && (rs % E == 0) && (bs % E == 0);
+  LockPartial* part = static_cast<LockPartial*>(ws);
+  dim3 grid(B * R_max, nchunks);
+  if (vec)
+    launch_pdl(lock_partial_kernel<T, true>, grid, kLockThreads, 0, stream, z, y, R_src, V, rs,
+               bs, R_max, row_idx, count, nchunks, part);
+  else
+    launch_pdl(lock_partial_kernel<T, false>, grid, kLockThreads, 0, stream, z, y, R_src, V, rs,
+               bs, R_max, row_idx, count, nchunks, part);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  const int64_t rows = (int64_t)B * R_max;
+  launch_pdl(lock_merge_kernel, (unsigned)((rows + 7) / 8), 256, 0, stream, B, R_src, R_max,
+             row_idx, count, out_idx, out_cols, nchunks, part, kl_out, unc_out, dev_status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || locked == nullptr) return e;
+  const size_t smem = (size_t)R_max * sizeof(uint32_t);
+  if (R_max > kGateMaxRows) return cudaErrorInvalidValue;
+  // the limit is set once per kernel: raise it to the largest size any call uses
+  e = ensure_smem_limit(reinterpret_cast<const void*>(lock_gate_kernel),
+                        kGateMaxRows * (int)sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  launch_pdl(lock_gate_kernel, B, kGateThreads, smem, stream, R_max, count, out_idx, out_cols,
+             kl_out, unc_out, eps, gate_q, locked, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t lock_workspace_bytes(int B, int R_max, int V, int dtype) {
+  const int n = dtype == DLLM_BF16 ? lock_nchunks<__nv_bfloat16>(V) : lock_nchunks<float>(V);
+  return (size_t)B * (size_t)R_max * (size_t)n * sizeof(LockPartial);
+}
+
+cudaError_t launch_lock_criterion(const void* z, const void* y, int dtype, int B, int R_src,
+                                  int V, int64_t rs, int64_t bs, int R_max,
+                                  const int32_t* row_idx, const int32_t* count,
+                                  const int32_t* out_idx, int out_cols, float eps, float gate_q,
+                                  float* kl_out, float* unc_out, uint8_t* locked, void* ws,
+                                  int32_t* dev_status, cudaStream_t stream) {
+  if (dtype == DLLM_BF16)
+    return launch_lock_typed(static_cast<const __nv_bfloat16*>(z),
+                             static_cast<const __nv_bfloat16*>(y), B, R_src, V, rs, bs, R_max,
+                             row_idx, count, out_idx, out_cols, eps, gate_q, kl_out, unc_out,
+                             locked, ws, dev_status, stream);
+  return launch_lock_typed(static_cast<const float*>(z), static_cast<const float*>(y), B, R_src,
+                           V, rs, bs, R_max, row_idx, count, out_idx, out_cols, eps, gate_q,
+                           kl_out, unc_out, locked, ws, dev_status, stream);
+}
+
+cudaError_t launch_adaptive_prefix(const float* score, int B, int L, int32_t* start, float lo,
+                                   float hi, int advance_start, int32_t* len_out, float* tau_out,
+                                   int32_t* dev_status, cudaStream_t stream) {
+  launch_pdl(adaptive_prefix_kernel, B, kPrefixScanThreads, 0, stream, score, L, start, lo, hi,
+             advance_start, len_out, tau_out, dev_status);
+  return cudaGetLastError();
+}
+
+}  // namespace dllm

@@ -511,8 +511,8 @@ def test_adaptive_prefix_brute_force_characterisation():
                     if A == 0:
                         assert ln[0] == 0 and np.isinf(tau[0])
                         continue
-                    k_lo = min(A, max(1, math.ceil(lo * A)))
-                    k_hi = max(k_lo, math.floor(hi * A))
+                    k_lo = min(A, max(1, math.ceil(float(np.float32(lo)) * A)))
+                    k_hi = max(k_lo, math.floor(float(np.float32(hi)) * A))
                     seg = score[0, start:]
                     assert tau[0] == np.min(seg[:k_lo])
                     feasible = [k for k in range(1, k_hi + 1) if np.all(seg[:k] >= tau[0])]
