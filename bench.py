@@ -49,6 +49,11 @@ CSRC = os.path.join(ROOT, "partial_attention_saliency_b300", "csrc")
 
 ENTRY_ORDER = ["dllm_saliency_select", "dllm_kv_scatter", "dllm_partial_attention",
                "dllm_attention_colsum", "dllm_confidence", "dllm_stable_prefix"]
+# the lock criterion between consecutive steps' logits and the adaptive prefix
+# threshold, appended to the step with --surelock
+SURELOCK_ORDER = ["dllm_lock_criterion", "dllm_adaptive_prefix"]
+LOCK_EPS, LOCK_GATE_Q = 1e-3, 0.5     # KL threshold, uncertainty percentile gate
+ADAPT_LO, ADAPT_HI = 0.25, 0.5        # fraction of the active length the prefix covers
 KERNELS = {  # kernels each entry point launches, and the source they come from
     "dllm_saliency_select": (["cos_rows_kernel", "compact_kernel"], "select.cu"),
     "dllm_kv_scatter": (["kv_scatter_kernel"], "kv_scatter.cu"),
@@ -57,6 +62,9 @@ KERNELS = {  # kernels each entry point launches, and the source they come from
     "dllm_attention_colsum": (["attn_colsum_tc_kernel"], "attention_tc.cu"),
     "dllm_confidence": (["conf_stream_kernel", "conf_merge_kernel"], "confidence.cu"),
     "dllm_stable_prefix": (["stable_prefix_kernel"], "stable_prefix.cu"),
+    "dllm_lock_criterion": (["lock_partial_kernel", "lock_merge_kernel", "lock_gate_kernel"],
+                            "lock.cu"),
+    "dllm_adaptive_prefix": (["adaptive_prefix_kernel"], "lock.cu"),
 }
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of an
@@ -88,6 +96,9 @@ def parse():
     ap.add_argument("--pattern", choices=["random", "cluster"], default="random")
     ap.add_argument("--locked", type=float, default=0.0,
                     help="long_4k: locked fraction (0 = first step of the schedule)")
+    ap.add_argument("--surelock", action="store_true",
+                    help="long_4k, long_4k_schedule: add the lock criterion between this and "
+                         "the previous step's logits of the active rows and the adaptive prefix")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time spent on the oracle baseline sample")
@@ -238,9 +249,29 @@ class Workload:
     default_steps: int
     desc: str
     schedule: int = 0  # steps of a lock schedule (masks from lock_schedule), 0 = none
+    surelock: bool = False  # lock criterion and adaptive prefix after the six calls
+
+
+def entries(wl: "Workload"):
+    return ENTRY_ORDER + (SURELOCK_ORDER if wl.surelock else [])
 
 
 def make_workload(args) -> Workload:
+    wl = _make_workload(args)
+    if args.surelock:
+        if wl.conf != "gather":
+            raise SystemExit("--surelock needs a long_4k workload (logits of every position)")
+        wl = dataclasses.replace(
+            wl, name=wl.name + "_surelock", surelock=True,
+            desc=wl.desc + f"; then the lock criterion (KL < {LOCK_EPS}, uncertainty gate at "
+                           f"the {round(100 * LOCK_GATE_Q)}th percentile) between these and the "
+                           f"previous step's logits of the active rows, and the adaptive prefix "
+                           f"({round(100 * ADAPT_LO)}-{round(100 * ADAPT_HI)}% of the active "
+                           f"length)")
+    return wl
+
+
+def _make_workload(args) -> Workload:
     if args.workload == "step_1k":
         s = workloads.STEP_1K
         return Workload("step_1k", s, s.n_salient, "random", 0.0, "window", s.logit_rows, 10000,
@@ -286,6 +317,14 @@ def build_set(wl: Workload, seed: int, device):
     g = torch.Generator().manual_seed(seed + 7)
     if wl.conf == "gather":
         inp["logits"] = workloads.normal(g, (s.B, s.L, s.V), 2.0, s.dtype)
+        if wl.surelock:
+            # the previous step's logits: these plus noise whose scale, one per
+            # position, spans 1e-3 .. 1, so the divergences span decades
+            scale = torch.logspace(-3, 0, s.L)[torch.randperm(s.L, generator=g)]
+            prev = inp["logits"].float()
+            prev.add_(scale[None, :, None] * torch.randn(prev.shape, generator=g))
+            inp["logits_prev"] = prev.to(s.dtype)
+            del prev
     elif wl.conf == "compact":
         inp["logits"] = workloads.normal(g, (s.B, wl.logit_rows, s.V), 2.0, s.dtype)
     locked = None
@@ -304,6 +343,8 @@ def build_set(wl: Workload, seed: int, device):
         d["logits"] = buf
     elif wl.conf is not None:
         d["logits"] = inp["logits"].to(device)
+    if wl.surelock:
+        d["logits_prev"] = inp["logits_prev"].to(device)
     d["score"] = torch.full((s.B, s.L), float("inf"), device=device)
     d["start"] = torch.full((s.B,), s.win_start, dtype=torch.int32, device=device)
     d["host"] = inp
@@ -355,11 +396,22 @@ class Buffers:
         aw = dl.dllm_attention_workspace_bytes(s.B, s.L, s.H, s.d, self.M_max, s.dtype)
         self.attn_ws = torch.empty((max(aw, 16),), dtype=torch.uint8, device=device)
         self.attn_split = aw > 0
+        if wl.surelock:
+            self.kl = torch.empty((s.B, s.L), dtype=f32, device=device)
+            self.unc = torch.empty((s.B, s.L), dtype=f32, device=device)
+            self.lock_flags = torch.zeros((s.B, s.L), dtype=torch.uint8, device=device)
+            lw = dl.dllm_lock_workspace_bytes(s.B, s.Lw, s.V, s.dtype)
+            self.lock_ws = torch.empty((max(lw, 16),), dtype=torch.uint8, device=device)
+            self.alen = torch.empty((s.B,), dtype=i32, device=device)
+            self.atau = torch.empty((s.B,), dtype=f32, device=device)
 
 
 def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None, locked=None):
-    """The six calls in order; optional events bracket each call.  ``locked``
-    overrides the set's locked mask (schedule steps)."""
+    """The six calls in order (eight with the lock criterion and the adaptive
+    prefix); optional events bracket each call.  ``locked`` overrides the
+    set's locked mask (schedule steps).  The lock flags go to a buffer of
+    their own: the set's mask or the schedule decides what is locked, so that
+    every replay of the step does the same work."""
     s = wl.shape
     w = s.win_start
     ev = events
@@ -398,12 +450,25 @@ def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None, locked=None)
     dl.dllm_stable_prefix(d["score"], d["start"], 0.9, min_commit=True, advance_start=False,
                           len_out=bf.length, dev_status=bf.dev_status, stream=stream)
     if ev: ev[6].record(stream)
+    if not wl.surelock:
+        return
+    dl.dllm_lock_criterion(d["logits"], d["logits_prev"], LOCK_EPS, gate_q=LOCK_GATE_Q,
+                           R_max=s.Lw, row_idx=bf.idx, count=bf.count, out_idx=bf.idx,
+                           out_cols=s.L, kl_out=bf.kl, unc_out=bf.unc,
+                           locked_inout=bf.lock_flags, ws=bf.lock_ws, dev_status=bf.dev_status,
+                           stream=stream)
+    if ev: ev[7].record(stream)
+    dl.dllm_adaptive_prefix(d["score"], d["start"], ADAPT_LO, ADAPT_HI, len_out=bf.alen,
+                            tau_out=bf.atau, dev_status=bf.dev_status, stream=stream)
+    if ev: ev[8].record(stream)
 
 
 def launches_per_step(wl: Workload, bf: Buffers) -> int:
     n = 2 + 1 + (2 if bf.attn_split else 1) + 1 + 1
     if wl.conf is not None:
         n += 2
+    if wl.surelock:
+        n += 3 + 1
     return n
 
 
@@ -428,7 +493,11 @@ def algorithmic_work(wl: Workload, counts):
         conf_rows = M
     conf_b = conf_rows * (s.V * el + 12)
     prefix_b = s.B * s.Lw * 4
+    # both logit rows of every active row, its index twice, kl, unc and flag
+    lock_b = M * (2 * s.V * el + 4 + 4 + 4 + 4 + 1)
     return {
+        "dllm_lock_criterion": {"bytes": lock_b, "flops": 0.0},
+        "dllm_adaptive_prefix": {"bytes": s.B * s.Lw * 4, "flops": 0.0},
         "dllm_saliency_select": {"bytes": select_b, "flops": 6.0 * s.B * s.Lw * s.D},
         "dllm_kv_scatter": {"bytes": scatter_b, "flops": 0.0},
         "dllm_partial_attention": {"bytes": attn_b, "flops": attn_f},
@@ -471,6 +540,10 @@ def oracle_step(wl: Workload, h, b: int, locked_mask=None):
         conf, _, _ = oracle.confidence(f("logits"), count=[n])
         score[0, idx[0, :n]] = conf[0, :n]
     oracle.stable_prefix(score, [w], 0.9, True)
+    if wl.surelock:
+        kl, unc = oracle.lock_kl(f("logits"), f("logits_prev"), count=count, row_idx=idx)
+        oracle.lock_decision(kl, unc, count, LOCK_EPS, LOCK_GATE_Q)
+        oracle.adaptive_prefix(score, [w], ADAPT_LO, ADAPT_HI)
     return int(count[0])
 
 
@@ -606,7 +679,8 @@ def main():
     with torch.cuda.graph(g_timed, stream=cap):
         for i in range(S):
             run_step(dl, wl, bf, sets[i % n_sets], torch.cuda.current_stream(), locked=lk(i))
-    nev = len(ENTRY_ORDER) + 1
+    order = entries(wl)
+    nev = len(order) + 1
     ev = [[torch.cuda.Event(enable_timing=True, external=True) for _ in range(nev)]
           for _ in range(S)]
     g_events = torch.cuda.CUDAGraph()
@@ -634,9 +708,9 @@ def main():
     torch.cuda.synchronize()
     assert int(bf.dev_status[0]) == 0, "device-side check failed"
     elapsed_ms = t_start.elapsed_time(t_end)
-    per_entry = {n: 0.0 for n in ENTRY_ORDER}
+    per_entry = {n: 0.0 for n in order}
     for i in range(S):
-        for j, n in enumerate(ENTRY_ORDER):
+        for j, n in enumerate(order):
             per_entry[n] += ev[i][j].elapsed_time(ev[i][j + 1])
     events_step_ms = sum(per_entry.values()) / S
     active_total = sum(sum(counts_per_step[i % period]) for i in range(S)) * (K // S)
@@ -655,7 +729,7 @@ def main():
     work = algorithmic_work(wl, mean_counts)
     ridge = pk["bf16_tflops"] * 1e12 / (pk["hbm_gbs"] * 1e9)
     kernels = {}
-    for n in ENTRY_ORDER:
+    for n in order:
         if n == "dllm_confidence" and wl.conf is None:
             continue
         avg_ms = per_entry[n] / S
@@ -734,6 +808,13 @@ def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev, lk, count
         "argmax": torch.empty_like(bf.argmax, device="cpu").pin_memory(),
         "length": torch.empty_like(bf.length, device="cpu").pin_memory(),
     }
+    out_dev = [("idx", bf.idx), ("count", bf.count), ("o", bf.o), ("lse", bf.lse),
+               ("colsum", bf.colsum), ("score", None), ("argmax", bf.argmax),
+               ("length", bf.length)]
+    if wl.surelock:  # the previous step's logits stay on the device
+        for k, t in (("lock_flags", bf.lock_flags), ("alen", bf.alen)):
+            out_host[k] = torch.empty_like(t, device="cpu").pin_memory()
+            out_dev.append((k, t))
     h2d = sum(t.numel() * t.element_size() for t in pinned[0].values())
     d2h = sum(t.numel() * t.element_size() for t in out_host.values())
 
@@ -743,10 +824,8 @@ def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev, lk, count
             dst = d[k][:, :pinned[i % n_sets][k].shape[1]] if k == "logits" else d[k]
             dst.copy_(pinned[i % n_sets][k], non_blocking=True)
         run_step(dl, wl, bf, d, stream, locked=lk(i))
-        for k, src in (("idx", bf.idx), ("count", bf.count), ("o", bf.o), ("lse", bf.lse),
-                       ("colsum", bf.colsum), ("score", d["score"]), ("argmax", bf.argmax),
-                       ("length", bf.length)):
-            out_host[k].copy_(src, non_blocking=True)
+        for k, src in out_dev:
+            out_host[k].copy_(d["score"] if src is None else src, non_blocking=True)
 
     for i in range(max(args.warmup, 3)):
         one(i)

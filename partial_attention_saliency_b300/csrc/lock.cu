@@ -9,10 +9,13 @@
 // threshold of the stable prefix is chosen so that the committed block
 // covers a fraction [lo, hi] of the active length.
 //
-// lock_partial_kernel  one CTA per (row, 32 KB chunk of each of the two
-//                      logit rows): block maxima of z and y first, then
-//                      sum exp(z - Mz), sum exp(z - Mz)(z - y) and
-//                      sum exp(y - My); HBM bound, 2 V sizeof(T) per row.
+// lock_partial_kernel  one CTA per (row, chunk of 256 kLockU 16-byte vectors
+//                      of each of the two logit rows): every thread sums
+//                      exp(z - mz), exp(z - mz)(z - y) and exp(y - my) over
+//                      its own elements relative to its own maxima, then
+//                      rescales them to the block maxima (one exchange) and
+//                      the block adds them up; HBM bound, 2 V sizeof(T) per
+//                      row.
 // lock_merge_kernel    one warp per row folds the chunks in a fixed order and
 //                      evaluates KL = A / lz - (Mz + ln lz) + (My + ln ly) in
 //                      double; the uncertainty is 1 - 1 / lz.
@@ -32,7 +35,19 @@ namespace dllm {
 namespace {
 
 constexpr int kLockThreads = 256;
-constexpr int kLockU = 8;  // 16-byte vectors per thread per chunk and input
+// Tuned on bf16 rows of 126464 logits: 4 16-byte vectors per thread and
+// input with at least 4 CTAs per SM (64 registers, a 56-byte spill) ran at
+// 333 us for 2867 rows, against 370 us at 3 CTAs per SM, 388 us with 2
+// vectors and 518 us with 8.  Taking a quarter to a half of the previous
+// row's exponentials from an FMA-pipe polynomial instead of the SFU was
+// slower (457 to 476 us): the SFU is not the limit here.
+#ifndef DLLM_LOCK_U
+#define DLLM_LOCK_U 4
+#endif
+#ifndef DLLM_LOCK_MINB
+#define DLLM_LOCK_MINB 4
+#endif
+constexpr int kLockU = DLLM_LOCK_U;  // 16-byte vectors per thread per chunk and input
 constexpr int kGateThreads = 1024;
 constexpr int kGateMaxRows = 16384;  // uncertainty keys held in shared memory (64 KB)
 
@@ -98,37 +113,17 @@ __device__ __forceinline__ bool lock_row(int b, int r, int R_max, int R_src,
   return true;
 }
 
-__device__ __forceinline__ float block_max(float v, float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_max(v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float m = red[0];
-  for (int w = 1; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-  __syncthreads();
-  return m;
-}
-
-__device__ __forceinline__ float block_sum(float v, float* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_sum(v);
-  if (lane == 0) red[warp] = v;
-  __syncthreads();
-  float s = 0.f;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];  // fixed order
-  __syncthreads();
-  return s;
-}
-
 template <typename T, bool VEC>
-__global__ void __launch_bounds__(kLockThreads)
+__global__ void __launch_bounds__(kLockThreads, DLLM_LOCK_MINB)
 lock_partial_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs, int64_t bs, int R_max,
                     const int32_t* row_idx, const int32_t* count, int nchunks, LockPartial* ws) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  __shared__ float red[kLockThreads / 32];
+  __shared__ float red_max[2][kLockThreads / 32];
+  __shared__ float red_sum[3][kLockThreads / 32];
   constexpr int E = lvec<T>();
   const int br = blockIdx.x, chunk = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = br / R_max, r = br - b * R_max;
   int row;
   bool bad;
@@ -145,42 +140,76 @@ lock_partial_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs, int6
     vz[u] = vi < nvec ? lload<T, VEC>(zrow, vi, V) : make_uint4(sent, sent, sent, sent);
     vy[u] = vi < nvec ? lload<T, VEC>(yrow, vi, V) : make_uint4(sent, sent, sent, sent);
   }
+  // 1. this thread's maxima and its sums relative to them: no block-wide
+  //    step before the exponentials
   float mz = -INFINITY, my = -INFINITY;
 #pragma unroll
   for (int u = 0; u < kLockU; ++u)
 #pragma unroll
-    for (int e = 0; e < E; ++e) {
-      mz = fmaxf(mz, lelem<T>(vz[u], e));
-      my = fmaxf(my, lelem<T>(vy[u], e));
+    for (int e = 0; e < E; e += 2) {
+      mz = fmax3(mz, lelem<T>(vz[u], e), lelem<T>(vz[u], e + 1));
+      my = fmax3(my, lelem<T>(vy[u], e), lelem<T>(vy[u], e + 1));
     }
-  const float Mz = block_max(mz, red);
-  const float My = block_max(my, red);
   float lz = 0.f, a = 0.f, ly = 0.f;
-  if (Mz != -INFINITY) {
-    const float nz = -Mz * kLog2e, ny = -My * kLog2e;
+  if (mz != -INFINITY) {
+    const float nz = -mz * kLog2e, ny = -my * kLog2e;
 #pragma unroll
     for (int u = 0; u < kLockU; ++u)
 #pragma unroll
-      for (int e = 0; e < E; ++e) {
-        const float z = lelem<T>(vz[u], e), y = lelem<T>(vy[u], e);
-        if (z != -INFINITY) {  // padding past the row end
-          const float pz = ex2_approx(fmaf(z, kLog2e, nz));
-          lz += pz;
-          a = fmaf(pz, z - y, a);
-          ly += ex2_approx(fmaf(y, kLog2e, ny));
+      for (int e = 0; e < E; e += 2) {
+        const float z0 = lelem<T>(vz[u], e), z1 = lelem<T>(vz[u], e + 1);
+        const float y0 = lelem<T>(vy[u], e), y1 = lelem<T>(vy[u], e + 1);
+        const float p0 = ex2_approx(fmaf(z0, kLog2e, nz));
+        const float p1 = ex2_approx(fmaf(z1, kLog2e, nz));
+        const float q0 = ex2_approx(fmaf(y0, kLog2e, ny));
+        const float q1 = ex2_approx(fmaf(y1, kLog2e, ny));
+        // padding past the row end holds -inf in both rows: no contribution
+        if (z0 != -INFINITY) {
+          lz += p0;
+          a = fmaf(p0, z0 - y0, a);
+          ly += q0;
+        }
+        if (z1 != -INFINITY) {
+          lz += p1;
+          a = fmaf(p1, z1 - y1, a);
+          ly += q1;
         }
       }
   }
-  lz = block_sum(lz, red);
-  a = block_sum(a, red);
-  ly = block_sum(ly, red);
+  // 2. block maxima (one exchange), each thread rescales its own sums
+  const float wz = warp_max(mz), wy = warp_max(my);
+  if (lane == 0) {
+    red_max[0][warp] = wz;
+    red_max[1][warp] = wy;
+  }
+  __syncthreads();
+  float Mz = red_max[0][0], My = red_max[1][0];
+#pragma unroll
+  for (int w = 1; w < kLockThreads / 32; ++w) {
+    Mz = fmaxf(Mz, red_max[0][w]);
+    My = fmaxf(My, red_max[1][w]);
+  }
+  const float cz = mz == -INFINITY ? 0.f : ex2_approx((mz - Mz) * kLog2e);
+  const float cy = my == -INFINITY ? 0.f : ex2_approx((my - My) * kLog2e);
+  lz = warp_sum(lz * cz);
+  a = warp_sum(a * cz);
+  ly = warp_sum(ly * cy);
+  if (lane == 0) {
+    red_sum[0][warp] = lz;
+    red_sum[1][warp] = a;
+    red_sum[2][warp] = ly;
+  }
+  __syncthreads();
   if (threadIdx.x == 0) {
     LockPartial out;
     out.mz = Mz;
-    out.lz = lz;
-    out.a = a;
     out.my = My;
-    out.ly = ly;
+    out.lz = out.a = out.ly = 0.f;
+    for (int w = 0; w < kLockThreads / 32; ++w) {  // fixed order
+      out.lz += red_sum[0][w];
+      out.a += red_sum[1][w];
+      out.ly += red_sum[2][w];
+    }
     out.pad0 = out.pad1 = out.pad2 = 0.f;
     ws[(int64_t)br * nchunks + chunk] = out;
   }
@@ -249,13 +278,19 @@ __global__ void lock_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
     const double kl = (double)acc.a / (double)acc.lz - lse_z + lse_y;
     const int64_t o = (int64_t)b * out_cols + col;
     kl_out[o] = (float)kl;
-    unc_out[o] = 1.0f - 1.0f / acc.lz;
+    // lz >= 1 up to rounding (the largest term is exp(0)): clamp at 0
+    unc_out[o] = fmaxf(1.0f - 1.0f / acc.lz, 0.0f);
   }
 }
 
-// Order-preserving key of a non-negative float (NaN sorts last).
+// Order-preserving unsigned key of a float (NaN sorts last), and its inverse.
 __device__ __forceinline__ uint32_t ukey(float u) {
-  return isnan(u) ? 0xffffffffu : __float_as_uint(u);
+  if (isnan(u)) return 0xffffffffu;
+  const uint32_t x = __float_as_uint(u);
+  return (x & 0x80000000u) ? ~x : (x | 0x80000000u);
+}
+__device__ __forceinline__ float ukey_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
 __global__ void __launch_bounds__(kGateThreads)
@@ -309,7 +344,7 @@ lock_gate_kernel(int R_max, const int32_t* count, const int32_t* out_idx, int ou
       __syncthreads();
     }
     const uint32_t tk = s_prefix;
-    t = tk == 0xffffffffu ? INFINITY : __uint_as_float(tk);
+    t = tk == 0xffffffffu ? INFINITY : ukey_value(tk);
   }
   if (locked == nullptr) return;
   const float e32 = eps;
