@@ -714,13 +714,7 @@ def main():
             per_entry[n] += ev[i][j].elapsed_time(ev[i][j + 1])
     events_step_ms = sum(per_entry.values()) / S
     active_total = sum(sum(counts_per_step[i % period]) for i in range(S)) * (K // S)
-    if pg:
-        t = torch.tensor([elapsed_ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
-        a = torch.tensor([float(active_total)], device=device)
-        pg.all_reduce(a, op=pg.ReduceOp.SUM)
-        active_total = a.item()
+    elapsed_ms, active_total = reduce_over_ranks(pg, elapsed_ms, active_total, device)
     value = active_total / (elapsed_ms / 1e3)
     ms_per_step = elapsed_ms / K
 
@@ -793,6 +787,18 @@ def main():
     return 0
 
 
+def reduce_over_ranks(pg, elapsed_ms: float, units: float, device):
+    """Whole-job figures of a replicated run: the slowest rank's time and the
+    units all ranks processed (each rank steps its own batch rows)."""
+    if pg is None:
+        return elapsed_ms, units
+    t = torch.tensor([float(elapsed_ms)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    pg.all_reduce(u, op=pg.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev, lk, counts_per_step):
     """Same metric through the public API with pinned host buffers: H2D of the
     step's fresh inputs and D2H of its results inside the timed region."""
@@ -840,12 +846,8 @@ def e2e_run(dl, wl, bf, sets, n_sets, stream, args, pg, device, K_dev, lk, count
     b.record(stream)
     torch.cuda.synchronize()
     ms = a.elapsed_time(b)
-    if pg:
-        t = torch.tensor([ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
     active = sum(sum(counts_per_step[i % len(counts_per_step)]) for i in range(K))
-    active *= pg.get_world_size() if pg else 1
+    ms, active = reduce_over_ranks(pg, ms, active, device)
     return {"value": active / (ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": K, "ms_per_step": ms / K}
 

@@ -83,6 +83,44 @@ def test_invalid_arguments_rejected_before_launch(lib):
     assert st == 1
 
 
+def test_lock_workspace_query_host_only(lib):
+    # one 32-byte partial per (row, chunk of 256 threads x 4 16-byte vectors)
+    assert lib.dllm_lock_workspace_bytes(1, 100, 126464, 1) == 100 * 16 * 32
+    assert lib.dllm_lock_workspace_bytes(2, 100, 126464, 1) == 2 * 100 * 16 * 32
+    assert lib.dllm_lock_workspace_bytes(1, 100, 126464, 0) == 100 * 31 * 32  # f32: 4 per vector
+    assert lib.dllm_lock_workspace_bytes(0, 100, 126464, 1) == 0
+    assert lib.dllm_lock_workspace_bytes(1, 100, 126464, 5) == 0
+
+
+def test_lock_and_adaptive_prefix_rejected_before_launch(lib):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    big = 1 << 30
+
+    def lock(z=p, V=64, rs=64, R_max=4, out_cols=4, kl=p, locked=None, ws_bytes=big, ws=p,
+             row_idx=None):
+        return lib.dllm_lock_criterion(z, p, 1, 1, 4, V, rs, 4 * rs, R_max, row_idx, None, None,
+                                       out_cols, 0.1, 0.5, kl, p, locked, ws, ws_bytes, None,
+                                       None)
+
+    assert lock(z=None) == 1 and b"NULL" in lib.dllm_last_error()
+    assert lock(kl=None) == 1 and b"NULL" in lib.dllm_last_error()
+    assert lock(V=0) == 1
+    assert lock(rs=32) == 1 and b"row_stride" in lib.dllm_last_error()
+    assert lock(R_max=8) == 1 and b"row_idx" in lib.dllm_last_error()
+    assert lock(R_max=8, row_idx=p, out_cols=4) == 1 and b"out_cols" in lib.dllm_last_error()
+    assert lock(ws_bytes=16) == 1 and b"workspace" in lib.dllm_last_error()
+    assert lock(ws=ctypes.c_void_p(0x1004)) == 1 and b"misaligned" in lib.dllm_last_error()
+    st = lib.dllm_lock_criterion(p, p, 1, 1, 4, 64, 64, 256, 20000, p, None, p, 20000, 0.1, 0.5,
+                                 p, p, p, p, big, None, None)
+    assert st == 1 and b"16384" in lib.dllm_last_error()
+    st = lib.dllm_adaptive_prefix(None, 1, 16, p, 0.25, 0.5, 0, p, p, None, None)
+    assert st == 1 and b"NULL" in lib.dllm_last_error()
+    st = lib.dllm_adaptive_prefix(p, 1, 16, p, 0.25, 1.5, 0, p, p, None, None)
+    assert st == 1 and b"fractions" in lib.dllm_last_error()
+    st = lib.dllm_adaptive_prefix(p, 0, 16, p, 0.25, 0.5, 0, p, p, None, None)
+    assert st == 1
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from partial_attention_saliency_b300 import _lib
     with pytest.raises(ImportError):
