@@ -21,5 +21,8 @@ from .dllm_oracle import (  # noqa: F401
     lock_kl,
     lock_decision,
     adaptive_prefix,
+    approx_attention_update,
+    attn_scores,
+    attn_sampler_select,
     step,
 )

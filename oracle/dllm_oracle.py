@@ -49,6 +49,9 @@ __all__ = [
     "lock_kl",
     "lock_decision",
     "adaptive_prefix",
+    "approx_attention_update",
+    "attn_scores",
+    "attn_sampler_select",
     "step",
 ]
 
@@ -394,6 +397,115 @@ def adaptive_prefix(score, start, lo: float, hi: float):
         lens[b] = max(ln, 1)
         taus[b] = tau
     return lens, taus
+
+
+# --------------------------------------------------------------------------
+# Approximate attention update of the stable rows (the non-salient path)
+# --------------------------------------------------------------------------
+
+def approx_attention_update(o_prev, q_prev, lse_prev, k_prev, v_prev, v_new, idx, count,
+                            stable_idx, stable_count, scale: Optional[float] = None):
+    """Output of the stable rows after this step's value changes.
+
+    DyLLM, technical summary, Methodology 2 (non-salient path): for a stable
+    row the change of its attention weights is taken as negligible, and its
+    output is updated by the change of the value vectors of the salient
+    tokens weighted by the existing attention weights; cost O(N |A_t|).
+    Reading: the existing weights are the previous step's softmax row,
+    recovered exactly from the cached query, the previous keys of the salient
+    positions and the cached log-sum-exp:
+    p_ij = exp(scale q_i . k_j - lse_i), and
+    o_i <- o_i + sum_{a < count} p_{i, idx_a} (v_new_a - v_prev[idx_a]).
+
+    o_prev, q_prev, k_prev, v_prev [B, L, H, d] (the previous step's outputs,
+    queries, keys and values of every position; k_prev and v_prev before this
+    step's cache update); lse_prev [B, H, L]; v_new [B, M_max, H, d], row a
+    the fresh value of position idx[b, a] for a < count[b]; stable rows
+    stable_idx[b, r] for r < stable_count[b].  Returns an updated copy of
+    o_prev (only the stable rows change).
+    """
+    o = np.array(_f64(o_prev), copy=True)
+    q, lse, k, v, vn = (_f64(x) for x in (q_prev, lse_prev, k_prev, v_prev, v_new))
+    B, L, H, d = o.shape
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    for b in range(B):
+        A = [int(idx[b][a]) for a in range(int(count[b]))]
+        rows = [int(stable_idx[b][r]) for r in range(int(stable_count[b]))]
+        if not A or not rows:
+            continue
+        for h in range(H):
+            Q = q[b, rows, h, :]                       # [N, d]
+            K_A = k[b, A, h, :]                        # [|A|, d]
+            dV = vn[b, :len(A), h, :] - v[b, A, h, :]  # [|A|, d]
+            P = np.exp(scale * (Q @ K_A.T) - lse[b, h, rows][:, None])
+            o[b, rows, h, :] += P @ dV
+    return o
+
+
+# --------------------------------------------------------------------------
+# Attention-guided decoding order (Attn-Sampler)
+# --------------------------------------------------------------------------
+
+def attn_scores(colsum):
+    """Total attention each position receives.
+
+    Attn-Sampler, technical summary, Methodology 1 (key insight: decode in
+    descending order of the column sums of the attention matrix) and the
+    ablation on layers and heads (aggregating over all of them works best).
+    colsum [B, ..., L] (per head, or per layer and head); returns the sum over
+    every axis between the batch and the position axis, [B, L].
+    """
+    c = _f64(colsum)
+    return c.reshape(c.shape[0], -1, c.shape[-1]).sum(axis=1)
+
+
+def attn_sampler_select(score, candidates, tau: float, gamma: float, k_max: int):
+    """Decoding order and the number of tokens to decode in parallel.
+
+    Attn-Sampler, technical summary, Methodology 2: tokens with the highest
+    column sums are decoded first (order determination); tokens are decoded
+    in parallel only while their score exceeds a threshold (parallel
+    decoding).  The page does not print the dynamic threshold; reading: the
+    threshold of a step is thr = max(tau, gamma * a_top), a floor given by the
+    caller and a fraction of that step's top score (gamma = 1 gives one token
+    per step unless the top is tied; gamma <= 0 drops the second term, a
+    static threshold).
+
+    score [B, L] (compared as float32); candidates [B, L] nonzero where a
+    position may be decoded (None: all).  order[b] lists the candidates by
+    descending score, equal scores by ascending position, NaN last (-0 and +0
+    are equal), padded with -1; n[b] is the number of leading entries with
+    score >= thr (float32, thr = max(float32 tau, float32(gamma) * a_top
+    rounded to float32) for gamma > 0, else float32 tau), capped at k_max
+    when k_max > 0, and at least 1 when there is a candidate.  Returns order [B, L] int32, n [B] int32.
+    """
+    s32 = np.asarray(score, dtype=np.float32)
+    B, L = s32.shape
+    order = np.full((B, L), -1, dtype=np.int32)
+    n_out = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        cand = [j for j in range(L) if candidates is None or candidates[b][j]]
+        if not cand:
+            continue
+
+        def key(j):
+            v = float(s32[b, j])
+            return (1, 0.0, j) if math.isnan(v) else (0, -v, j)
+
+        ranked = sorted(cand, key=key)
+        order[b, :len(ranked)] = ranked
+        top = s32[b, ranked[0]]
+        thr = np.float32(tau)
+        if gamma > 0:
+            thr = max(thr, np.float32(np.float32(gamma) * top))
+        n = 0
+        while n < len(ranked) and s32[b, ranked[n]] >= thr:
+            n += 1
+        if k_max > 0:
+            n = min(n, k_max)
+        n_out[b] = max(n, 1)
+    return order, n_out
 
 
 # --------------------------------------------------------------------------

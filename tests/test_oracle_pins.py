@@ -525,3 +525,143 @@ def test_adaptive_prefix_nan_stops_and_fallback():
     score = np.array([[0.9, np.nan, 0.9, 0.9], [np.nan, 0.9, 0.9, 0.9]], dtype=np.float32)
     ln, tau = oracle.adaptive_prefix(score, [0, 0], 0.25, 1.0)
     assert ln.tolist() == [1, 1]
+
+
+# ---------------------------------------------------------------- approximate attention update
+
+def _attention_all_rows(q, k, v, scale=None):
+    B, L = q.shape[:2]
+    return oracle.partial_attention(q, k, v, [L] * B, scale=scale)
+
+
+def test_approx_update_golden(golden):
+    for case in golden["approx_attention"]:
+        q = np.array(case["q"])[None, None, None, :]           # [1, 1, 1, d]
+        k = np.array(case["k"])[None, :, None, :]              # [1, 2, 1, d]
+        v = np.array(case["v_prev"])[None, :, None, :]
+        o_prev, lse, _ = oracle.partial_attention(q, k, v, [1], scale=case["scale"])
+        # the query row is position 0; position 1 is salient
+        L = k.shape[1]
+        qa = np.zeros((1, L, 1, q.shape[-1])); qa[:, 0] = q[:, 0]
+        oa = np.zeros((1, L, 1, q.shape[-1])); oa[:, 0] = o_prev[:, 0]
+        la = np.zeros((1, 1, L)); la[:, :, 0] = lse[:, :, 0]
+        v_new = np.array(case["v_new_pos1"])[None, None, None, :]
+        o = oracle.approx_attention_update(oa, qa, la, k, v, v_new, [[1]], [1], [[0]], [1],
+                                           scale=case["scale"])
+        assert np.allclose(o[0, 0, 0], case["o_new"], atol=1e-14, rtol=0), (o[0, 0, 0], case)
+
+
+@pytest.mark.parametrize("scale", [None, 0.3])
+def test_approx_update_exact_when_only_values_change(scale):
+    """With queries and keys unchanged the attention weights do not change,
+    so the update of the non-salient path is exact: it must equal attention
+    recomputed over the updated value cache, for every stable row."""
+    B, L, H, d = 2, 13, 3, 8
+    q = RNG.standard_normal((B, L, H, d))
+    k = RNG.standard_normal((B, L, H, d))
+    v = RNG.standard_normal((B, L, H, d))
+    o_prev, lse, _ = _attention_all_rows(q, k, v, scale)
+    counts = [4, 1]
+    idx = np.full((B, L), -1)
+    idx[0, :4] = [1, 5, 6, 12]
+    idx[1, :1] = [0]
+    v_new = RNG.standard_normal((B, L, H, d))
+    stable = np.full((B, L), -1)
+    s_counts = []
+    for b in range(B):
+        rest = [j for j in range(L) if j not in set(idx[b, :counts[b]])]
+        stable[b, :len(rest)] = rest
+        s_counts.append(len(rest))
+    o = oracle.approx_attention_update(o_prev, q, lse, k, v, v_new, idx, counts, stable, s_counts,
+                                       scale=scale)
+    _, v_upd = oracle.kv_scatter(k, v, k, v_new, idx, counts)
+    o_exact, _, _ = _attention_all_rows(q, k, v_upd, scale)
+    for b in range(B):
+        rows = stable[b, :s_counts[b]]
+        assert np.max(np.abs(o[b, rows] - o_exact[b, rows])) < 1e-12
+        sal = idx[b, :counts[b]]
+        assert np.array_equal(o[b, sal], o_prev[b, sal])  # only stable rows change
+
+
+def test_approx_update_no_change_cases():
+    B, L, H, d = 1, 9, 2, 4
+    q, k, v = (RNG.standard_normal((B, L, H, d)) for _ in range(3))
+    o_prev, lse, _ = _attention_all_rows(q, k, v)
+    idx = np.array([[2, 7] + [-1] * 7])
+    stable = np.array([[0, 1, 3, 4, 5, 6, 8, -1, -1]])
+    v_same = np.zeros((B, L, H, d))
+    v_same[0, :2] = v[0, [2, 7]]
+    o = oracle.approx_attention_update(o_prev, q, lse, k, v, v_same, idx, [2], stable, [7])
+    assert np.max(np.abs(o - o_prev)) < 1e-15                       # dV = 0
+    o = oracle.approx_attention_update(o_prev, q, lse, k, v, v_same + 1, idx, [0], stable, [7])
+    assert np.array_equal(o, o_prev)                                 # no salient token
+    o = oracle.approx_attention_update(o_prev, q, lse, k, v, v_same + 1, idx, [2], stable, [0])
+    assert np.array_equal(o, o_prev)                                 # no stable row
+
+
+# ---------------------------------------------------------------- Attn-Sampler order
+
+def test_attn_sampler_golden(golden):
+    for case in golden["attn_sampler"]:
+        order, n = oracle.attn_sampler_select(np.array([case["score"]]),
+                                              np.array([case["candidates"]]), case["tau"],
+                                              case["gamma"], case["k_max"])
+        assert order[0].tolist() == case["order"] and int(n[0]) == case["n"], case
+
+
+def test_attn_scores_sum_heads_and_layers():
+    # the row-softmax probabilities of each active row add up to 1 per head,
+    # so the scores of a batch row add up to H * count
+    B, L, H, d = 2, 11, 3, 8
+    q, k, v = (RNG.standard_normal((B, L, H, d)) for _ in range(3))
+    _, _, colsum = oracle.partial_attention(q, k, v, [5, 11])
+    a = oracle.attn_scores(colsum)
+    assert a.shape == (B, L)
+    assert np.allclose(a.sum(axis=1), [H * 5, H * 11], atol=1e-12, rtol=0)
+    per_layer = np.stack([colsum, 2 * colsum], axis=1)           # [B, layers, H, L]
+    assert np.allclose(oracle.attn_scores(per_layer), 3 * a, atol=1e-12, rtol=0)
+
+
+def test_attn_sampler_order_matches_lexsort():
+    B, L = 4, 200
+    score = np.round(RNG.standard_normal((B, L)) * 4) / 4          # many ties
+    cand = RNG.random((B, L)) < 0.7
+    order, n = oracle.attn_sampler_select(score, cand, -np.inf, 0.0, 0)
+    for b in range(B):
+        pos = np.nonzero(cand[b])[0]
+        ref = pos[np.lexsort((pos, -score[b, pos].astype(np.float32)))]
+        assert np.array_equal(order[b, :len(pos)], ref)
+        assert np.all(order[b, len(pos):] == -1)
+        assert n[b] == len(pos)                                     # threshold -inf: all
+
+
+def test_attn_sampler_count_brute_force():
+    """n is the largest k <= cap such that the k leading entries reach the
+    threshold (at least 1); checked over all threshold, fraction and cap
+    settings of small random cases."""
+    for trial in range(200):
+        L = 1 + trial % 9
+        score = np.round(RNG.random((1, L)) * 8) / 8
+        cand = RNG.random((1, L)) < 0.8
+        for tau, gamma, k_max in itertools.product([0.0, 0.3, 0.9], [0.0, 0.5, 1.0], [0, 1, 3]):
+            order, n = oracle.attn_sampler_select(score, cand, tau, gamma, k_max)
+            o = [j for j in order[0] if j >= 0]
+            if not o:
+                assert n[0] == 0
+                continue
+            thr = np.float32(tau)
+            if gamma > 0:
+                thr = max(thr, np.float32(gamma) * np.float32(score[0, o[0]]))
+            best = 0
+            for kk in range(1, len(o) + 1):
+                if all(np.float32(score[0, j]) >= thr for j in o[:kk]) and (k_max <= 0 or kk <= k_max):
+                    best = kk
+            assert n[0] == max(best, 1)
+
+
+def test_attn_sampler_nan_and_signed_zero():
+    score = np.array([[np.nan, 0.0, -0.0, 1.0, -np.inf]])
+    order, n = oracle.attn_sampler_select(score, None, -1.0, 0.0, 0)
+    # 1.0, then the two zeros by position (-0 == +0), -inf, NaN last
+    assert order[0].tolist() == [3, 1, 2, 4, 0]
+    assert n[0] == 3
