@@ -364,6 +364,54 @@ dllm_status dllm_adaptive_prefix(const float* score, int B, int L,
                                  float* tau_out, int32_t* dev_status,
                                  void* stream);
 
+/*
+ * dllm_attn_scores -- total attention each position receives.
+ *
+ * Attn-Sampler, technical summary, Methodology 1 (decode in descending order
+ * of the column sums of the attention matrix) and the ablation on layers and
+ * heads (aggregate over all of them):
+ *   score[b, j] (+)= sum_h colsum[b, h, j], heads added in order 0 .. H-1.
+ *
+ *   colsum      [B, H, L] float32, contiguous (the column sums of
+ *               dllm_partial_attention or dllm_attention_colsum).
+ *   accumulate  nonzero: add onto score_inout (the sum over layers is one
+ *               call per layer); zero: overwrite it.
+ *   score_inout [B, L] float32, contiguous.
+ * Errors: INVALID_ARG (NULLs, sizes, B above 65535).  dev_status is unused
+ * (no device-side index is read) and may be NULL.
+ */
+dllm_status dllm_attn_scores(const float* colsum, int B, int H, int L,
+                             int accumulate, float* score_inout,
+                             int32_t* dev_status, void* stream);
+
+/*
+ * dllm_attn_sampler_select -- decoding order and the number of tokens to
+ * decode in parallel.
+ *
+ * Attn-Sampler, technical summary, Methodology 2: the tokens with the highest
+ * scores are decoded first, and in parallel only while their score exceeds a
+ * threshold.  The page does not give the dynamic threshold; here it is
+ * thr = max(tau, gamma * score of the top candidate) for gamma > 0 (product
+ * rounded to float32; a NaN top leaves tau), else tau.
+ *
+ *   score       [B, L] float32, contiguous (e.g. from dllm_attn_scores).
+ *   candidates  [B, L] uint8, nonzero where a position may be decoded (still
+ *               masked), or NULL for all positions.
+ *   k_max       cap on the count when > 0.
+ *   order_out   [B, L] int32: the candidates by descending score, equal scores
+ *               by ascending position (-0 equals +0, NaN last), then -1.
+ *   n_out       [B] int32: the number of leading entries of order_out whose
+ *               score is >= thr, capped at k_max, at least 1 when there is a
+ *               candidate, 0 when there is none.
+ * L at most 16384.  Errors: INVALID_ARG (NULLs, sizes, NaN tau or gamma).
+ * dev_status is unused and may be NULL.
+ */
+dllm_status dllm_attn_sampler_select(const float* score, int B, int L,
+                                     const uint8_t* candidates, float tau,
+                                     float gamma, int k_max,
+                                     int32_t* order_out, int32_t* n_out,
+                                     int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

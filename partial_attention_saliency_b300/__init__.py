@@ -13,6 +13,8 @@ from ._lib import (  # noqa: F401
     SIGNATURES,
     dllm_adaptive_prefix,
     dllm_attention_colsum,
+    dllm_attn_sampler_select,
+    dllm_attn_scores,
     dllm_attention_workspace_bytes,
     dllm_confidence,
     dllm_confidence_workspace_bytes,

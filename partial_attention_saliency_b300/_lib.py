@@ -48,6 +48,8 @@ SIGNATURES = {
     "dllm_lock_criterion": (_I, [_P, _P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _F, _F,
                                  _P, _P, _P, _P, _SZ, _P, _P]),
     "dllm_adaptive_prefix": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
+    "dllm_attn_scores": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
+    "dllm_attn_sampler_select": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
 }
 
 
@@ -357,3 +359,41 @@ def dllm_adaptive_prefix(score, start, lo: float, hi: float, *, advance_start: b
                                     int(advance_start), _ptr(len_out), _ptr(tau_out),
                                     _ptr(dev_status), _stream(stream)))
     return len_out, tau_out
+
+
+def dllm_attn_scores(colsum, *, score_inout=None, accumulate: bool = False, dev_status=None,
+                     stream=None):
+    """Sum over heads of the attention column sums ``colsum`` [B, H, L];
+    ``accumulate`` adds onto ``score_inout`` (layers).  Returns [B, L]."""
+    lib = load_library()
+    B, H, L = colsum.shape
+    _need(colsum, torch.float32, (B, H, L), "colsum")
+    if score_inout is None:
+        if accumulate:
+            raise ValueError("accumulate needs score_inout")
+        score_inout = torch.empty((B, L), dtype=torch.float32, device=colsum.device)
+    _need(score_inout, torch.float32, (B, L), "score_inout")
+    _check(lib.dllm_attn_scores(_ptr(colsum), B, H, L, int(accumulate), _ptr(score_inout),
+                                _ptr(dev_status), _stream(stream)))
+    return score_inout
+
+
+def dllm_attn_sampler_select(score, *, candidates=None, tau: float = 0.0, gamma: float = 0.0,
+                             k_max: int = 0, order_out=None, n_out=None, dev_status=None,
+                             stream=None):
+    """Candidates by descending score and how many of them to decode.
+    Returns (order [B, L] int32, n [B] int32)."""
+    lib = load_library()
+    B, L = score.shape
+    _need(score, torch.float32, (B, L), "score")
+    if candidates is not None:
+        _need(candidates, torch.uint8, (B, L), "candidates")
+    dev = score.device
+    order_out = torch.empty((B, L), dtype=torch.int32, device=dev) if order_out is None else order_out
+    n_out = torch.empty((B,), dtype=torch.int32, device=dev) if n_out is None else n_out
+    _need(order_out, torch.int32, (B, L), "order_out")
+    _need(n_out, torch.int32, (B,), "n_out")
+    _check(lib.dllm_attn_sampler_select(_ptr(score), B, L, _ptr(candidates), float(tau),
+                                        float(gamma), int(k_max), _ptr(order_out), _ptr(n_out),
+                                        _ptr(dev_status), _stream(stream)))
+    return order_out, n_out

@@ -281,6 +281,34 @@ dllm_status dllm_adaptive_prefix(const float* score, int B, int L, int32_t* star
                    "dllm_adaptive_prefix launch");
 }
 
+dllm_status dllm_attn_scores(const float* colsum, int B, int H, int L, int accumulate,
+                             float* score_inout, int32_t* dev_status, void* stream) {
+  (void)dev_status;  // nothing is read through device-side indices
+  REQUIRE(colsum && score_inout, "dllm_attn_scores: NULL pointer argument");
+  REQUIRE(B >= 1 && H >= 1 && L >= 1, "dllm_attn_scores: B=%d H=%d L=%d must be >= 1", B, H, L);
+  REQUIRE(B <= 65535, "dllm_attn_scores: B=%d above 65535", B);
+  return from_cuda(dllm::launch_attn_scores(colsum, B, H, L, accumulate, score_inout,
+                                            static_cast<cudaStream_t>(stream)),
+                   "dllm_attn_scores launch");
+}
+
+dllm_status dllm_attn_sampler_select(const float* score, int B, int L,
+                                     const uint8_t* candidates, float tau, float gamma,
+                                     int k_max, int32_t* order_out, int32_t* n_out,
+                                     int32_t* dev_status, void* stream) {
+  (void)dev_status;  // nothing is read through device-side indices
+  REQUIRE(score && order_out && n_out, "dllm_attn_sampler_select: NULL pointer argument");
+  REQUIRE(B >= 1 && L >= 1, "dllm_attn_sampler_select: B=%d L=%d must be >= 1", B, L);
+  REQUIRE(L <= dllm::attn_sampler_max_len(), "dllm_attn_sampler_select: L=%d above %d", L,
+          dllm::attn_sampler_max_len());
+  REQUIRE(!std::isnan(tau) && !std::isnan(gamma),
+          "dllm_attn_sampler_select: NaN threshold or fraction");
+  return from_cuda(dllm::launch_attn_sampler_select(score, B, L, candidates, tau, gamma, k_max,
+                                                    order_out, n_out,
+                                                    static_cast<cudaStream_t>(stream)),
+                   "dllm_attn_sampler_select launch");
+}
+
 }  // extern "C"
 
 namespace dllm {

@@ -71,6 +71,16 @@ cudaError_t launch_adaptive_prefix(const float* score, int B, int L, int32_t* st
                                    float hi, int advance_start, int32_t* len_out, float* tau_out,
                                    int32_t* dev_status, cudaStream_t stream);
 
+cudaError_t launch_attn_scores(const float* colsum, int B, int H, int L, int accumulate,
+                               float* score, cudaStream_t stream);
+
+int attn_sampler_max_len();
+
+cudaError_t launch_attn_sampler_select(const float* score, int B, int L,
+                                       const uint8_t* candidates, float tau, float gamma,
+                                       int k_max, int32_t* order, int32_t* n_out,
+                                       cudaStream_t stream);
+
 int num_sms();
 
 // Raises the dynamic shared-memory limit of `func` to `bytes` on the current
