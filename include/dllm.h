@@ -412,6 +412,48 @@ dllm_status dllm_attn_sampler_select(const float* score, int B, int L,
                                      int32_t* order_out, int32_t* n_out,
                                      int32_t* dev_status, void* stream);
 
+/*
+ * dllm_approx_attention_update -- output update of the stable rows from the
+ * value changes of the salient rows.
+ *
+ * DyLLM, technical summary, Methodology 2 (non-salient path): a stable row
+ * keeps its attention weights, and its output moves by the change of the
+ * salient tokens' values weighted by them; cost O(N |A|).  The weights are
+ * the previous step's, recovered from the cached query, the previous keys of
+ * the salient positions and the cached log-sum-exp:
+ *   o[i] += sum_{a < count} exp(scale q[i].k[idx_a] - lse[i]) (v_new[a] - v[idx_a])
+ * for every stable position i = stable_idx[r], r < stable_count.
+ *
+ *   q_prev, k_prev, v_prev  [B, L, H, d] of `dtype`, contiguous: the previous
+ *               step's queries, keys and values of every position (k_prev
+ *               and v_prev before this step's dllm_kv_scatter).
+ *   lse_prev    [B, H, L] float32: the previous step's log-sum-exp of every
+ *               position's score row.
+ *   v_new       [B, M_max, H, d]: row a is the fresh value of position
+ *               idx[b, a], a < count[b] (the layout of dllm_kv_scatter).
+ *   idx, count  [B, M_max], [B] int32: the salient positions.
+ *   stable_idx, stable_count  [B, N_max], [B] int32: distinct positions
+ *               whose outputs are updated.
+ *   scale       <= 0 selects 1/sqrt(d).
+ *   o_inout     [B, L, H, d] of `dtype`: outputs by position, updated in
+ *               place on the stable rows only (float32 arithmetic, rounded to
+ *               the dtype once).
+ * d in {32, 64, 128}.  Errors: INVALID_ARG, UNSUPPORTED (head dim);
+ * dev_status gets DEVICE_CHECK for counts or positions out of range (the
+ * row or column is skipped).
+ */
+dllm_status dllm_approx_attention_update(const void* q_prev,
+                                         const float* lse_prev,
+                                         const void* k_prev, const void* v_prev,
+                                         const void* v_new, int dtype, int B,
+                                         int L, int H, int d, int M_max,
+                                         const int32_t* idx,
+                                         const int32_t* count, int N_max,
+                                         const int32_t* stable_idx,
+                                         const int32_t* stable_count,
+                                         float scale, void* o_inout,
+                                         int32_t* dev_status, void* stream);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

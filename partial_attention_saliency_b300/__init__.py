@@ -12,6 +12,7 @@ from ._lib import (  # noqa: F401
     LIB_PATH,
     SIGNATURES,
     dllm_adaptive_prefix,
+    dllm_approx_attention_update,
     dllm_attention_colsum,
     dllm_attn_sampler_select,
     dllm_attn_scores,

@@ -50,6 +50,8 @@ SIGNATURES = {
     "dllm_adaptive_prefix": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
     "dllm_attn_scores": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dllm_attn_sampler_select": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
+    "dllm_approx_attention_update": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
+                                          _I, _P, _P, _F, _P, _P, _P]),
 }
 
 
@@ -397,3 +399,29 @@ def dllm_attn_sampler_select(score, *, candidates=None, tau: float = 0.0, gamma:
                                         float(gamma), int(k_max), _ptr(order_out), _ptr(n_out),
                                         _ptr(dev_status), _stream(stream)))
     return order_out, n_out
+
+
+def dllm_approx_attention_update(q_prev, lse_prev, k_prev, v_prev, v_new, idx, count, stable_idx,
+                                 stable_count, o_inout, *, scale: float = 0.0, dev_status=None,
+                                 stream=None):
+    """Update the outputs ``o_inout`` [B, L, H, d] of the stable rows in place
+    from the value changes of the salient rows.  Returns ``o_inout``."""
+    lib = load_library()
+    dt = _dtype(q_prev, k_prev, v_prev, v_new, o_inout)
+    B, L, H, d = q_prev.shape
+    M_max = v_new.shape[1]
+    N_max = stable_idx.shape[1]
+    for t, n in ((q_prev, "q_prev"), (k_prev, "k_prev"), (v_prev, "v_prev"), (o_inout, "o_inout")):
+        _need(t, q_prev.dtype, (B, L, H, d), n)
+    _need(v_new, q_prev.dtype, (B, M_max, H, d), "v_new")
+    _need(lse_prev, torch.float32, (B, H, L), "lse_prev")
+    _need(idx, torch.int32, (B, M_max), "idx")
+    _need(count, torch.int32, (B,), "count")
+    _need(stable_idx, torch.int32, (B, N_max), "stable_idx")
+    _need(stable_count, torch.int32, (B,), "stable_count")
+    _check(lib.dllm_approx_attention_update(_ptr(q_prev), _ptr(lse_prev), _ptr(k_prev),
+                                            _ptr(v_prev), _ptr(v_new), dt, B, L, H, d, M_max,
+                                            _ptr(idx), _ptr(count), N_max, _ptr(stable_idx),
+                                            _ptr(stable_count), float(scale), _ptr(o_inout),
+                                            _ptr(dev_status), _stream(stream)))
+    return o_inout

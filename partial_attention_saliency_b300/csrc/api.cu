@@ -309,6 +309,33 @@ dllm_status dllm_attn_sampler_select(const float* score, int B, int L,
                    "dllm_attn_sampler_select launch");
 }
 
+dllm_status dllm_approx_attention_update(const void* q_prev, const float* lse_prev,
+                                         const void* k_prev, const void* v_prev,
+                                         const void* v_new, int dtype, int B, int L, int H, int d,
+                                         int M_max, const int32_t* idx, const int32_t* count,
+                                         int N_max, const int32_t* stable_idx,
+                                         const int32_t* stable_count, float scale, void* o_inout,
+                                         int32_t* dev_status, void* stream) {
+  REQUIRE(q_prev && lse_prev && k_prev && v_prev && v_new && idx && count && stable_idx &&
+              stable_count && o_inout,
+          "dllm_approx_attention_update: NULL pointer argument");
+  REQUIRE(valid_dtype(dtype), "dllm_approx_attention_update: unknown dtype %d", dtype);
+  REQUIRE(B >= 1 && L >= 1 && H >= 1 && M_max >= 1 && N_max >= 1,
+          "dllm_approx_attention_update: B=%d L=%d H=%d M_max=%d N_max=%d must be >= 1", B, L, H,
+          M_max, N_max);
+  REQUIRE(B <= 65535 && H <= 65535, "dllm_approx_attention_update: B=%d or H=%d above 65535", B,
+          H);
+  if (d != 32 && d != 64 && d != 128)
+    return fail(DLLM_ERR_UNSUPPORTED, "dllm_approx_attention_update: head dim %d not in {32, 64, 128}",
+                d);
+  if (!(scale > 0.0f)) scale = 1.0f / std::sqrt((float)d);
+  return from_cuda(dllm::launch_approx_attention_update(
+                       q_prev, lse_prev, k_prev, v_prev, v_new, dtype, B, L, H, d, M_max, idx,
+                       count, N_max, stable_idx, stable_count, scale, o_inout, dev_status,
+                       static_cast<cudaStream_t>(stream)),
+                   "dllm_approx_attention_update launch");
+}
+
 }  // extern "C"
 
 namespace dllm {

@@ -81,6 +81,14 @@ cudaError_t launch_attn_sampler_select(const float* score, int B, int L,
                                        int k_max, int32_t* order, int32_t* n_out,
                                        cudaStream_t stream);
 
+cudaError_t launch_approx_attention_update(const void* q, const float* lse, const void* k,
+                                           const void* v, const void* v_new, int dtype, int B,
+                                           int L, int H, int d, int M_max, const int32_t* idx,
+                                           const int32_t* count, int N_max,
+                                           const int32_t* stable_idx,
+                                           const int32_t* stable_count, float scale, void* o,
+                                           int32_t* dev_status, cudaStream_t stream);
+
 int num_sms();
 
 // Raises the dynamic shared-memory limit of `func` to `bytes` on the current

@@ -121,6 +121,24 @@ def test_lock_and_adaptive_prefix_rejected_before_launch(lib):
     assert st == 1
 
 
+def test_sampler_and_stable_row_update_rejected_before_launch(lib):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    assert lib.dllm_attn_scores(None, 1, 32, 16, 0, p, None, None) == 1
+    assert lib.dllm_attn_scores(p, 1, 0, 16, 0, p, None, None) == 1
+    st = lib.dllm_attn_sampler_select(p, 1, 16385, None, 0.0, 0.0, 0, p, p, None, None)
+    assert st == 1 and b"16384" in lib.dllm_last_error()
+    st = lib.dllm_attn_sampler_select(p, 1, 16, None, float("nan"), 0.0, 0, p, p, None, None)
+    assert st == 1 and b"NaN" in lib.dllm_last_error()
+
+    def upd(d=128, o=p, B=1):
+        return lib.dllm_approx_attention_update(p, p, p, p, p, 1, B, 64, 2, d, 8, p, p, 8, p, p,
+                                                0.0, o, None, None)
+
+    assert upd(o=None) == 1 and b"NULL" in lib.dllm_last_error()
+    assert upd(d=48) == 2 and b"head dim" in lib.dllm_last_error()
+    assert upd(B=0) == 1
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from partial_attention_saliency_b300 import _lib
     with pytest.raises(ImportError):
