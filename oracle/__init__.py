@@ -24,5 +24,6 @@ from .dllm_oracle import (  # noqa: F401
     approx_attention_update,
     attn_scores,
     attn_sampler_select,
+    slowfast_phases,
     step,
 )

@@ -52,6 +52,7 @@ __all__ = [
     "approx_attention_update",
     "attn_scores",
     "attn_sampler_select",
+    "slowfast_phases",
     "step",
 ]
 
@@ -506,6 +507,47 @@ def attn_sampler_select(score, candidates, tau: float, gamma: float, k_max: int)
             n = min(n, k_max)
         n_out[b] = max(n, 1)
     return order, n_out
+
+
+# --------------------------------------------------------------------------
+# SlowFast phase control
+# --------------------------------------------------------------------------
+
+def slowfast_phases(starts, e_cands, window: int, sigma2: float):
+    """Phase and region of each step of SlowFast sampling.
+
+    SlowFast, section 2 (pipeline): in the slow (exploratory) phase the
+    prediction of the convergence point e_cand is watched over a sliding
+    window of steps; when the variance of the prediction falls below
+    sigma^2_stable the region [s_cycle, e_cycle] is stable and the fast phase
+    decodes it in one step; then a new cycle starts.  Reading: one cycle
+    starts empty; each step appends that step's e_cand; with the last
+    ``window`` predictions x_1 .. x_W of the cycle, the region is stable iff
+    their population variance is below sigma2 (evaluated exactly as
+    W sum x^2 - (sum x)^2 < sigma2 W^2, the right side in float64) and the
+    latest prediction lies beyond the start; that step is fast with region
+    [start, latest e_cand), and the next step begins a new cycle.
+
+    starts, e_cands: [T, B] integers (start of the undecoded suffix and the
+    prediction at each step).  Returns phase [T, B] (0 slow, 1 fast) and
+    region end [T, B] (the region's end on fast steps, -1 otherwise).
+    """
+    T, B = len(starts), len(starts[0])
+    phase = np.zeros((T, B), dtype=np.int32)
+    end = np.full((T, B), -1, dtype=np.int32)
+    for b in range(B):
+        hist = []
+        for t in range(T):
+            hist.append(int(e_cands[t][b]))
+            if len(hist) > window:
+                hist.pop(0)
+            if len(hist) == window and hist[-1] > int(starts[t][b]):
+                num = window * sum(x * x for x in hist) - sum(hist) ** 2
+                if num < float(sigma2) * (window * window):
+                    phase[t, b] = 1
+                    end[t, b] = hist[-1]
+                    hist = []
+    return phase, end
 
 
 # --------------------------------------------------------------------------

@@ -665,3 +665,48 @@ def test_attn_sampler_nan_and_signed_zero():
     # 1.0, then the two zeros by position (-0 == +0), -inf, NaN last
     assert order[0].tolist() == [3, 1, 2, 4, 0]
     assert n[0] == 3
+
+
+# ---------------------------------------------------------------- SlowFast phases
+
+def test_slowfast_golden(golden):
+    for case in golden["slowfast"]:
+        starts = [[s] for s in case["start"]]
+        preds = [[e] for e in case["e_cand"]]
+        phase, end = oracle.slowfast_phases(starts, preds, case["window"], case["sigma2"])
+        assert phase[:, 0].tolist() == case["phase"], case
+        assert end[:, 0].tolist() == case["region_end"], case
+
+
+def test_slowfast_matches_numpy_variance():
+    """Away from exact ties the integer form is numpy's population variance
+    of the window below sigma2; a cycle restarts after each fast step."""
+    for trial in range(40):
+        W = 1 + trial % 5
+        sigma2 = [0.3, 1.7, 4.9, 0.0][trial % 4] + 1e-7  # never a multiple of 1 / W^2
+        T = 60
+        e = np.cumsum(RNG.integers(0, 3, T)) + RNG.integers(0, 2, T)
+        starts = np.minimum(e - RNG.integers(0, 4, T), e).astype(int)
+        phase, end = oracle.slowfast_phases(starts[:, None], e[:, None], W, sigma2)
+        hist = []
+        for t in range(T):
+            hist = (hist + [int(e[t])])[-W:]
+            fast = len(hist) == W and hist[-1] > starts[t] and np.var(hist) < sigma2
+            assert phase[t, 0] == int(fast) and end[t, 0] == (hist[-1] if fast else -1)
+            if fast:
+                hist = []
+
+
+def test_slowfast_special_cases():
+    # a prediction that never moves past the start never decodes fast
+    ph, _ = oracle.slowfast_phases([[5]] * 10, [[5]] * 10, 3, 100.0)
+    assert ph.sum() == 0
+    # sigma2 = 0: the variance is never below it
+    ph, _ = oracle.slowfast_phases([[0]] * 10, [[7]] * 10, 2, 0.0)
+    assert ph.sum() == 0
+    # a constant prediction beyond the start: fast every W steps
+    ph, end = oracle.slowfast_phases([[0]] * 12, [[7]] * 12, 3, 0.1)
+    assert ph[:, 0].tolist() == [0, 0, 1] * 4 and set(end[ph[:, 0] == 1, 0]) == {7}
+    # window 1: fast whenever the prediction lies beyond the start
+    ph, _ = oracle.slowfast_phases([[0], [3], [3]], [[2], [3], [9]], 1, 0.5)
+    assert ph[:, 0].tolist() == [1, 0, 1]
