@@ -454,6 +454,41 @@ dllm_status dllm_approx_attention_update(const void* q_prev,
                                          float scale, void* o_inout,
                                          int32_t* dev_status, void* stream);
 
+/*
+ * SlowFast phase control (host side).
+ *
+ * SlowFast, section 2 (pipeline): the slow phase watches the prediction of
+ * the convergence point e_cand over a sliding window of steps; once its
+ * variance falls below sigma^2_stable the region [s_cycle, e_cycle] is
+ * stable and the fast phase decodes it (every masked token of the region
+ * above the high confidence threshold at once); then a new cycle begins.
+ *
+ * The controller keeps, per batch row, the predictions of the current cycle
+ * (at most `window`).  dllm_slowfast_observe appends this step's prediction;
+ * the step is fast iff the window is full, the latest prediction lies beyond
+ * start[b], and W sum x^2 - (sum x)^2 < sigma2 W^2 (the population variance
+ * below sigma2, left side exact in 64-bit integers, right side in double).
+ * A fast step reports phase 1 and region [start[b], e_cand[b]) and empties
+ * the window; otherwise phase 0 and region end -1.
+ *
+ * All pointers of these three calls are HOST memory: start, e_cand,
+ * phase_out, region_end_out are [B] int32 arrays.  e_cand is typically
+ * start + the stable-prefix length of the confidence scores from start
+ * (dllm_stable_prefix with the confidence threshold), read back by the
+ * caller.  A handle is not thread-safe; create returns INVALID_ARG for
+ * B < 1, window < 1 or sigma2 < 0 (or NaN).
+ */
+typedef struct dllm_slowfast dllm_slowfast;
+
+dllm_status dllm_slowfast_create(int B, int window, double sigma2_stable,
+                                 dllm_slowfast** out);
+
+dllm_status dllm_slowfast_observe(dllm_slowfast* sf, const int32_t* start,
+                                  const int32_t* e_cand, int32_t* phase_out,
+                                  int32_t* region_end_out);
+
+void dllm_slowfast_destroy(dllm_slowfast* sf);
+
 #ifdef __cplusplus
 }  /* extern "C" */
 #endif

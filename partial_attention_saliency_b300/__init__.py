@@ -2,7 +2,9 @@
 
 One step recomputes only a selected subset of token positions: cosine saliency
 selection, KV-cache scatter, partial attention with column sums, confidence /
-argmax / margin, and the longest stable prefix.  Every operation runs in the
+argmax / margin, and the longest stable prefix; around it the lock criterion
+between steps, the adaptive prefix threshold, the stable rows' output update,
+the attention-guided decoding order and the slow/fast phase controller.  Every operation runs in the
 hand-written sm_103a kernels of ``libdllm.so`` behind a C ABI
 (``include/dllm.h``); the functions below are its ctypes binding, with the
 same names.  PyTorch provides device memory and streams only.
@@ -11,6 +13,7 @@ from ._lib import (  # noqa: F401
     DllmError,
     LIB_PATH,
     SIGNATURES,
+    SlowFast,
     dllm_adaptive_prefix,
     dllm_approx_attention_update,
     dllm_attention_colsum,

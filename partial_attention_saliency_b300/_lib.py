@@ -52,6 +52,9 @@ SIGNATURES = {
     "dllm_attn_sampler_select": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
     "dllm_approx_attention_update": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                                           _I, _P, _P, _F, _P, _P, _P]),
+    "dllm_slowfast_create": (_I, [_I, _I, ctypes.c_double, ctypes.POINTER(_P)]),
+    "dllm_slowfast_observe": (_I, [_P, _P, _P, _P, _P]),
+    "dllm_slowfast_destroy": (None, [_P]),
 }
 
 
@@ -425,3 +428,42 @@ def dllm_approx_attention_update(q_prev, lse_prev, k_prev, v_prev, v_new, idx, c
                                             _ptr(stable_count), float(scale), _ptr(o_inout),
                                             _ptr(dev_status), _stream(stream)))
     return o_inout
+
+
+class SlowFast:
+    """Host-side SlowFast phase controller (``dllm_slowfast_*``).
+
+    ``observe(start, e_cand)`` takes [B] int32 host arrays (numpy or CPU
+    tensors) of this step and returns (phase [B], region_end [B]) as int32
+    numpy arrays: phase 1 with the region [start, region_end) on a fast step.
+    """
+
+    def __init__(self, B: int, window: int, sigma2_stable: float):
+        import numpy as np
+        self._np = np
+        self._lib = load_library()
+        self.B = int(B)
+        h = _P()
+        _check(self._lib.dllm_slowfast_create(self.B, int(window), float(sigma2_stable),
+                                              ctypes.byref(h)))
+        self._h = h
+
+    def observe(self, start, e_cand):
+        np = self._np
+        s = np.ascontiguousarray(np.asarray(start, dtype=np.int32))
+        e = np.ascontiguousarray(np.asarray(e_cand, dtype=np.int32))
+        if s.shape != (self.B,) or e.shape != (self.B,):
+            raise ValueError(f"start and e_cand must be [{self.B}]")
+        phase = np.zeros(self.B, dtype=np.int32)
+        end = np.zeros(self.B, dtype=np.int32)
+        _check(self._lib.dllm_slowfast_observe(self._h, s.ctypes.data, e.ctypes.data,
+                                               phase.ctypes.data, end.ctypes.data))
+        return phase, end
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            self._lib.dllm_slowfast_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        self.close()
