@@ -25,5 +25,6 @@ from .dllm_oracle import (  # noqa: F401
     attn_scores,
     attn_sampler_select,
     slowfast_phases,
+    snap_prefix,
     step,
 )

@@ -53,6 +53,7 @@ __all__ = [
     "attn_scores",
     "attn_sampler_select",
     "slowfast_phases",
+    "snap_prefix",
     "step",
 ]
 
@@ -507,6 +508,37 @@ def attn_sampler_select(score, candidates, tau: float, gamma: float, k_max: int)
             n = min(n, k_max)
         n_out[b] = max(n, 1)
     return order, n_out
+
+
+# --------------------------------------------------------------------------
+# Structural snapping of the committed block
+# --------------------------------------------------------------------------
+
+def snap_prefix(tokens, delim, start, length, min_len: int):
+    """Length of the committed block after structural snapping.
+
+    LSP, technical summary section 2, step 3 (structural snapping): the end
+    of the selected block is moved to the nearest natural boundary
+    (punctuation, newline, code symbol) inside the candidate block, so that
+    no word or sentence is frozen half way.  Reading: the tokenizer's
+    delimiter set is given as a flag per vocabulary id; the block
+    [start, start + length) ends after its last delimiter token at a position
+    p >= start + max(min_len, 1) - 1, i.e. the new length is p - start + 1;
+    with no such delimiter the length is unchanged.
+
+    tokens [B, L] (e.g. the argmax of each position), delim [V], start and
+    length [B].  Returns the snapped lengths [B] int32.
+    """
+    tok = np.asarray(tokens)
+    out = np.array(length, dtype=np.int32, copy=True)
+    for b in range(tok.shape[0]):
+        s, n = int(start[b]), int(length[b])
+        lo = s + max(int(min_len), 1) - 1
+        for p in range(s + n - 1, lo - 1, -1):
+            if delim[int(tok[b, p])]:
+                out[b] = p - s + 1
+                break
+    return out
 
 
 # --------------------------------------------------------------------------

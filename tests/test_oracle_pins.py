@@ -710,3 +710,36 @@ def test_slowfast_special_cases():
     # window 1: fast whenever the prediction lies beyond the start
     ph, _ = oracle.slowfast_phases([[0], [3], [3]], [[2], [3], [9]], 1, 0.5)
     assert ph[:, 0].tolist() == [1, 0, 1]
+
+
+# ---------------------------------------------------------------- structural snapping
+
+def test_snap_prefix_golden(golden):
+    for case in golden["snap_prefix"]:
+        V = 1 + max(max(case["tokens"]), max(case["delim_ids"]))
+        delim = np.zeros(V, dtype=np.uint8)
+        delim[case["delim_ids"]] = 1
+        got = oracle.snap_prefix(np.array([case["tokens"]]), delim, [case["start"]],
+                                 [case["length"]], case["min_len"])
+        assert int(got[0]) == case["snapped"], case
+
+
+def test_snap_prefix_characterisation():
+    """The snapped block ends on a delimiter at or after the minimum and no
+    delimiter lies between its end and the original end; without such a
+    delimiter the length is unchanged; it never grows."""
+    for trial in range(300):
+        L, V = 1 + trial % 23, 6
+        tok = RNG.integers(0, V, (1, L))
+        delim = (RNG.random(V) < 0.3).astype(np.uint8)
+        s = int(RNG.integers(0, L))
+        n = int(RNG.integers(0, L - s + 1))
+        m = int(RNG.integers(0, n + 2))
+        got = int(oracle.snap_prefix(tok, delim, [s], [n], m)[0])
+        lo = s + max(m, 1) - 1
+        ends = [p for p in range(lo, s + n) if delim[tok[0, p]]]
+        if ends:
+            assert got == max(ends) - s + 1 and delim[tok[0, s + got - 1]]
+        else:
+            assert got == n
+        assert got <= n
