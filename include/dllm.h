@@ -455,6 +455,32 @@ dllm_status dllm_approx_attention_update(const void* q_prev,
                                          int32_t* dev_status, void* stream);
 
 /*
+ * dllm_snap_prefix -- structural snapping of the committed block.
+ *
+ * LSP, technical summary section 2, step 3: the end of the selected block
+ * moves to the nearest natural boundary (punctuation, newline, code symbol)
+ * inside the candidate block.  The block [start[b], start[b] + len[b]) ends
+ * after its last boundary token at a position >= start + max(min_len, 1) - 1:
+ * len becomes that position - start + 1; with no such token len is kept.
+ *
+ *   tokens      [B, L] int32, contiguous: the token at each position (e.g.
+ *               argmax_out of dllm_confidence).
+ *   delim       [V] uint8: nonzero for the vocabulary ids that are
+ *               boundaries (the tokenizer's punctuation, newline, code
+ *               symbols; supplied by the caller).
+ *   start       [B] int32; len_inout [B] int32 (e.g. from
+ *               dllm_adaptive_prefix), updated in place.
+ *   min_len     the shortest block snapping may leave (e.g. the lower end of
+ *               the adaptive range).
+ * Errors: INVALID_ARG; dev_status gets DEVICE_CHECK for a block outside
+ * [0, L] (left as it is) or a token outside [0, V) (not a boundary).
+ */
+dllm_status dllm_snap_prefix(const int32_t* tokens, int B, int L, int V,
+                             const uint8_t* delim, const int32_t* start,
+                             int32_t* len_inout, int min_len,
+                             int32_t* dev_status, void* stream);
+
+/*
  * SlowFast phase control (host side).
  *
  * SlowFast, section 2 (pipeline): the slow phase watches the prediction of

@@ -27,6 +27,7 @@ from ._lib import (  # noqa: F401
     dllm_lock_workspace_bytes,
     dllm_partial_attention,
     dllm_saliency_select,
+    dllm_snap_prefix,
     dllm_stable_prefix,
     dllm_version,
     load_library,

@@ -52,6 +52,7 @@ SIGNATURES = {
     "dllm_attn_sampler_select": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
     "dllm_approx_attention_update": (_I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P,
                                           _I, _P, _P, _F, _P, _P, _P]),
+    "dllm_snap_prefix": (_I, [_P, _I, _I, _I, _P, _P, _P, _I, _P, _P]),
     "dllm_slowfast_create": (_I, [_I, _I, ctypes.c_double, ctypes.POINTER(_P)]),
     "dllm_slowfast_observe": (_I, [_P, _P, _P, _P, _P]),
     "dllm_slowfast_destroy": (None, [_P]),
@@ -428,6 +429,23 @@ def dllm_approx_attention_update(q_prev, lse_prev, k_prev, v_prev, v_new, idx, c
                                             _ptr(stable_count), float(scale), _ptr(o_inout),
                                             _ptr(dev_status), _stream(stream)))
     return o_inout
+
+
+def dllm_snap_prefix(tokens, delim, start, len_inout, *, min_len: int = 1, dev_status=None,
+                     stream=None):
+    """Snap the committed blocks [start, start + len) to their last boundary
+    token (``delim`` [V] uint8 flags); ``len_inout`` [B] is updated in place
+    and returned."""
+    lib = load_library()
+    B, L = tokens.shape
+    V = delim.shape[0]
+    _need(tokens, torch.int32, (B, L), "tokens")
+    _need(delim, torch.uint8, (V,), "delim")
+    _need(start, torch.int32, (B,), "start")
+    _need(len_inout, torch.int32, (B,), "len_inout")
+    _check(lib.dllm_snap_prefix(_ptr(tokens), B, L, V, _ptr(delim), _ptr(start), _ptr(len_inout),
+                                int(min_len), _ptr(dev_status), _stream(stream)))
+    return len_inout
 
 
 class SlowFast:

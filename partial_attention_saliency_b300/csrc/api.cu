@@ -336,6 +336,16 @@ dllm_status dllm_approx_attention_update(const void* q_prev, const float* lse_pr
                    "dllm_approx_attention_update launch");
 }
 
+dllm_status dllm_snap_prefix(const int32_t* tokens, int B, int L, int V, const uint8_t* delim,
+                             const int32_t* start, int32_t* len_inout, int min_len,
+                             int32_t* dev_status, void* stream) {
+  REQUIRE(tokens && delim && start && len_inout, "dllm_snap_prefix: NULL pointer argument");
+  REQUIRE(B >= 1 && L >= 1 && V >= 1, "dllm_snap_prefix: B=%d L=%d V=%d must be >= 1", B, L, V);
+  return from_cuda(dllm::launch_snap_prefix(tokens, B, L, V, delim, start, len_inout, min_len,
+                                            dev_status, static_cast<cudaStream_t>(stream)),
+                   "dllm_snap_prefix launch");
+}
+
 }  // extern "C"
 
 namespace dllm {

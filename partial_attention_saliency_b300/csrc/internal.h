@@ -89,6 +89,10 @@ cudaError_t launch_approx_attention_update(const void* q, const float* lse, cons
                                            const int32_t* stable_count, float scale, void* o,
                                            int32_t* dev_status, cudaStream_t stream);
 
+cudaError_t launch_snap_prefix(const int32_t* tokens, int B, int L, int V, const uint8_t* delim,
+                               const int32_t* start, int32_t* len, int min_len,
+                               int32_t* dev_status, cudaStream_t stream);
+
 int num_sms();
 
 // Raises the dynamic shared-memory limit of `func` to `bytes` on the current
