@@ -3,14 +3,26 @@
  * models (one step that recomputes only a selected subset of token positions).
  *
  * The library (libdllm.so) runs every entry point as CUDA kernels for sm_103a
- * (B300) on the caller's stream.  It never allocates device memory, never
- * synchronises the stream and never reads device data back to the host: the
- * active-row counts stay on the device, so a whole step can be captured in a
- * CUDA graph.
+ * (B300) on the caller's stream (the SlowFast controller is plain host code).
+ * It never allocates device memory, never synchronises the stream and never
+ * reads device data back to the host: the active-row counts stay on the
+ * device, so a whole step can be captured in a CUDA graph.
+ *
+ * Entry points
+ *   The step, in order: dllm_saliency_select, dllm_kv_scatter,
+ *   dllm_partial_attention (with or without column sums; the sums alone:
+ *   dllm_attention_colsum), dllm_confidence (dllm_confidence_static_ws for
+ *   callers that cannot allocate), dllm_stable_prefix.
+ *   Around it: dllm_lock_criterion (SureLock), dllm_adaptive_prefix and
+ *   dllm_snap_prefix (LSP), dllm_approx_attention_update (DyLLM's stable
+ *   rows), dllm_attn_scores and dllm_attn_sampler_select (Attn-Sampler), and
+ *   the host-side SlowFast controller dllm_slowfast_create / _observe /
+ *   _destroy.
  *
  * Common conventions
- *   - Every data pointer is a DEVICE pointer owned by the caller.  Inputs are
- *     read only; outputs are written only where stated.
+ *   - Every data pointer is a DEVICE pointer owned by the caller (the SlowFast
+ *     controller's arrays excepted: host memory).  Inputs are read only;
+ *     outputs are written only where stated.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
  *   - Element types: DLLM_F32 (IEEE float32) or DLLM_BF16 (bfloat16).  Scores,
  *     log-sum-exps and column sums are always float32; indices int32.
