@@ -28,7 +28,15 @@ maximum of a temperature-1 softmax; argmax ties go to the lowest vocabulary
 index and then the margin is 0; attention is unmasked (bidirectional) with
 scale 1/sqrt(d); column sums add the row-normalised probabilities of the
 active query rows only; a prefix position is stable iff score >= tau, NaN is
-unstable.
+unstable.  Around the step: the lock criterion's percentile is taken over the
+active rows of a batch row; the adaptive prefix threshold is the prefix
+minimum at the lower end of the fraction range; the stable rows' existing
+attention weights are the previous step's, recovered from the cached query,
+keys and log-sum-exp; the decoding order's dynamic threshold is
+max(tau, gamma * top score); structural boundaries are caller-given flags per
+vocabulary id; the SlowFast convergence point is tracked by the exact
+population variance of a window of predictions.  Each function's docstring
+states its reading in full.
 """
 from __future__ import annotations
 
