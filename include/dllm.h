@@ -124,7 +124,11 @@ dllm_status dllm_saliency_select(const void* cur, const void* prev, int dtype,
  *               b*batch_stride + r*row_stride (row_stride >= V).
  *   R_max       rows scored per batch row (launch size).
  *   row_idx     [B, R_max] int32 or NULL: row r reads logits row row_idx[b,r]
- *               (must be in [0, R_src)); NULL reads row r (R_max <= R_src).
+ *               (must be in [0, R_src)); NULL reads row r, which must lie
+ *               below R_src (with count NULL, R_max <= R_src is required; with
+ *               count given, R_src may be below R_max -- e.g. a buffer that
+ *               holds only the rows a step can have -- and a count above
+ *               R_src is a device-side error).
  *   count       [B] int32 or NULL: rows r < count[b] are scored (NULL: all
  *               R_max).  Must lie in [0, R_max].
  *   out_idx     [B, R_max] int32 or NULL: the results of row r land in column
@@ -138,7 +142,8 @@ dllm_status dllm_saliency_select(const void* cur, const void* prev, int dtype,
  *               bytes (256-byte aligned); its contents need no initialisation.
  * Columns not written are left untouched.  Logits must be finite.
  * Errors: INVALID_ARG (NULLs, V < 2, R_max < 1, strides, small workspace);
- * dev_status gets DEVICE_CHECK for counts/indices out of range (row skipped).
+ * dev_status gets DEVICE_CHECK for counts/indices out of range, including a
+ * row r >= R_src read without row_idx (row skipped).
  */
 size_t dllm_confidence_workspace_bytes(int B, int R_max, int V, int dtype);
 

@@ -32,4 +32,5 @@ from ._lib import (  # noqa: F401
     dllm_version,
     load_library,
 )
+from .loop import BlockDecodeLoop  # noqa: F401
 from .step import PartialStep  # noqa: F401

@@ -121,7 +121,11 @@ dllm_status dllm_confidence(const void* logits, int dtype, int B, int R_src, int
   REQUIRE(row_stride >= V, "dllm_confidence: row_stride %lld < V", (long long)row_stride);
   REQUIRE(B == 1 || batch_stride >= (int64_t)R_src * row_stride,
           "dllm_confidence: batch_stride too small");
-  REQUIRE(row_idx != nullptr || R_max <= R_src, "dllm_confidence: R_max > R_src without row_idx");
+  // Without row_idx, rows r < count[b] are read; a count above R_src is caught on the device
+  // (DEVICE_CHECK, the rows past R_src skipped), so only a call that scores all R_max rows
+  // needs R_max <= R_src here.
+  REQUIRE(row_idx != nullptr || count != nullptr || R_max <= R_src,
+          "dllm_confidence: R_max > R_src without row_idx or count");
   REQUIRE(out_cols >= 1 && (out_idx != nullptr || R_max <= out_cols),
           "dllm_confidence: out_cols %d too small", out_cols);
   const size_t need = dllm::confidence_workspace_bytes(B, R_max, V, dtype);
