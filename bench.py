@@ -70,7 +70,8 @@ KERNELS = {  # kernels each entry point launches, and the source they come from
     "dllm_kv_scatter": (["kv_scatter_kernel"], "kv_scatter.cu"),
     "dllm_partial_attention": (["attn_fwd_tc_kernel", "attn_split_merge_kernel"],
                                "attention_tc.cu"),
-    "dllm_attention_colsum": (["attn_colsum_tc_kernel"], "attention_tc.cu"),
+    "dllm_attention_colsum": (["attn_colsum_stream_kernel", "attn_colsum_tc_kernel"],
+                              "attention_tc.cu"),
     "dllm_confidence": (["conf_stream_kernel", "conf_merge_kernel"], "confidence.cu"),
     "dllm_stable_prefix": (["stable_prefix_kernel"], "stable_prefix.cu"),
     "dllm_lock_criterion": (["lock_partial_kernel", "lock_merge_kernel", "lock_gate_kernel"],
@@ -544,7 +545,10 @@ def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None, locked=None)
 
 
 def launches_per_step(wl: Workload, bf: Buffers) -> int:
-    n = 2 + 1 + (2 if bf.attn_split else 1) + 1 + 1
+    # select 2, scatter 1, attention 1 (+ the split merge), column sums 2
+    # (persistent kernel for small heads, key-tile-group kernel for the
+    # rest), prefix 1; confidence 2 (streaming kernel, row merge)
+    n = 2 + 1 + (2 if bf.attn_split else 1) + 2 + 1
     if wl.conf is not None:
         n += 2
     if wl.surelock:
@@ -700,8 +704,9 @@ def reference_arm(args, rank):
 # ----------------------------------------------------------------------------- decoding loop
 
 LOOP_ORDER = ENTRY_ORDER  # the six calls of a loop step, in order
-LOOP_LAUNCHES_PER_STEP = 9  # cos_rows + compact, kv_scatter, attn_fwd + split merge, colsum,
-                            # conf_stream + conf_merge, stable_prefix
+LOOP_LAUNCHES_PER_STEP = 10  # cos_rows + compact, kv_scatter, attn_fwd + split merge,
+                             # colsum (persistent + key-tile-group), conf_stream + conf_merge,
+                             # stable_prefix
 
 
 def loop_desc(sh) -> str:

@@ -7,20 +7,27 @@
 // cost O(M N d).  Attn-Sampler, technical summary, Methodology 2: column sums
 // of the attention matrix, computed block by block without materialising it.
 //
-// attn_fwd_tc_kernel -- persistent, one CTA per SM; work items are (128 active
-//   query rows, head, batch row), each optionally limited to a slice of the
-//   key range when there are fewer query tiles than SMs (attn_split_merge_kernel
-//   then combines the slices):
-//   warp 0     TMA producer: the Q tile once, then K/V tiles of 128 keys into
-//              a two-stage ring (128-byte swizzle, 16 KB boxes of 64 dims).
-//   warp 1     one thread issues tcgen05.mma: S = Q K^T into one of two TMEM
-//              score buffers (so the next tile's QK^T overlaps the softmax),
-//              then O += P V into a TMEM accumulator.
-//   warps 2-5  softmax: each thread owns one query row (its TMEM lane), loads
-//              the S row with tcgen05.ld, keeps a running maximum (rescaling O
-//              in TMEM only when the maximum grows by more than 2^8) and sum,
-//              and writes P in bf16 to shared memory in the operand layout the
-//              P V product reads.  Epilogue: O / l in bf16 and the row's lse.
+// attn_fwd_tc_kernel -- persistent, one CTA per SM; a work item is a pair of
+//   query tiles of 128 active rows of one (batch row, head), or a single tile
+//   when the head has an odd number of tiles, optionally limited to a slice
+//   of the key range when there are too few items for the SMs
+//   (attn_split_merge_kernel then combines the slices):
+//   warp 8     TMA producer: the Q tiles once per item, then K and V tiles of
+//              128 keys into a three-stage K ring and a two-stage V ring
+//              (128-byte swizzle, 16 KB boxes of 64 dims).
+//   warp 9     one thread issues tcgen05.mma: S_x = Q K^T into one of two TMEM
+//              score buffers, then O_x += P_x V into a TMEM accumulator.
+//   warps 0-7  two softmax warpgroups, slot x = warp / 4, each thread one
+//              query row (its TMEM lane).  In a pair item slot x holds query
+//              tile x over every key tile (the two tiles ping-pong on the
+//              tensor cores and share each K/V tile).  In a one-tile item slot
+//              x takes the key tiles t with t % 2 == x, so the next tile's
+//              Q K^T never waits for this tile's softmax, and slot 0 merges
+//              slot 1's partial O, maximum and sum at the end.  Each slot
+//              loads its S row with tcgen05.ld, keeps a running maximum
+//              (rescaling O in TMEM only when it grows by more than 2^8) and
+//              sum, and writes P in bf16 back over S, where the P V product
+//              reads it.  Epilogue: O / l in bf16 and the row's lse.
 // attn_colsum_tc_kernel -- second normalised pass, one CTA per (128 keys,
 //   head, batch row): S^T = K Q^T per tile of 128 active queries on the tensor
 //   cores, then each thread (one key) adds exp(s - lse_i) over the active
@@ -57,10 +64,11 @@ constexpr int kFwdThreads = 320;
 constexpr int kWarpTma = 8;
 constexpr int kWarpMma = 9;
 // Exponential pairs computed on the FMA pipe (exp2_poly2) instead of MUFU,
-// out of every 8: the forward softmax and the column sums are otherwise
-// bound by the MUFU ex2 rate.
+// out of every 8: the forward softmax is otherwise bound by the MUFU ex2
+// rate.  The column sums are not (measured faster with MUFU alone: their
+// FMA pipe is busy with the scaling and the sums).
 constexpr int kFwdPoly = 2;
-constexpr int kColsumPoly = 3;
+constexpr int kColsumPoly = 0;
 
 struct FwdParams {
   const int32_t* count;
@@ -81,13 +89,25 @@ struct ColsumParams {
   int L, H, M_max;
   float scale_log2;
   int32_t* dev_status;
+  int min_qt;  // the kernel handles batch rows with more than min_qt - 1 query tiles
 };
 
-// shared-memory map of the forward kernel (offsets from a 1024-aligned base)
+// Batch rows with at most kCsMaxQt query tiles (and empty rows) take the
+// persistent column-sum kernel; the others the key-tile-group kernel.
+constexpr int kCsMaxQt = 2;
+
+// shared-memory map of the forward kernel (offsets from a 1024-aligned base).
+// K and V have rings of their own: a K tile is free once the Q K^T products
+// of its tile are done, a V tile only after the P V products, so K runs a
+// stage deeper and its loads start earlier.
+constexpr int kKStages = 3;                                // K ring depth
+constexpr int kVStages = 2;                                // V ring depth
 constexpr uint32_t kFwdQ = 0;                              // Q tile A, then Q tile B
-constexpr uint32_t kFwdKV = 2 * kTile;                     // + s * 2 * kTile: K, then V
-constexpr uint32_t kFwdBar = kFwdKV + kStages * 2 * kTile; // 192 KB
-constexpr uint32_t kFwdSmem = kFwdBar + 256 + 1024;
+constexpr uint32_t kFwdK = 2 * kTile;                      // + s * kTile
+constexpr uint32_t kFwdV = kFwdK + kKStages * kTile;       // + s * kTile
+constexpr uint32_t kFwdBar = kFwdV + kVStages * kTile;     // 224 KB
+constexpr uint32_t kFwdX = kFwdBar + 256;                  // one-tile items: (m, l) of slot 1
+constexpr uint32_t kFwdSmem = kFwdX + 2 * kBM * 4 + 1024;
 
 // tensor-memory columns of the forward kernel (512 allocated): scores S of
 // tile A and B (P overwrites the first 64 columns of its S as bf16 pairs),
@@ -156,8 +176,11 @@ __device__ FwdPlan make_plan(const FwdParams& p, const int* s_cnt, int n_ctas) {
   int ns = 1, tail = 0;
   if (qp > 0 && p.max_split_items > 0) {
     if (qp < n_ctas) {
+      // as many splits as fit in one round: with at least half the SMs busy
+      // (ns = 1) every SM streams its pair's whole key range and no merge is
+      // needed; the HBM, not the SM count, is then the limit
       tail = qp;
-      ns = (n_ctas + qp - 1) / qp;
+      ns = n_ctas / qp;
     } else if (2 * (qp % n_ctas) <= n_ctas) {  // a last round at most half full
       tail = qp % n_ctas;
       ns = tail > 0 ? n_ctas / tail : 1;
@@ -253,23 +276,31 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kFwdBar);
   uint64_t* q_full = bars + 0;
   uint64_t* q_empty = bars + 1;
-  uint64_t* kv_full = bars + 2;   // [kStages]
-  uint64_t* kv_empty = bars + 4;  // [kStages]
-  uint64_t* s_full = bars + 6;    // [2]: S of tile A / B written
-  uint64_t* p_full = bars + 8;    // [2]: P of tile A / B written (4 warps each)
-  uint64_t* o_done = bars + 10;   // [2]: last P V of the item completed
-  uint64_t* o_free = bars + 12;   // [2]: epilogue has read O (4 warps each)
-  uint64_t* mma_done = bars + 14;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
-  int* abort_flag = reinterpret_cast<int*>(bars + 16);
+  uint64_t* k_full = bars + 2;    // [kKStages]
+  uint64_t* k_empty = bars + 5;   // [kKStages]
+  uint64_t* v_full = bars + 8;    // [kVStages]
+  uint64_t* v_empty = bars + 10;  // [kVStages]
+  uint64_t* s_full = bars + 12;   // [2]: S of tile A / B written
+  uint64_t* p_full = bars + 14;   // [2]: P of tile A / B written (4 warps each)
+  uint64_t* o_done = bars + 16;   // [2]: last P V of the item completed
+  uint64_t* o_free = bars + 18;   // [2]: epilogue has read O (4 warps each)
+  uint64_t* mma_done = bars + 20;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 21);
+  int* abort_flag = reinterpret_cast<int*>(bars + 22);
+  uint64_t* x_ready = bars + 23;  // one-tile items: slot 1's (m, l) published (4 warps)
+  float* x_ml = reinterpret_cast<float*>(gbase + kFwdX);  // [2][128]: m, then l
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+    for (int s = 0; s < kKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < kVStages; ++s) {
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int x = 0; x < 2; ++x) {
       mbar_init(&s_full[x], 1);
@@ -278,6 +309,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       mbar_init(&o_free[x], 4);
     }
     mbar_init(mma_done, 1);
+    mbar_init(x_ready, 4);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -294,7 +326,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
       tma_prefetch_desc(&tv);
-      int j = 0, g = 0;
+      int j = 0, gk = 0, gv = 0;  // items, K tiles and V tiles issued
       bool ok = true;
       for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
         int b, h, pair, nq, qi, kt0, nt, slot;
@@ -307,27 +339,39 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           tma_load_4d(gbase + kFwdQ + x * kTile, &tq, q_full, 0, h, row0, b);
           tma_load_4d(gbase + kFwdQ + x * kTile + kBox, &tq, q_full, 64, h, row0, b);
         }
-        for (int t = 0; t < nt; ++t, ++g) {
-          const int s = g % kStages;
-          if (g >= kStages && !mbar_wait(&kv_empty[s], ((g / kStages) - 1) & 1, abort)) {
+        // K(t), then V(t): V(t)'s slot is freed by the P V products of tile
+        // t - 2, which also lets K(t + 1) start three tiles before its Q K^T.
+        for (int t = 0; t < nt; ++t) {
+          const int key0 = (kt0 + t) * kBN;
+          const int sk = gk % kKStages;
+          if (gk >= kKStages && !mbar_wait(&k_empty[sk], ((gk / kKStages) - 1) & 1, abort)) {
             ok = false;
             break;
           }
-          uint8_t* kdst = gbase + kFwdKV + s * 2 * kTile;
-          uint8_t* vdst = kdst + kTile;
-          const int key0 = (kt0 + t) * kBN;
-          mbar_expect_tx(&kv_full[s], 2 * kTile);
-          tma_load_4d(kdst, &tk, &kv_full[s], 0, h, key0, b);
-          tma_load_4d(kdst + kBox, &tk, &kv_full[s], 64, h, key0, b);
-          tma_load_4d(vdst, &tv, &kv_full[s], 0, h, key0, b);
-          tma_load_4d(vdst + kBox, &tv, &kv_full[s], 64, h, key0, b);
+          uint8_t* kdst = gbase + kFwdK + sk * kTile;
+          mbar_expect_tx(&k_full[sk], kTile);
+          tma_load_4d(kdst, &tk, &k_full[sk], 0, h, key0, b);
+          tma_load_4d(kdst + kBox, &tk, &k_full[sk], 64, h, key0, b);
+          ++gk;
+          const int sv = gv % kVStages;
+          if (gv >= kVStages && !mbar_wait(&v_empty[sv], ((gv / kVStages) - 1) & 1, abort)) {
+            ok = false;
+            break;
+          }
+          uint8_t* vdst = gbase + kFwdV + sv * kTile;
+          mbar_expect_tx(&v_full[sv], kTile);
+          tma_load_4d(vdst, &tv, &v_full[sv], 0, h, key0, b);
+          tma_load_4d(vdst + kBox, &tv, &v_full[sv], 64, h, key0, b);
+          ++gv;
         }
       }
       // Drain: never leave with copies in flight into this CTA's shared memory.
       int none = 0;
       if (j > 0) mbar_wait(q_full, (j - 1) & 1, &none);
-      for (int k = g - kStages < 0 ? 0 : g - kStages; k < g; ++k)
-        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &none);
+      for (int k = gk - kKStages < 0 ? 0 : gk - kKStages; k < gk; ++k)
+        mbar_wait(&k_full[k % kKStages], (k / kKStages) & 1, &none);
+      for (int k = gv - kVStages < 0 ? 0 : gv - kVStages; k < gv; ++k)
+        mbar_wait(&v_full[k % kVStages], (k / kVStages) & 1, &none);
       if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
     }
   } else if (warp == kWarpMma) {
@@ -335,9 +379,10 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     if (lane == 0) {
       const uint32_t id_qk = idesc_bf16_f32(kBM, kBN, false, false);
       const uint32_t id_pv = idesc_bf16_f32(kBM, kHD, false, true);
-      auto issue_qk = [&](int x, int s) {
-        const uint32_t sQ = base + kFwdQ + x * kTile;
-        const uint32_t sK = base + kFwdKV + s * 2 * kTile;
+      // S_x = Q_qx K(s)^T, then s_full[x]
+      auto issue_qk = [&](int qx, int x, int s) {
+        const uint32_t sQ = base + kFwdQ + qx * kTile;
+        const uint32_t sK = base + kFwdK + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < kHD / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
@@ -347,7 +392,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         mma_commit(&s_full[x]);
       };
       auto issue_pv = [&](int x, int s, bool acc) {
-        const uint32_t sV = base + kFwdKV + s * 2 * kTile + kTile;
+        const uint32_t sV = base + kFwdV + s * kTile;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_bf16_ts(tmem + kTmO + x * kHD, tmem + kTmS + x * kBN + kk * 8,
@@ -363,42 +408,106 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         item_of(plan, v, &qi, &kt0, &nt, &slot);
         decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
         if (!mbar_wait(q_full, j & 1, abort)) break;
-        if (!mbar_wait(&kv_full[g % kStages], (g / kStages) & 1, abort)) break;
-        tc_fence_after();
-        for (int x = 0; x < nq; ++x) issue_qk(x, g % kStages);
-        if (nt == 1) mma_commit(q_empty);
-        for (int t = 0; t < nt && ok; ++t) {
-          const int s = (g + t) % kStages;
-          const int s1 = (g + t + 1) % kStages;
-          const bool more = t + 1 < nt;
-          for (int x = 0; x < nq; ++x) {
-            if (!mbar_wait(&p_full[x], gt[x] & 1, abort)) {
-              ok = false;
-              break;
-            }
-            if (t == 0 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            issue_pv(x, s, t > 0);
-            if (x == nq - 1) mma_commit(&kv_empty[s]);  // V(t) (and K(t)) no longer read
-            if (more) {
-              if (x == 0 && !mbar_wait(&kv_full[s1], ((g + t + 1) / kStages) & 1, abort)) {
+        if (nq == 2) {
+          // Pair of query tiles: per key tile t the order is
+          //   O_A += P_A(t) V(t), S_A = Q_A K(t+1)^T, O_B += P_B(t) V(t), S_B = Q_B K(t+1)^T.
+          if (!mbar_wait(&k_full[g % kKStages], (g / kKStages) & 1, abort)) break;
+          tc_fence_after();
+          for (int x = 0; x < 2; ++x) issue_qk(x, x, g % kKStages);
+          mma_commit(&k_empty[g % kKStages]);  // K(0) is read by its Q K^T products only
+          if (nt == 1) mma_commit(q_empty);
+          for (int t = 0; t < nt && ok; ++t) {
+            const int sv = (g + t) % kVStages;
+            const int sk1 = (g + t + 1) % kKStages;
+            const bool more = t + 1 < nt;
+            for (int x = 0; x < 2; ++x) {
+              if (!mbar_wait(&p_full[x], gt[x] & 1, abort)) {
+                ok = false;
+                break;
+              }
+              if (t == 0 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort)) {
+                ok = false;
+                break;
+              }
+              if (x == 0 && !mbar_wait(&v_full[sv], ((g + t) / kVStages) & 1, abort)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
-              issue_qk(x, s1);
-              if (x == nq - 1 && t + 2 == nt) mma_commit(q_empty);  // last read of Q
+              issue_pv(x, sv, t > 0);
+              if (x == 1) mma_commit(&v_empty[sv]);  // V(t) no longer read
+              if (more) {
+                if (x == 0 && !mbar_wait(&k_full[sk1], ((g + t + 1) / kKStages) & 1, abort)) {
+                  ok = false;
+                  break;
+                }
+                tc_fence_after();
+                issue_qk(x, x, sk1);
+                if (x == 1) {
+                  mma_commit(&k_empty[sk1]);                // K(t + 1) no longer read
+                  if (t + 2 == nt) mma_commit(q_empty);     // last read of Q
+                }
+              } else {
+                mma_commit(&o_done[x]);
+              }
+              ++gt[x];
+            }
+          }
+          g += nt;
+          ++jt[0];
+          ++jt[1];
+        } else {
+          // One query tile: key tile t goes to slot x = t % 2 (S_x, then
+          // O_x), so the two softmax warpgroups take alternate key tiles and
+          // the Q K^T of tile t + 2 is issued right after the P V of tile t.
+          for (int t = 0; t < 2 && t < nt && ok; ++t) {
+            const int sk = (g + t) % kKStages;
+            if (!mbar_wait(&k_full[sk], ((g + t) / kKStages) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_qk(0, t, sk);
+            mma_commit(&k_empty[sk]);
+          }
+          if (ok && nt <= 2) mma_commit(q_empty);
+          for (int t = 0; t < nt && ok; ++t) {
+            const int x = t & 1;
+            const int sv = (g + t) % kVStages;
+            if (!mbar_wait(&p_full[x], gt[x] & 1, abort)) {
+              ok = false;
+              break;
+            }
+            if (t < 2 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            if (!mbar_wait(&v_full[sv], ((g + t) / kVStages) & 1, abort)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_pv(x, sv, t >= 2);
+            mma_commit(&v_empty[sv]);  // V(t) no longer read
+            if (t + 2 < nt) {
+              const int sk = (g + t + 2) % kKStages;
+              if (!mbar_wait(&k_full[sk], ((g + t + 2) / kKStages) & 1, abort)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              issue_qk(0, x, sk);
+              mma_commit(&k_empty[sk]);
+              if (t + 3 == nt) mma_commit(q_empty);  // last read of Q
             } else {
               mma_commit(&o_done[x]);
             }
             ++gt[x];
           }
+          g += nt;
+          ++jt[0];
+          if (nt > 1) ++jt[1];
         }
-        g += nt;
-        for (int x = 0; x < nq; ++x) ++jt[x];
       }
       // Every MMA issued above completes before the tensor memory is freed.
       mma_commit(mma_done);
@@ -408,25 +517,46 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int x = warp >> 2;           // query tile slot: 0 = A, 1 = B
+    // Slot x = warp / 4 owns S_x and O_x.  In a pair item slot x holds query
+    // tile x over every key tile; in a one-tile item both slots hold the same
+    // query tile, slot x the key tiles t with t % 2 == x, and slot 0 merges
+    // slot 1's partial O, maximum and sum into the result.
+    const int x = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // row of the tile
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     const uint32_t tS = tmem + lane_base + kTmS + x * kBN;
     const uint32_t tO = tmem + lane_base + kTmO + x * kHD;
+    const uint32_t tO1 = tmem + lane_base + kTmO + kHD;  // slot 1's O (read by slot 0)
     const float sl2 = p.scale_log2;
-    int gx = 0, jx = 0;
+    int gx = 0, jx = 0, jd = 0;  // tiles and items of this slot, merged one-tile items
     bool ok = true;
     for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x) {
       int b, h, pair, nq, qi, kt0, nt, wslot;
       item_of(plan, v, &qi, &kt0, &nt, &wslot);
       decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
-      if (x >= nq) continue;
+      const bool single = nq == 1;
+      const int qtile = single ? 0 : x;  // query tile of the pair this slot reads
+      const int mine = single ? (x == 0 ? (nt + 1) / 2 : nt / 2) : nt;  // key tiles of this slot
+      if (mine == 0) continue;
+      const bool merge = single && nt > 1;  // slot 0 combines both slots' results
+      // A warp whose 32 rows all lie past the count only keeps the
+      // handshakes: its P rows feed only O rows that are never stored (row i
+      // of P V depends on row i of P alone).
+      const bool idle = (2 * pair + qtile) * kBM + quarter * 32 >= cnt_of(p, s_cnt, b);
       float m = -INFINITY, l = 0.f;
-      for (int t = 0; t < nt; ++t, ++gx) {
+      // key tiles kt0 + x, kt0 + x + 2, ... (one-tile item) or kt0, kt0 + 1, ...
+      const int kstep = single ? 2 : 1;
+      int kvalid = p.L - (kt0 + (single ? x : 0)) * kBN;  // < kBN only on the last, partial tile
+      for (int tt = 0; tt < mine; ++tt, ++gx, kvalid -= kstep * kBN) {
         if (!warp_wait(&s_full[x], gx & 1, abort)) {
           ok = false;
           break;
+        }
+        if (idle) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&p_full[x]);
+          continue;
         }
         tc_fence_after();
         // The whole S row (128 keys) is read with one wait; the row maximum
@@ -434,7 +564,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         // in chunks of 32 keys and stored as bf16 pairs into the first 64
         // columns of S (P column j holds keys 2j, 2j + 1; those S columns
         // are already in registers).
-        const int kvalid = p.L - (kt0 + t) * kBN;  // < kBN only on the last, partial tile
         uint32_t raw[kBN];
 #pragma unroll
         for (int c = 0; c < kBN / 32; ++c)
@@ -492,9 +621,9 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         }
         // O is rescaled in place when some row's maximum grew (tcgen05.ld/st
         // are warp-collective, so the warp votes; rows that did not grow
-        // multiply by 1).  O of the first tile of an item is written without
+        // multiply by 1).  The slot's first P V of an item is written without
         // accumulation and needs none.
-        if (t > 0 && __any_sync(0xffffffffu, grow)) {
+        if (tt > 0 && __any_sync(0xffffffffu, grow)) {
 #pragma unroll 1
           for (int c = 0; c < kHD / 32; ++c) {
             uint32_t ov[32];
@@ -516,22 +645,65 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         break;
       }
       ++jx;
+      if (merge && x == 1) {
+        // slot 1 publishes its maximum and sum; slot 0 reads O_1 and
+        // releases it
+        if (!idle) {
+          x_ml[r] = m;
+          x_ml[kBM + r] = l;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(x_ready);
+        continue;
+      }
       // ---------------------------------------------------------- epilogue
+      float a0 = 1.0f, a1 = 0.0f;  // weights of O_x and O_1 (merged one-tile items)
+      if (merge) {
+        if (!warp_wait(x_ready, jd & 1, abort)) {
+          ok = false;
+          break;
+        }
+        ++jd;
+        if (!idle) {
+          const float m1 = x_ml[r], l1 = x_ml[kBM + r];
+          const float mm = fmaxf(m, m1);
+          a0 = ex2_approx(m - mm);
+          a1 = ex2_approx(m1 - mm);
+          l = a0 * l + a1 * l1;
+          m = mm;
+        }
+      }
       tc_fence_after();
       const int n = cnt_of(p, s_cnt, b);
-      const int i = (2 * pair + x) * kBM + r;
+      const int i = (2 * pair + qtile) * kBM + r;
       const bool store = i < n;
       const bool partial = wslot >= 0;
       const float inv = partial ? 1.0f : 1.0f / l;
-      const int64_t slot = (int64_t)wslot * 2 + x;  // workspace tile slot (split items)
+      const float w0 = a0 * inv, w1 = a1 * inv;
+      const int64_t slot = (int64_t)wslot * 2 + qtile;  // workspace tile slot (split items)
       __nv_bfloat16* orow =
           p.o + ((int64_t)b * p.M_max + i) * ((int64_t)p.H * kHD) + (int64_t)h * kHD;
       float* prow = p.ws_o + (slot * kBM + r) * kHD;
 #pragma unroll 1
-      for (int c = 0; c < kHD / 32; ++c) {
+      for (int c = 0; c < (idle ? 0 : kHD / 32); ++c) {
         uint32_t ov[32];
         tmem_ld_32x32b_x32(tO + c * 32, ov);
-        tmem_ld_wait();
+        if (merge) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            uint32_t o1[16];
+            tmem_ld_32x32b_x16(tO1 + c * 32 + hf * 16, o1);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+              ov[hf * 16 + q] = __float_as_uint(
+                  fmaf(__uint_as_float(ov[hf * 16 + q]), w0, __uint_as_float(o1[q]) * w1));
+          }
+        } else {
+          tmem_ld_wait();
+#pragma unroll
+          for (int q = 0; q < 32; ++q) ov[q] = __float_as_uint(__uint_as_float(ov[q]) * w0);
+        }
         if (store && partial) {
           float4* dst = reinterpret_cast<float4*>(prow + c * 32);
 #pragma unroll
@@ -543,18 +715,22 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             uint4 w;
-            w.x = pack_bf16(__uint_as_float(ov[q * 8 + 0]) * inv, __uint_as_float(ov[q * 8 + 1]) * inv);
-            w.y = pack_bf16(__uint_as_float(ov[q * 8 + 2]) * inv, __uint_as_float(ov[q * 8 + 3]) * inv);
-            w.z = pack_bf16(__uint_as_float(ov[q * 8 + 4]) * inv, __uint_as_float(ov[q * 8 + 5]) * inv);
-            w.w = pack_bf16(__uint_as_float(ov[q * 8 + 6]) * inv, __uint_as_float(ov[q * 8 + 7]) * inv);
+            w.x = pack_bf16(__uint_as_float(ov[q * 8 + 0]), __uint_as_float(ov[q * 8 + 1]));
+            w.y = pack_bf16(__uint_as_float(ov[q * 8 + 2]), __uint_as_float(ov[q * 8 + 3]));
+            w.z = pack_bf16(__uint_as_float(ov[q * 8 + 4]), __uint_as_float(ov[q * 8 + 5]));
+            w.w = pack_bf16(__uint_as_float(ov[q * 8 + 6]), __uint_as_float(ov[q * 8 + 7]));
             dst[q] = w;
           }
         }
       }
-      // O is read: the next item's first P V may overwrite it.
+      // O is read: the next item's first P V may overwrite it (both slots'
+      // O after a merged one-tile item).
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&o_free[x]);
+      if (lane == 0) {
+        mbar_arrive(&o_free[x]);
+        if (merge) mbar_arrive(&o_free[1]);
+      }
       if (store) {
         if (partial) {
           p.ws_ml[(slot * kBM + r) * 2 + 0] = m;
@@ -674,6 +850,7 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   int n = __ldca(p.count + b);
   n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
   const int nqt = (n + kBM - 1) / kBM;
+  if (nqt < p.min_qt) return;  // the persistent kernel covers this batch row
   const int nkt = (p.L + kBN - 1) / kBN;
   const int nk = min(NK, nkt - kg * NK);  // key tiles of this CTA
   const int key_base = kg * NK * kBN;
@@ -865,6 +1042,272 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
   if (threadIdx.x == 0 && *abort) report(p.dev_status, DLLM_ERR_TIMEOUT);
 }
 
+// Column sums of batch rows with at most two query tiles (the small active
+// sets of most steps), persistent: one CTA per SM takes a contiguous range of
+// (batch row, head, key tile) items.  Warp 8 loads the query tiles of a head
+// once (they stay resident while its key tiles pass) and streams the key
+// tiles through a four-stage ring; warp 9 issues S^T = K Q^T for each query
+// tile of the item into the TMEM buffer of softmax warpgroup g = item % 2
+// (256 columns each), so one warpgroup adds up the exponentials of one key
+// tile while the tensor cores and the other warpgroup work on the next.  Each
+// softmax thread owns one key: it adds 2^(s * scale * log2 e - lse * log2 e)
+// over the active query rows (chunks of 32 queries past the count are
+// skipped; -lse sits in a warp-private shared buffer per head) and writes the
+// key's column sum.  Rows with no active query get zeros.  Each key has one
+// owner thread: no atomics, run-to-run identical.
+constexpr int kCsThreads = 320;  // warps 0-7 softmax (two groups), 8 TMA, 9 MMA
+constexpr int kCsKStages = 4;
+constexpr uint32_t kCsQ = 0;                                   // kCsMaxQt query tiles
+constexpr uint32_t kCsK = kCsMaxQt * kTile;                    // + s * kTile
+constexpr uint32_t kCsL = kCsK + kCsKStages * kTile;           // [8 warps][256] -lse log2 e
+constexpr uint32_t kCsBar = kCsL + 8 * kCsMaxQt * kBM * 4;
+constexpr uint32_t kCsSmem = kCsBar + 256 + 1024;
+
+__global__ void __launch_bounds__(kCsThreads, 1)
+attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
+                          const __grid_constant__ CUtensorMap tk, ColsumParams p, int B) {
+  pdl_wait();  // the previous kernel on the stream has completed
+  pdl_trigger();
+  __shared__ int s_nqt[kPlanMaxB];      // query tiles of each batch row; -1: not handled here
+  __shared__ int s_first[kPlanMaxB + 1];  // first item of each batch row
+  const int nkt = (p.L + kBN - 1) / kBN;
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int b = 0; b < B; ++b) {
+      int n = __ldca(p.count + b);
+      n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
+      const int nqt = (n + kBM - 1) / kBM;
+      s_first[b] = acc;
+      s_nqt[b] = nqt <= kCsMaxQt ? nqt : -1;
+      if (nqt <= kCsMaxQt) acc += p.H * nkt;
+    }
+    s_first[B] = acc;
+  }
+  __syncthreads();
+  const int N = s_first[B];
+  const int i0 = (int)((long long)blockIdx.x * N / gridDim.x);
+  const int i1 = (int)((long long)(blockIdx.x + 1) * N / gridDim.x);
+  if (i0 >= i1) return;
+  // item i -> (b, h, kt).  The key tiles of a head are taken last first:
+  // the forward pass that usually runs just before streams every head's key
+  // tiles first to last, so its last tiles are the ones still in L2.
+  auto decode = [&](int i, int* b, int* h, int* kt) {
+    int bb = 0;
+    while (s_nqt[bb] < 0 || i >= s_first[bb + 1]) ++bb;
+    const int r = i - s_first[bb];
+    *b = bb;
+    *h = r / nkt;
+    *kt = nkt - 1 - (r - *h * nkt);
+  };
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_addr);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kCsBar);
+  uint64_t* q_full = bars + 0;
+  uint64_t* q_empty = bars + 1;
+  uint64_t* k_full = bars + 2;                // [kCsKStages]
+  uint64_t* k_empty = bars + 2 + kCsKStages;  // [kCsKStages]
+  uint64_t* s_full = bars + 2 + 2 * kCsKStages;  // [2]
+  uint64_t* s_free = bars + 4 + 2 * kCsKStages;  // [2] (4 warps each)
+  uint64_t* mma_done = bars + 6 + 2 * kCsKStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * kCsKStages);
+  int* abort_flag = reinterpret_cast<int*>(bars + 8 + 2 * kCsKStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    for (int s = 0; s < kCsKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int g = 0; g < 2; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&s_free[g], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) tmem_alloc(tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abort = abort_flag;
+
+  if (warp == 8) {
+    // ------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      int kc = 0, sq = 0, cur = -1;
+      for (int i = i0; i < i1; ++i) {
+        int b, h, kt;
+        decode(i, &b, &h, &kt);
+        const int nqt = s_nqt[b];
+        if (nqt == 0) continue;
+        if (b * p.H + h != cur) {  // a new head: its query tiles, once
+          if (sq > 0 && !mbar_wait(q_empty, (sq - 1) & 1, abort)) break;
+          mbar_expect_tx(q_full, (uint32_t)nqt * kTile);
+          for (int qt = 0; qt < nqt; ++qt) {
+            tma_load_4d(gbase + kCsQ + qt * kTile, &tq, q_full, 0, h, qt * kBM, b);
+            tma_load_4d(gbase + kCsQ + qt * kTile + kBox, &tq, q_full, 64, h, qt * kBM, b);
+          }
+          cur = b * p.H + h;
+          ++sq;
+        }
+        const int s = kc % kCsKStages;
+        if (kc >= kCsKStages && !mbar_wait(&k_empty[s], ((kc / kCsKStages) - 1) & 1, abort))
+          break;
+        mbar_expect_tx(&k_full[s], kTile);
+        tma_load_4d(gbase + kCsK + s * kTile, &tk, &k_full[s], 0, h, kt * kBN, b);
+        tma_load_4d(gbase + kCsK + s * kTile + kBox, &tk, &k_full[s], 64, h, kt * kBN, b);
+        ++kc;
+      }
+      int none = 0;
+      if (sq > 0) mbar_wait(q_full, (sq - 1) & 1, &none);
+      for (int k = kc - kCsKStages < 0 ? 0 : kc - kCsKStages; k < kc; ++k)
+        mbar_wait(&k_full[k % kCsKStages], (k / kCsKStages) & 1, &none);
+      if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id = idesc_bf16_f32(kBN, kBM, false, false);
+      int kc = 0, sq = 0, cur = -1;
+      int ng[2] = {0, 0};  // items with query tiles per softmax group
+      bool ok = true;
+      for (int i = i0; ok && i < i1; ++i) {
+        int b, h, kt;
+        decode(i, &b, &h, &kt);
+        const int nqt = s_nqt[b];
+        if (nqt == 0) continue;
+        const int g = (i - i0) & 1;
+        if (b * p.H + h != cur) {
+          if (sq > 0) mma_commit(q_empty);  // every product with the previous head's Q issued
+          if (!mbar_wait(q_full, sq & 1, abort)) break;
+          cur = b * p.H + h;
+          ++sq;
+        }
+        const int s = kc % kCsKStages;
+        if (!mbar_wait(&k_full[s], (kc / kCsKStages) & 1, abort)) break;
+        if (ng[g] > 0 && !mbar_wait(&s_free[g], (ng[g] - 1) & 1, abort)) break;
+        tc_fence_after();
+        const uint32_t sK = base + kCsK + s * kTile;
+        for (int qt = 0; qt < nqt; ++qt) {
+          const uint32_t sQ = base + kCsQ + qt * kTile;
+#pragma unroll
+          for (int kk = 0; kk < kHD / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            mma_bf16_ss(tmem + g * 256 + qt * kBM, smem_desc_sw128(sK + off, 16, 1024),
+                        smem_desc_sw128(sQ + off, 16, 1024), id, kk > 0);
+          }
+        }
+        mma_commit(&s_full[g]);
+        mma_commit(&k_empty[s]);
+        ++kc;
+        ++ng[g];
+      }
+      mma_commit(mma_done);
+      int none = 0;
+      mbar_wait(mma_done, 0, &none);
+      if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int g = warp >> 2;
+    const int quarter = warp & 3;
+    const int j = quarter * 32 + lane;  // key of this thread within the tile
+    const uint32_t tS = tmem + ((uint32_t)(quarter * 32) << 16) + g * 256;
+    float* lb = reinterpret_cast<float*>(gbase + kCsL) + warp * (kCsMaxQt * kBM);
+    const float sl2 = p.scale_log2;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    int ng = 0, cur = -1, n = 0;
+    bool ok = true;
+    for (int i = i0 + g; ok && i < i1; i += 2) {
+      int b, h, kt;
+      decode(i, &b, &h, &kt);
+      const int nqt = s_nqt[b];
+      const int key = kt * kBN + j;
+      float* out = p.colsum + ((int64_t)b * p.H + h) * p.L;
+      if (nqt == 0) {
+        if (key < p.L) out[key] = 0.f;
+        continue;
+      }
+      if (b * p.H + h != cur) {  // -lse (log2 units) of the head's query rows, -inf past the count
+        cur = b * p.H + h;
+        n = __ldca(p.count + b);
+        n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
+        const float* lse_g = p.lse + ((int64_t)b * p.H + h) * p.M_max;
+        __syncwarp();
+        for (int q = lane; q < nqt * kBM; q += 32) lb[q] = q < n ? -__ldca(lse_g + q) * kLog2e : -INFINITY;
+        __syncwarp();
+      }
+      if (!warp_wait(&s_full[g], ng & 1, abort)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      const int nch = (n + 31) / 32;  // chunks of 32 queries holding an active row
+      auto add_chunk = [&](const uint32_t(&rw)[32], int c) {
+        const float4* nl4 = reinterpret_cast<const float4*>(lb + c * 32);
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 L4 = nl4[q4];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int q = q4 * 4 + hh * 2;
+            const float2 a = __ffma2_rn(make_float2(__uint_as_float(rw[q]), __uint_as_float(rw[q + 1])),
+                                        sl2x2, hh ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y));
+            float2 e;
+            if (((q >> 1) & 7) >= 8 - kColsumPoly) {
+              e = exp2_poly2(a);
+            } else {
+              e.x = ex2_approx(a.x);
+              e.y = ex2_approx(a.y);
+            }
+            if (hh)
+              acc1 = __fadd2_rn(acc1, e);
+            else
+              acc0 = __fadd2_rn(acc0, e);
+          }
+        }
+      };
+      // two register buffers: the next chunk's scores load while one is summed
+      uint32_t ra[32], rb[32];
+      tmem_ld_32x32b_x32(tS, ra);
+      tmem_ld_wait();
+      for (int c = 0; c < nch; c += 2) {
+        if (c + 1 < nch) tmem_ld_32x32b_x32(tS + (c + 1) * 32, rb);
+        add_chunk(ra, c);
+        tmem_ld_wait();
+        if (c + 1 < nch) {
+          if (c + 2 < nch) tmem_ld_32x32b_x32(tS + (c + 2) * 32, ra);
+          add_chunk(rb, c + 1);
+          tmem_ld_wait();
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[g]);  // S_g is read: the item after next may overwrite it
+      ++ng;
+      if (key < p.L) out[key] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 8) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+  if (threadIdx.x == 0 && *abort) report(p.dev_status, DLLM_ERR_TIMEOUT);
+}
+
 template <int NK>
 constexpr uint32_t colsum_smem_bytes() {
   return NK * kTile + kStages * kTile + 4 * NK * 2 * kBM * 4 + 256 + 1024;
@@ -963,13 +1406,23 @@ cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, 
   CUtensorMap tq, tk;
   if (!make_rows_map(&tq, q, B, M_max, H) || !make_rows_map(&tk, k, B, L, H))
     return cudaErrorInvalidValue;
-  ColsumParams cp{count, lse, colsum, L, H, M_max, scale * kLog2e, dev_status};
-  // Key tiles per CTA: 4 (one query tile feeds four key tiles, four warps
-  // per scheduler) while that still leaves two CTAs per SM, else fewer.
+  ColsumParams cp{count, lse, colsum, L, H, M_max, scale * kLog2e, dev_status, 0};
   const int nkt = (L + kBN - 1) / kBN;
   const int64_t bh = (int64_t)B * H;
   const int sms = num_sms();
   cudaError_t e;
+  if (B <= kPlanMaxB) {
+    // batch rows with at most kCsMaxQt query tiles: the persistent kernel;
+    // the key-tile-group kernel below then takes only the larger ones
+    e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_stream_kernel), (int)kCsSmem);
+    if (e != cudaSuccess) return e;
+    launch_pdl(attn_colsum_stream_kernel, sms, kCsThreads, kCsSmem, stream, tq, tk, cp, B);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cp.min_qt = kCsMaxQt + 1;
+  }
+  // Key tiles per CTA: 4 (one query tile feeds four key tiles, four warps
+  // per scheduler) while that still leaves two CTAs per SM, else fewer.
   if (bh * ((nkt + 3) / 4) >= 2 * sms) {
     e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_tc_kernel<4>),
                           (int)colsum_smem_bytes<4>());

@@ -97,12 +97,12 @@ def test_workload_names_and_options():
 
 def test_launch_counts():
     wl = _wl("--workload", "step_1k")
-    assert bench.launches_per_step(wl, types.SimpleNamespace(attn_split=False)) == 8
-    assert bench.launches_per_step(wl, types.SimpleNamespace(attn_split=True)) == 9
+    assert bench.launches_per_step(wl, types.SimpleNamespace(attn_split=False)) == 9
+    assert bench.launches_per_step(wl, types.SimpleNamespace(attn_split=True)) == 10
     nolog = _wl("--workload", "batch8_2k")
-    assert bench.launches_per_step(nolog, types.SimpleNamespace(attn_split=True)) == 7
+    assert bench.launches_per_step(nolog, types.SimpleNamespace(attn_split=True)) == 8
     sl = _wl("--workload", "long_4k", "--surelock")
-    assert bench.launches_per_step(sl, types.SimpleNamespace(attn_split=False)) == 12
+    assert bench.launches_per_step(sl, types.SimpleNamespace(attn_split=False)) == 13
 
 
 def test_lock_schedule_is_nested_and_linear():
