@@ -25,6 +25,9 @@ from .dllm_oracle import (  # noqa: F401
     attn_scores,
     attn_sampler_select,
     slowfast_phases,
+    slowfast_fast_select,
+    slowfast_slow_select,
+    slowfast_select,
     snap_prefix,
     step,
 )

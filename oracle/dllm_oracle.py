@@ -35,7 +35,10 @@ attention weights are the previous step's, recovered from the cached query,
 keys and log-sum-exp; the decoding order's dynamic threshold is
 max(tau, gamma * top score); structural boundaries are caller-given flags per
 vocabulary id; the SlowFast convergence point is tracked by the exact
-population variance of a window of predictions.  Each function's docstring
+population variance of a window of predictions; the fast phase unmasks the
+masked tokens of [start, region end) with confidence strictly above the
+high threshold, the slow phase the k most confident masked tokens of the
+exploration window [start, start + width).  Each function's docstring
 states its reading in full.
 """
 from __future__ import annotations
@@ -61,6 +64,9 @@ __all__ = [
     "attn_scores",
     "attn_sampler_select",
     "slowfast_phases",
+    "slowfast_fast_select",
+    "slowfast_slow_select",
+    "slowfast_select",
     "snap_prefix",
     "step",
 ]
@@ -588,6 +594,76 @@ def slowfast_phases(starts, e_cands, window: int, sigma2: float):
                     end[t, b] = hist[-1]
                     hist = []
     return phase, end
+
+
+def slowfast_fast_select(conf, masked, start, region_end, tau_high: float):
+    """Tokens the fast phase unmasks in one step.
+
+    SlowFast, section 2 (pipeline, accelerated decoding phase): once the
+    region [s_cycle, e_cycle] is stable, every still-masked token of the
+    region whose confidence exceeds the high threshold tau_high_conf is
+    unmasked at the same time.  Reading: the region is [start, region_end)
+    (the controller's region: from the start of the undecoded suffix to the
+    latest convergence prediction); "exceeds" is strict, conf > tau_high,
+    compared in float32 (NaN never passes); no fallback -- a region with no
+    such token unmasks nothing.
+
+    conf [B, L] (e.g. the confidence of dllm_confidence), masked [B, L]
+    nonzero where a position is still masked (None: all), start and
+    region_end [B].  Returns idx [B, L] int32 (ascending positions, -1 pad)
+    and count [B] int32.
+    """
+    c32 = np.asarray(conf, dtype=np.float32)
+    B, L = c32.shape
+    t32 = np.float32(tau_high)
+    idx = np.full((B, L), -1, dtype=np.int32)
+    count = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        lo, hi = max(int(start[b]), 0), min(int(region_end[b]), L)
+        sel = [p for p in range(lo, hi)
+               if (masked is None or masked[b][p]) and c32[b, p] > t32]
+        idx[b, :len(sel)] = sel
+        count[b] = len(sel)
+    return idx, count
+
+
+def slowfast_slow_select(conf, masked, start, width: int, k: int):
+    """Tokens the slow (exploratory) phase unmasks in one step.
+
+    SlowFast, section 2 (pipeline, exploratory phase): the model decodes
+    cautiously, selecting the tokens with the highest confidence in an
+    exploration window.  Reading: the window is [start, start + width) cut at
+    L; its still-masked positions with a non-NaN confidence are ranked by
+    descending float32 confidence, equal confidences by ascending position;
+    the first min(k, candidates) are selected.  Returned in ascending
+    position order: idx [B, L] int32 (-1 pad), count [B] int32.
+    """
+    c32 = np.asarray(conf, dtype=np.float32)
+    B, L = c32.shape
+    idx = np.full((B, L), -1, dtype=np.int32)
+    count = np.zeros(B, dtype=np.int32)
+    for b in range(B):
+        lo = max(int(start[b]), 0)
+        hi = min(lo + int(width), L)
+        cand = [p for p in range(lo, hi)
+                if (masked is None or masked[b][p]) and not np.isnan(c32[b, p])]
+        ranked = sorted(cand, key=lambda p: (-float(c32[b, p]), p))
+        sel = sorted(ranked[:max(int(k), 0)])
+        idx[b, :len(sel)] = sel
+        count[b] = len(sel)
+    return idx, count
+
+
+def slowfast_select(conf, masked, start, phase, region_end, tau_high: float, width: int, k: int):
+    """One SlowFast step's unmasked tokens, per batch row: the fast phase's
+    (phase 1, region [start, region_end)) or the slow phase's (phase 0)."""
+    B = len(start)
+    fi, fc = slowfast_fast_select(conf, masked, start, region_end, tau_high)
+    si, sc = slowfast_slow_select(conf, masked, start, width, k)
+    idx = np.where(np.asarray(phase)[:, None] == 1, fi, si).astype(np.int32)
+    count = np.where(np.asarray(phase) == 1, fc, sc).astype(np.int32)
+    assert idx.shape[0] == B
+    return idx, count
 
 
 # --------------------------------------------------------------------------

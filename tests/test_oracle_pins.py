@@ -743,3 +743,86 @@ def test_snap_prefix_characterisation():
         else:
             assert got == n
         assert got <= n
+
+
+# ---------------------------------------------------------------- SlowFast token selection
+
+def test_slowfast_select_golden(golden):
+    for case in golden["slowfast_select"]:
+        conf = np.array([case["conf"]], dtype=np.float64)
+        masked = np.array([case["masked"]], dtype=np.uint8)
+        idx, count = oracle.slowfast_select(conf, masked, [case["start"]], [case["phase"]],
+                                            [case["region_end"]], case["tau_high"],
+                                            case["width"], case["k"])
+        n = len(case["idx"])
+        assert count.tolist() == [n], case["derivation"]
+        assert idx[0, :n].tolist() == case["idx"], case["derivation"]
+        assert np.all(idx[0, n:] == -1)
+
+
+def test_slowfast_slow_select_matches_lexsort():
+    """The slow phase's top k against numpy's lexsort ranking (descending
+    float32 confidence, then ascending position) of the window's masked,
+    non-NaN candidates, with ties and NaN in the draws."""
+    rng = np.random.default_rng(5)
+    B, L = 6, 300
+    conf = np.round(rng.random((B, L)), 2)  # two decimals: many ties
+    conf[rng.random((B, L)) < 0.05] = np.nan
+    masked = (rng.random((B, L)) < 0.7).astype(np.uint8)
+    for width, k in ((50, 1), (64, 7), (300, 40), (17, 100)):
+        start = rng.integers(0, L, B)
+        idx, count = oracle.slowfast_slow_select(conf, masked, start, width, k)
+        for b in range(B):
+            lo, hi = start[b], min(start[b] + width, L)
+            pos = np.arange(lo, hi)
+            c32 = conf[b, lo:hi].astype(np.float32)
+            keep = (masked[b, lo:hi] != 0) & ~np.isnan(c32)
+            pos, c32 = pos[keep], c32[keep]
+            order = np.lexsort((pos, -c32.astype(np.float64)))
+            want = np.sort(pos[order[:k]])
+            assert count[b] == len(want) == min(k, len(pos))
+            assert np.array_equal(idx[b, :count[b]], want)
+
+
+def test_slowfast_slow_select_invariants():
+    """Every selected candidate is at least as confident as every candidate
+    left out, and a tie at the boundary goes to the lower position."""
+    rng = np.random.default_rng(6)
+    conf = rng.integers(0, 4, (4, 64)).astype(np.float64) / 4
+    idx, count = oracle.slowfast_slow_select(conf, None, [0, 10, 30, 60], 32, 5)
+    for b, st in enumerate([0, 10, 30, 60]):
+        window = set(range(st, min(st + 32, 64)))
+        sel = set(idx[b, :count[b]].tolist())
+        rest = window - sel
+        assert count[b] == min(5, len(window))
+        if sel and rest:
+            lo = min(conf[b, p] for p in sel)
+            assert all(conf[b, p] <= lo for p in rest)
+            assert all(p > max(q for q in sel if conf[b, q] == lo)
+                       for p in rest if conf[b, p] == lo)
+
+
+def test_slowfast_fast_select_against_boolean_masks():
+    """The fast phase equals numpy's boolean selection of the masked region
+    positions above the threshold, and its special cases: tau = -inf takes
+    every masked non-NaN position of the region, a region ending at or
+    before its start and a threshold of 1 (conf <= 1) take none."""
+    rng = np.random.default_rng(7)
+    B, L = 5, 400
+    conf = rng.random((B, L))
+    conf[rng.random((B, L)) < 0.03] = np.nan
+    masked = (rng.random((B, L)) < 0.8).astype(np.uint8)
+    start = rng.integers(0, L, B)
+    end = np.minimum(start + rng.integers(0, 200, B), L)
+    for tau in (0.3, 0.9, -np.inf, 1.0):
+        idx, count = oracle.slowfast_fast_select(conf, masked, start, end, tau)
+        for b in range(B):
+            region = np.zeros(L, dtype=bool)
+            region[start[b]:end[b]] = True
+            want = np.flatnonzero(region & (masked[b] != 0) &
+                                  (conf[b].astype(np.float32) > np.float32(tau)))
+            assert np.array_equal(idx[b, :count[b]], want)
+            if tau == 1.0:
+                assert count[b] == 0
+    idx, count = oracle.slowfast_fast_select(conf, masked, [50] * B, [50] * B, 0.0)
+    assert count.tolist() == [0] * B
