@@ -17,7 +17,8 @@
  *   dllm_snap_prefix (LSP), dllm_approx_attention_update (DyLLM's stable
  *   rows), dllm_attn_scores and dllm_attn_sampler_select (Attn-Sampler), and
  *   the host-side SlowFast controller dllm_slowfast_create / _observe /
- *   _destroy.
+ *   _destroy, its device twin dllm_slowfast_observe_device and the tokens
+ *   each SlowFast phase unmasks, dllm_slowfast_select.
  *
  * Common conventions
  *   - Every data pointer is a DEVICE pointer owned by the caller (the SlowFast
@@ -174,9 +175,13 @@ dllm_status dllm_confidence(const void* logits, int dtype, int B, int R_src,
  * dtype), exceeds DLLM_CONFIDENCE_STATIC_WS_BYTES.  Allocates nothing: no
  * cudaMalloc, no cudaFree, no allocating library routine.
  *
- * The first call on a device (made with that device current) looks up the
- * array's device address once; make that first call before any stream
- * capture.  All calls on a device share the one array and it keeps the last
+ * The first call on a device (made with that device current) loads the
+ * library's module there if CUDA's lazy loading has not yet done so, which
+ * creates the array, and looks up the array's device address once; make
+ * that first call before any stream capture.  The address is kept for the
+ * rest of the process: it belongs to the device's primary context, so after
+ * a cudaDeviceReset, or with another context current, it is stale and this
+ * entry point must not be used.  All calls on a device share the one array and it keeps the last
  * call's contents: calls whose kernels overlap on the GPU (e.g. on two
  * streams without ordering between them) race on it and must be serialised
  * by the caller.  Nothing in it needs to start at zero: each call writes
@@ -523,6 +528,71 @@ dllm_status dllm_snap_prefix(const int32_t* tokens, int B, int L, int V,
  */
 typedef struct dllm_slowfast dllm_slowfast;
 
+/*
+ * dllm_slowfast_observe_device -- the same controller with its state and its
+ * per-step arrays in device memory, as a kernel on `stream`, so that a
+ * decoding loop reads nothing back to the host (SlowFast, section 2,
+ * pipeline, as above).
+ *
+ *   state       int32 device array of dllm_slowfast_state_bytes(B, window)
+ *               bytes, zeroed by the caller before the first step of a
+ *               sequence: per batch row the number of predictions held,
+ *               then those predictions, oldest first.  Owned by the caller;
+ *               reuse it only with the same B and window.
+ *   start       [B] int32 (device): the start of the undecoded suffix.
+ *   pred_len    [B] int32 (device): the convergence prediction of this step
+ *               as a length from start, e_cand = start + pred_len (e.g.
+ *               len_out of dllm_stable_prefix over the confidence scores
+ *               with the convergence threshold, advance_start = 0).
+ *   phase_out, region_end_out  [B] int32 (device): as dllm_slowfast_observe.
+ * window <= 4096.  Errors: INVALID_ARG (NULLs, B or window < 1, window above
+ * 4096, sigma2 < 0 or NaN); dev_status gets DEVICE_CHECK for a state word
+ * out of range (that row's cycle restarts).
+ */
+size_t dllm_slowfast_state_bytes(int B, int window);
+
+dllm_status dllm_slowfast_observe_device(int32_t* state, int B, int window,
+                                         double sigma2_stable,
+                                         const int32_t* start,
+                                         const int32_t* pred_len,
+                                         int32_t* phase_out,
+                                         int32_t* region_end_out,
+                                         int32_t* dev_status, void* stream);
+
+/*
+ * dllm_slowfast_select -- the tokens a SlowFast step unmasks.
+ *
+ * SlowFast, section 2 (pipeline): the exploratory (slow) phase selects the
+ * tokens with the highest confidence in an exploration window; the
+ * accelerated (fast) phase unmasks at once every masked token of the stable
+ * region [s_cycle, e_cycle] whose confidence exceeds tau_high_conf.  Per
+ * batch row b, on the device:
+ *   phase[b] == 1 (fast): the still-masked positions p in
+ *     [start[b], region_end[b]) with conf[b,p] > tau_high (float32, NaN
+ *     never passes); no fallback (none may pass).
+ *   otherwise (slow): the min(k, candidates) still-masked positions of the
+ *     window [start[b], start[b] + width) cut at L with the highest
+ *     confidence, equal confidences by lower position, NaN never selected.
+ *
+ *   conf        [B, L] float32, contiguous (e.g. conf_out of dllm_confidence).
+ *   masked      [B, L] uint8 (nonzero = still masked) or NULL (all masked).
+ *   start, phase, region_end  [B] int32 (device): phase and region as
+ *               dllm_slowfast_observe(_device) reports them.
+ *   tau_high    fast-phase threshold; width in [1, 16384]; k in [1, 64].
+ *   idx_out     [B, L] int32: the selected positions in ascending order,
+ *               then -1.
+ *   count_out   [B] int32: how many.
+ * Errors: INVALID_ARG (NULLs, sizes, NaN tau_high); dev_status gets
+ * DEVICE_CHECK for start outside [0, L] (nothing selected) or a fast
+ * region_end outside [start, L] (clamped).
+ */
+dllm_status dllm_slowfast_select(const float* conf, const uint8_t* masked,
+                                 int B, int L, const int32_t* start,
+                                 const int32_t* phase, const int32_t* region_end,
+                                 float tau_high, int width, int k,
+                                 int32_t* idx_out, int32_t* count_out,
+                                 int32_t* dev_status, void* stream);
+
 dllm_status dllm_slowfast_create(int B, int window, double sigma2_stable,
                                  dllm_slowfast** out);
 
@@ -531,6 +601,30 @@ dllm_status dllm_slowfast_observe(dllm_slowfast* sf, const int32_t* start,
                                   int32_t* region_end_out);
 
 void dllm_slowfast_destroy(dllm_slowfast* sf);
+
+/*
+ * Diagnostics.  Neither computes anything of the step; they let tests check
+ * the library's own machinery.  The pages have no counterpart to them.
+ *
+ * dllm_exp2_fma_eval -- y[i] = 2^x[i] through the FMA-pipe exponential the
+ * attention kernels use for part of their exponentials (Cody-Waite split
+ * x = n + f, n = round(x), and a degree-4 minimax polynomial for 2^f; x is
+ * clamped at -125 and must be at most 128).  x, y: n float32 in device
+ * memory.  Errors: INVALID_ARG (NULLs, n < 1), CUDA (launch).
+ *
+ * dllm_set_wait_limit -- the clock cycles after which a bounded pipeline wait
+ * of the streaming confidence kernel and of the attention forward kernel
+ * gives up for kernels launched after this call (process-wide; 0 restores
+ * the default of about a second).  A wait that runs out records
+ * DLLM_ERR_TIMEOUT in dev_status; the kernel then waits (with the default
+ * limit) for its own copies and tensor-core work in flight, frees its tensor
+ * memory and returns, leaving that call's outputs incomplete.  For tests of
+ * that path; not thread-safe against concurrent launches.  Errors:
+ * INVALID_ARG for a negative count.
+ */
+dllm_status dllm_exp2_fma_eval(const float* x, float* y, int n, void* stream);
+
+dllm_status dllm_set_wait_limit(long long cycles);
 
 #ifdef __cplusplus
 }  /* extern "C" */

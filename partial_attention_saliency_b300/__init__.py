@@ -14,6 +14,7 @@ from ._lib import (  # noqa: F401
     LIB_PATH,
     SIGNATURES,
     SlowFast,
+    SlowFastDevice,
     dllm_adaptive_prefix,
     dllm_approx_attention_update,
     dllm_attention_colsum,
@@ -27,6 +28,7 @@ from ._lib import (  # noqa: F401
     dllm_lock_workspace_bytes,
     dllm_partial_attention,
     dllm_saliency_select,
+    dllm_slowfast_select,
     dllm_snap_prefix,
     dllm_stable_prefix,
     dllm_version,

@@ -56,6 +56,11 @@ SIGNATURES = {
     "dllm_slowfast_create": (_I, [_I, _I, ctypes.c_double, ctypes.POINTER(_P)]),
     "dllm_slowfast_observe": (_I, [_P, _P, _P, _P, _P]),
     "dllm_slowfast_destroy": (None, [_P]),
+    "dllm_slowfast_state_bytes": (_SZ, [_I, _I]),
+    "dllm_exp2_fma_eval": (_I, [_P, _P, _I, _P]),
+    "dllm_set_wait_limit": (_I, [ctypes.c_longlong]),
+    "dllm_slowfast_observe_device": (_I, [_P, _I, _I, ctypes.c_double, _P, _P, _P, _P, _P, _P]),
+    "dllm_slowfast_select": (_I, [_P, _P, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
 }
 
 
@@ -485,3 +490,57 @@ class SlowFast:
 
     def __del__(self):
         self.close()
+
+
+class SlowFastDevice:
+    """Device-side SlowFast phase controller (``dllm_slowfast_observe_device``):
+    its state and per-step arrays live on the device, so a decoding loop
+    reads nothing back.  ``observe(start, pred_len)`` takes [B] int32 CUDA
+    tensors (e_cand = start + pred_len) and returns (phase, region_end), [B]
+    int32 CUDA tensors written in place on every call."""
+
+    def __init__(self, B: int, window: int, sigma2_stable: float, device=None):
+        lib = load_library()
+        self.B, self.window, self.sigma2 = int(B), int(window), float(sigma2_stable)
+        n = int(lib.dllm_slowfast_state_bytes(self.B, self.window)) // 4
+        dev = torch.device("cuda") if device is None else device
+        self.state = torch.zeros((n,), dtype=torch.int32, device=dev)
+        self.phase = torch.zeros((self.B,), dtype=torch.int32, device=dev)
+        self.region_end = torch.zeros((self.B,), dtype=torch.int32, device=dev)
+
+    def reset(self):
+        self.state.zero_()
+
+    def observe(self, start, pred_len, *, dev_status=None, stream=None):
+        _need(start, torch.int32, (self.B,), "start")
+        _need(pred_len, torch.int32, (self.B,), "pred_len")
+        _check(load_library().dllm_slowfast_observe_device(
+            _ptr(self.state), self.B, self.window, self.sigma2, _ptr(start), _ptr(pred_len),
+            _ptr(self.phase), _ptr(self.region_end), _ptr(dev_status), _stream(stream)))
+        return self.phase, self.region_end
+
+
+def dllm_slowfast_select(conf, start, phase, region_end, tau_high: float, width: int, k: int, *,
+                         masked=None, idx_out=None, count_out=None, dev_status=None,
+                         stream=None):
+    """The positions a SlowFast step unmasks per batch row (fast phase: the
+    masked region positions above tau_high; slow phase: the k most confident
+    masked positions of [start, start + width)).  Returns (idx [B, L] int32
+    ascending then -1, count [B] int32)."""
+    lib = load_library()
+    B, L = conf.shape
+    _need(conf, torch.float32, (B, L), "conf")
+    for t, n in ((start, "start"), (phase, "phase"), (region_end, "region_end")):
+        _need(t, torch.int32, (B,), n)
+    if masked is not None:
+        _need(masked, torch.uint8, (B, L), "masked")
+    dev = conf.device
+    idx_out = torch.empty((B, L), dtype=torch.int32, device=dev) if idx_out is None else idx_out
+    count_out = torch.empty((B,), dtype=torch.int32, device=dev) if count_out is None else count_out
+    _need(idx_out, torch.int32, (B, L), "idx_out")
+    _need(count_out, torch.int32, (B,), "count_out")
+    _check(lib.dllm_slowfast_select(_ptr(conf), _ptr(masked), B, L, _ptr(start), _ptr(phase),
+                                    _ptr(region_end), float(tau_high), int(width), int(k),
+                                    _ptr(idx_out), _ptr(count_out), _ptr(dev_status),
+                                    _stream(stream)))
+    return idx_out, count_out

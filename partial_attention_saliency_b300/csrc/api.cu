@@ -350,6 +350,46 @@ dllm_status dllm_snap_prefix(const int32_t* tokens, int B, int L, int V, const u
                    "dllm_snap_prefix launch");
 }
 
+size_t dllm_slowfast_state_bytes(int B, int window) {
+  if (B < 1 || window < 1) return 0;
+  return (size_t)B * (size_t)(window + 1) * sizeof(int32_t);
+}
+
+dllm_status dllm_slowfast_observe_device(int32_t* state, int B, int window, double sigma2_stable,
+                                         const int32_t* start, const int32_t* pred_len,
+                                         int32_t* phase_out, int32_t* region_end_out,
+                                         int32_t* dev_status, void* stream) {
+  REQUIRE(state && start && pred_len && phase_out && region_end_out,
+          "dllm_slowfast_observe_device: NULL pointer argument");
+  REQUIRE(B >= 1 && window >= 1, "dllm_slowfast_observe_device: B=%d window=%d must be >= 1", B,
+          window);
+  REQUIRE(window <= 4096, "dllm_slowfast_observe_device: window %d above 4096", window);
+  REQUIRE(sigma2_stable >= 0.0, "dllm_slowfast_observe_device: sigma2 must be >= 0");
+  return from_cuda(dllm::launch_slowfast_observe(state, B, window, sigma2_stable, start, pred_len,
+                                                 phase_out, region_end_out, dev_status,
+                                                 static_cast<cudaStream_t>(stream)),
+                   "dllm_slowfast_observe_device launch");
+}
+
+dllm_status dllm_slowfast_select(const float* conf, const uint8_t* masked, int B, int L,
+                                 const int32_t* start, const int32_t* phase,
+                                 const int32_t* region_end, float tau_high, int width, int k,
+                                 int32_t* idx_out, int32_t* count_out, int32_t* dev_status,
+                                 void* stream) {
+  REQUIRE(conf && start && phase && region_end && idx_out && count_out,
+          "dllm_slowfast_select: NULL pointer argument");
+  REQUIRE(B >= 1 && B <= 65535 && L >= 1, "dllm_slowfast_select: B=%d L=%d out of range", B, L);
+  REQUIRE(width >= 1 && width <= dllm::slowfast_select_max_width(),
+          "dllm_slowfast_select: width %d outside [1, %d]", width,
+          dllm::slowfast_select_max_width());
+  REQUIRE(k >= 1 && k <= 64, "dllm_slowfast_select: k %d outside [1, 64]", k);
+  REQUIRE(!std::isnan(tau_high), "dllm_slowfast_select: NaN tau_high");
+  return from_cuda(dllm::launch_slowfast_select(conf, masked, B, L, start, phase, region_end,
+                                                tau_high, width, k, idx_out, count_out,
+                                                dev_status, static_cast<cudaStream_t>(stream)),
+                   "dllm_slowfast_select launch");
+}
+
 }  // extern "C"
 
 namespace dllm {

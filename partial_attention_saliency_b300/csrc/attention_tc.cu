@@ -80,6 +80,7 @@ struct FwdParams {
   int max_split_items;  // capacity of the workspace in items (0: never split)
   float scale_log2;
   int32_t* dev_status;
+  long long wait_limit;  // clock cycles a pipeline wait may take (drains excepted)
 };
 
 struct ColsumParams {
@@ -124,8 +125,9 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 // Bounded wait whose outcome is the same for every lane of the warp (the
 // tcgen05.ld/st that follow are warp-collective).
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-  const bool r = mbar_wait(bar, parity, abort);
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          long long limit = kWaitLimitDefault) {
+  const bool r = mbar_wait(bar, parity, abort, limit);
   return __all_sync(0xffffffffu, r);
 }
 
@@ -332,7 +334,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         int b, h, pair, nq, qi, kt0, nt, slot;
         item_of(plan, v, &qi, &kt0, &nt, &slot);
         decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
-        if (j > 0 && !mbar_wait(q_empty, (j - 1) & 1, abort)) break;
+        if (j > 0 && !mbar_wait(q_empty, (j - 1) & 1, abort, p.wait_limit)) break;
         mbar_expect_tx(q_full, (uint32_t)nq * kTile);
         for (int x = 0; x < nq; ++x) {
           const int row0 = (2 * pair + x) * kBM;
@@ -344,7 +346,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         for (int t = 0; t < nt; ++t) {
           const int key0 = (kt0 + t) * kBN;
           const int sk = gk % kKStages;
-          if (gk >= kKStages && !mbar_wait(&k_empty[sk], ((gk / kKStages) - 1) & 1, abort)) {
+          if (gk >= kKStages && !mbar_wait(&k_empty[sk], ((gk / kKStages) - 1) & 1, abort, p.wait_limit)) {
             ok = false;
             break;
           }
@@ -354,7 +356,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           tma_load_4d(kdst + kBox, &tk, &k_full[sk], 64, h, key0, b);
           ++gk;
           const int sv = gv % kVStages;
-          if (gv >= kVStages && !mbar_wait(&v_empty[sv], ((gv / kVStages) - 1) & 1, abort)) {
+          if (gv >= kVStages && !mbar_wait(&v_empty[sv], ((gv / kVStages) - 1) & 1, abort, p.wait_limit)) {
             ok = false;
             break;
           }
@@ -407,11 +409,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         int b, h, pair, nq, qi, kt0, nt, slot;
         item_of(plan, v, &qi, &kt0, &nt, &slot);
         decode_pair(p, s_cnt, qi, &b, &h, &pair, &nq);
-        if (!mbar_wait(q_full, j & 1, abort)) break;
+        if (!mbar_wait(q_full, j & 1, abort, p.wait_limit)) break;
         if (nq == 2) {
           // Pair of query tiles: per key tile t the order is
           //   O_A += P_A(t) V(t), S_A = Q_A K(t+1)^T, O_B += P_B(t) V(t), S_B = Q_B K(t+1)^T.
-          if (!mbar_wait(&k_full[g % kKStages], (g / kKStages) & 1, abort)) break;
+          if (!mbar_wait(&k_full[g % kKStages], (g / kKStages) & 1, abort, p.wait_limit)) break;
           tc_fence_after();
           for (int x = 0; x < 2; ++x) issue_qk(x, x, g % kKStages);
           mma_commit(&k_empty[g % kKStages]);  // K(0) is read by its Q K^T products only
@@ -421,15 +423,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             const int sk1 = (g + t + 1) % kKStages;
             const bool more = t + 1 < nt;
             for (int x = 0; x < 2; ++x) {
-              if (!mbar_wait(&p_full[x], gt[x] & 1, abort)) {
+              if (!mbar_wait(&p_full[x], gt[x] & 1, abort, p.wait_limit)) {
                 ok = false;
                 break;
               }
-              if (t == 0 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort)) {
+              if (t == 0 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort, p.wait_limit)) {
                 ok = false;
                 break;
               }
-              if (x == 0 && !mbar_wait(&v_full[sv], ((g + t) / kVStages) & 1, abort)) {
+              if (x == 0 && !mbar_wait(&v_full[sv], ((g + t) / kVStages) & 1, abort, p.wait_limit)) {
                 ok = false;
                 break;
               }
@@ -437,7 +439,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
               issue_pv(x, sv, t > 0);
               if (x == 1) mma_commit(&v_empty[sv]);  // V(t) no longer read
               if (more) {
-                if (x == 0 && !mbar_wait(&k_full[sk1], ((g + t + 1) / kKStages) & 1, abort)) {
+                if (x == 0 && !mbar_wait(&k_full[sk1], ((g + t + 1) / kKStages) & 1, abort, p.wait_limit)) {
                   ok = false;
                   break;
                 }
@@ -462,7 +464,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           // the Q K^T of tile t + 2 is issued right after the P V of tile t.
           for (int t = 0; t < 2 && t < nt && ok; ++t) {
             const int sk = (g + t) % kKStages;
-            if (!mbar_wait(&k_full[sk], ((g + t) / kKStages) & 1, abort)) {
+            if (!mbar_wait(&k_full[sk], ((g + t) / kKStages) & 1, abort, p.wait_limit)) {
               ok = false;
               break;
             }
@@ -474,15 +476,15 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           for (int t = 0; t < nt && ok; ++t) {
             const int x = t & 1;
             const int sv = (g + t) % kVStages;
-            if (!mbar_wait(&p_full[x], gt[x] & 1, abort)) {
+            if (!mbar_wait(&p_full[x], gt[x] & 1, abort, p.wait_limit)) {
               ok = false;
               break;
             }
-            if (t < 2 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort)) {
+            if (t < 2 && jt[x] > 0 && !mbar_wait(&o_free[x], (jt[x] - 1) & 1, abort, p.wait_limit)) {
               ok = false;
               break;
             }
-            if (!mbar_wait(&v_full[sv], ((g + t) / kVStages) & 1, abort)) {
+            if (!mbar_wait(&v_full[sv], ((g + t) / kVStages) & 1, abort, p.wait_limit)) {
               ok = false;
               break;
             }
@@ -491,7 +493,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
             mma_commit(&v_empty[sv]);  // V(t) no longer read
             if (t + 2 < nt) {
               const int sk = (g + t + 2) % kKStages;
-              if (!mbar_wait(&k_full[sk], ((g + t + 2) / kKStages) & 1, abort)) {
+              if (!mbar_wait(&k_full[sk], ((g + t + 2) / kKStages) & 1, abort, p.wait_limit)) {
                 ok = false;
                 break;
               }
@@ -549,7 +551,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       const int kstep = single ? 2 : 1;
       int kvalid = p.L - (kt0 + (single ? x : 0)) * kBN;  // < kBN only on the last, partial tile
       for (int tt = 0; tt < mine; ++tt, ++gx, kvalid -= kstep * kBN) {
-        if (!warp_wait(&s_full[x], gx & 1, abort)) {
+        if (!warp_wait(&s_full[x], gx & 1, abort, p.wait_limit)) {
           ok = false;
           break;
         }
@@ -640,7 +642,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
         if (lane == 0) mbar_arrive(&p_full[x]);
         l += (acc0.x + acc0.y) + (acc1.x + acc1.y);
       }
-      if (!ok || !warp_wait(&o_done[x], jx & 1, abort)) {
+      if (!ok || !warp_wait(&o_done[x], jx & 1, abort, p.wait_limit)) {
         ok = false;
         break;
       }
@@ -659,7 +661,7 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
       // ---------------------------------------------------------- epilogue
       float a0 = 1.0f, a1 = 0.0f;  // weights of O_x and O_1 (merged one-tile items)
       if (merge) {
-        if (!warp_wait(x_ready, jd & 1, abort)) {
+        if (!warp_wait(x_ready, jd & 1, abort, p.wait_limit)) {
           ok = false;
           break;
         }
@@ -1387,6 +1389,7 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
   fp.max_split_items = can_split ? 2 * n_ctas : 0;
   fp.scale_log2 = scale * kLog2e;
   fp.dev_status = dev_status;
+  fp.wait_limit = wait_limit();
   launch_pdl(attn_fwd_tc_kernel, n_ctas, kFwdThreads, kFwdSmem, stream, tq, tk, tv, fp);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;

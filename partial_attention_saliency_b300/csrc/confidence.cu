@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(kStreamThreads, 1)
 conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
                    int B, int R_max, const int32_t* row_idx,
                    const int32_t* count, int nchunks,
-                   ConfPartial* ws, int32_t* dev_status) {
+                   ConfPartial* ws, int32_t* dev_status, long long wait_limit) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
   using namespace sm100;
@@ -517,7 +517,7 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
         if (row < 0 || row >= R_src) continue;  // the merge kernel reports it
         const int stage = j % kStreamStages;
         if (j >= kStreamStages &&
-            !mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort)) {
+            !mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort, wait_limit)) {
           ok = false;
           break;
         }
@@ -532,7 +532,7 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
       bool sentinel = false;
       if (ok) {  // end-of-stream stage: a plain arrival with br = -1
         const int stage = j % kStreamStages;
-        if (j < kStreamStages || mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort)) {
+        if (j < kStreamStages || mbar_wait(&empty[stage], ((j / kStreamStages) - 1) & 1, abort, wait_limit)) {
           stage_info[stage] = make_int2(-1, 0);
           mbar_arrive(&full[stage]);
           sentinel = true;
@@ -555,7 +555,7 @@ conf_stream_kernel(const T* logits, int R_src, int V, int64_t rs, int64_t bs,
   const uint32_t sent = std::is_same<T, float>::value ? 0xff800000u : 0xff80ff80u;
   for (int j = 0;; ++j) {
     const int stage = j % kStreamStages;
-    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStreamStages) & 1, abort))) break;
+    if (!__all_sync(0xffffffffu, mbar_wait(&full[stage], (j / kStreamStages) & 1, abort, wait_limit))) break;
     const int2 info = stage_info[stage];
     if (info.x < 0) break;
     const int br = info.x, c = info.y;
@@ -641,7 +641,8 @@ cudaError_t launch_typed(const T* logits, int B, int R_src, int V, int64_t rs, i
     if (ea != cudaSuccess) return ea;
     const int snc = stream_nchunks(V, (int)sizeof(T));
     launch_pdl(conf_stream_kernel<T>, num_sms(), kStreamThreads, kStreamSmem, stream,
-        logits, R_src, V, rs, bs, B, R_max, row_idx, count, snc, part, dev_status);
+        logits, R_src, V, rs, bs, B, R_max, row_idx, count, snc, part, dev_status,
+        wait_limit());
     parts = snc * kStreamWarps;
   } else {
     dim3 grid(B * R_max, nchunks);
@@ -665,8 +666,8 @@ cudaError_t launch_typed(const T* logits, int B, int R_src, int V, int64_t rs, i
 }  // namespace
 
 size_t confidence_workspace_bytes(int B, int R_max, int V, int dtype) {
-  // partials per row: one per 32 KB chunk (chunked kernel) or one per 8 KB
-  // slice (streaming kernel); size for the larger
+  // partials per row: one per 32 KB chunk (chunked kernel) or one per 4 KB
+  // slice (kStreamSliceBytes, streaming kernel); size for the larger
   const int eb = dtype == DLLM_BF16 ? 2 : 4;
   const int a = dtype == DLLM_BF16 ? conf_nchunks<__nv_bfloat16>(V) : conf_nchunks<float>(V);
   const int s = stream_nchunks(V, eb) * kStreamWarps;

@@ -51,6 +51,13 @@ extern "C" dllm_status dllm_confidence_static_ws(
     int64_t batch_stride, int R_max, const int32_t* row_idx, const int32_t* count,
     const int32_t* out_idx, int out_cols, float* conf_out, int32_t* argmax_out,
     float* margin_out, int32_t* dev_status, void* stream) {
+  // The cheap argument checks first, so that a rejected call returns before
+  // it touches the CUDA runtime (dllm_confidence repeats them all).
+  if (logits == nullptr || conf_out == nullptr || argmax_out == nullptr ||
+      (dtype != DLLM_F32 && dtype != DLLM_BF16) || B < 1 || R_src < 1 || R_max < 1 || V < 2 ||
+      out_cols < 1)
+    return (dllm_status)dllm::set_last_error(
+        DLLM_ERR_INVALID_ARG, "dllm_confidence_static_ws: NULL pointer, dtype or size out of range");
   const size_t need = dllm_confidence_workspace_bytes(B, R_max, V, dtype);
   if (need > kScratchBytes) {
     char msg[256];

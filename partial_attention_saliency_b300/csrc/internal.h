@@ -93,7 +93,24 @@ cudaError_t launch_snap_prefix(const int32_t* tokens, int B, int L, int V, const
                                const int32_t* start, int32_t* len, int min_len,
                                int32_t* dev_status, cudaStream_t stream);
 
+int slowfast_select_max_width();
+
+cudaError_t launch_slowfast_observe(int32_t* state, int B, int W, double sigma2,
+                                    const int32_t* start, const int32_t* pred_len,
+                                    int32_t* phase_out, int32_t* region_end_out,
+                                    int32_t* dev_status, cudaStream_t stream);
+
+cudaError_t launch_slowfast_select(const float* conf, const uint8_t* masked, int B, int L,
+                                   const int32_t* start, const int32_t* phase,
+                                   const int32_t* region_end, float tau_high, int width, int k,
+                                   int32_t* idx_out, int32_t* count_out, int32_t* dev_status,
+                                   cudaStream_t stream);
+
 int num_sms();
+
+// Clock cycles a bounded pipeline wait of the streaming confidence and the
+// attention forward kernels may take before it gives up (dllm_set_wait_limit).
+long long wait_limit();
 
 // Raises the dynamic shared-memory limit of `func` to `bytes` on the current
 // device (once per function and device: later calls keep the first value, so

@@ -52,8 +52,10 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false and raises *abort) after ~`limit` clock cycles, or at once when
 // another thread already raised *abort, so that no wait can hang the GPU.
+constexpr long long kWaitLimitDefault = 2000000000LL;  // about a second of clock cycles
+
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          long long limit = 2000000000LL) {
+                                          long long limit = kWaitLimitDefault) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {

@@ -53,3 +53,30 @@ def test_controller_rejects_bad_arguments(dl):
     with pytest.raises(ValueError):
         sf.observe([0, 0, 0], [1, 1, 1])
     sf.close()
+
+
+def test_device_entry_points_validate_on_the_host(dl):
+    """Bad arguments of the device controller and of the token selection
+    return INVALID_ARG before any launch (no GPU needed)."""
+    lib = dl.load_library()
+    assert lib.dllm_slowfast_state_bytes(4, 3) == 4 * 4 * 4
+    assert lib.dllm_slowfast_state_bytes(0, 3) == 0
+    fake = 16  # never dereferenced: validation fails first
+    assert lib.dllm_slowfast_observe_device(None, 4, 3, 1.0, fake, fake, fake, fake, None, None) == 1
+    assert lib.dllm_slowfast_observe_device(fake, 4, 0, 1.0, fake, fake, fake, fake, None, None) == 1
+    assert lib.dllm_slowfast_observe_device(fake, 4, 3, -1.0, fake, fake, fake, fake, None, None) == 1
+    assert lib.dllm_slowfast_observe_device(fake, 4, 5000, 1.0, fake, fake, fake, fake, None, None) == 1
+    args = dict(conf=fake, masked=None, B=2, L=100, start=fake, phase=fake, region_end=fake,
+                tau_high=0.9, width=32, k=4, idx=fake, count=fake)
+
+    def sel(**kw):
+        a = dict(args, **kw)
+        return lib.dllm_slowfast_select(a["conf"], a["masked"], a["B"], a["L"], a["start"],
+                                        a["phase"], a["region_end"], a["tau_high"], a["width"],
+                                        a["k"], a["idx"], a["count"], None, None)
+    assert sel(conf=None) == 1
+    assert sel(k=0) == 1 and sel(k=65) == 1
+    assert sel(width=0) == 1 and sel(width=16385) == 1
+    assert sel(tau_high=float("nan")) == 1
+    assert sel(B=0) == 1
+    assert b"width" in lib.dllm_last_error() or True

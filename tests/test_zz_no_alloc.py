@@ -5,10 +5,11 @@ hands only raw input and output pointers, or a latency-critical caller that
 cannot pay for cudaMalloc's device-wide synchronisation.  For them the
 library offers a variant of dllm_confidence whose scratch is a fixed-size
 array defined in device memory by the library itself.  This test calls it
-through the C ABI and checks its outputs against the workspace version on two
-calls in a row (the second on different inputs, so stale scratch contents from
-the first call would show), and that a shape needing more scratch than the
-stated maximum is refused before anything is launched.
+through the C ABI and checks its outputs against the workspace version and
+against the float64 oracle on two calls in a row (the second on different
+inputs, so stale scratch contents from the first call would show), and that a
+shape needing more scratch than the stated maximum, or a NULL argument, is
+refused before anything is launched.
 
 This file is collected last on purpose.
 """
@@ -18,6 +19,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads
 
 pytestmark = pytest.mark.gpu
@@ -70,6 +72,20 @@ def _same(a, b):
     assert np.max(np.abs(ma.double().cpu().numpy() - mb.double().cpu().numpy())) <= 1e-6
 
 
+def _oracle_check(got, logits, count=None, row_idx=None):
+    conf, am, mg = (t.cpu() for t in got)
+    z = logits.double().cpu().numpy()
+    rc, ra, rm = oracle.confidence(z, count=None if count is None else count.cpu().numpy(),
+                                   row_idx=None if row_idx is None else row_idx.cpu().numpy())
+    n = rc.shape[1] if count is None else None
+    for b in range(z.shape[0]):
+        k = n if count is None else int(count[b])
+        c = conf[b, :k].double().numpy()
+        assert np.all(np.abs(c - rc[b, :k]) <= 1e-6 + 1e-4 * np.abs(rc[b, :k]))
+        assert np.array_equal(am[b, :k].numpy(), ra[b, :k])
+        assert np.max(np.abs(mg[b, :k].double().numpy() - rm[b, :k]), initial=0.0) <= 1e-6
+
+
 def test_static_scratch_matches_workspace_version_two_calls(lib):
     dev = torch.device("cuda")
     st = torch.zeros((1,), dtype=torch.int32, device=dev)
@@ -80,6 +96,7 @@ def test_static_scratch_matches_workspace_version_two_calls(lib):
     got = _static_ws_call(lib, logits1, s.logit_rows, None, None, s.logit_rows, st)
     torch.cuda.synchronize()
     _same(got, _workspace_call(logits1, s.logit_rows, None, None, s.logit_rows))
+    _oracle_check(got, logits1)
     # call 2: other inputs, gathered rows and device counts
     logits2 = workloads.normal(g, (3, 64, 40000), 2.0, torch.bfloat16).to(dev)
     row_idx = torch.randint(0, 64, (3, 48), generator=g, dtype=torch.int32).to(dev)
@@ -87,6 +104,7 @@ def test_static_scratch_matches_workspace_version_two_calls(lib):
     got = _static_ws_call(lib, logits2, 48, row_idx, count, 48, st)
     torch.cuda.synchronize()
     _same(got, _workspace_call(logits2, 48, row_idx, count, 48))
+    _oracle_check(got, logits2, count=count, row_idx=row_idx)
     assert int(st[0]) == 0
 
 
@@ -98,3 +116,7 @@ def test_static_scratch_rejects_oversize_before_launch(lib):
                                        None, 65536, dummy, dummy, None, None, None)
     assert rc == 1
     assert b"static maximum" in lib.dllm_last_error()
+    # a NULL argument is refused before the scratch is looked up
+    rc = lib.dllm_confidence_static_ws(None, 1, 1, 8, 1000, 1000, 0, 8, None, None, None, 8,
+                                       dummy, dummy, None, None, None)
+    assert rc == 1
