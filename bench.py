@@ -102,7 +102,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload",
-                    choices=["loop_b4_2k_128", "step_1k", "batch8_2k", "long_4k",
+                    choices=["loop_b4_2k_128", "around_b4_2k", "step_1k", "batch8_2k", "long_4k",
                              "long_4k_schedule", "loop_b4_2k"],
                     default="loop_b4_2k_128")
     ap.add_argument("--frac", type=float, default=0.25,
@@ -1060,6 +1060,135 @@ def loop_e2e(lp, sh, steps, pools, dpools, counts, cap_rows, run, stream, pg, de
             "sample": f"the loop's steps 0-{E - 1} from pinned host buffers, {n_steps // E} times"}
 
 
+# ----------------------------------------------------------------------------- around the step
+
+FP32_SIMT_PEAK_TFLOPS = 148 * 128 * 2 * 2.032e9 / 1e12  # SMs x FP32 lanes x 2 (FMA) x max clock
+
+
+def main_around(args, rank, world, device, pg):
+    """The calls that run around the step, each timed alone (a graph of 20
+    calls, median of 15 replays), on the state of the 128-step loop's step 1
+    (batch 4, L 2048, the step's active rows): DyLLM's stable-row update
+    (every position not active this step is a stable row, the active ones
+    the salient columns), Attn-Sampler's total attention and order,
+    SlowFast's device controller and token selection, SureLock's lock
+    criterion (this step's logit rows against another step's).  Prints one
+    line whose value is the step's active rows per second through these
+    calls together, with the per-call breakdown."""
+    import partial_attention_saliency_b300 as dl
+    dl.load_library()
+    sh = workloads.LOOP_128
+    pools = workloads.make_loop_pools(sh)
+    dp = {k: v.to(device) for k, v in pools.items()}
+    cap = workloads.loop_row_cap(sh)
+    lp = dl.BlockDecodeLoop(sh.B, sh.L, sh.H, sh.d, sh.V, sh.dtype, sh.prompt, cap, sh.tau,
+                            sh.tau_c, device=device)
+    lp.reset(dp["k_cache"], dp["v_cache"])
+    st0, st1 = (workloads.loop_step_inputs(sh, dp, t, cap) for t in range(2))
+    for st in (st0, st1):
+        lp.step(st["cur"], dp["prev"], st["q"], st["k_new"], st["v_new"], st["logits"],
+                st["win_start"])
+    torch.cuda.synchronize()
+    counts = lp.count.cpu().tolist()
+    M = sum(counts)
+    Lw = sh.L - st1["win_start"]
+    idx = lp.idx(Lw)
+    B, L, H, d, V = sh.B, sh.L, sh.H, sh.d, sh.V
+    g = torch.Generator(device=device).manual_seed(9)
+    rnd = lambda *shape: torch.randn(shape, generator=g, device=device).to(sh.dtype)  # noqa: E731
+    q_prev, v_prev, o = rnd(B, L, H, d), rnd(B, L, H, d), rnd(B, L, H, d)
+    lse_prev = torch.randn((B, H, L), generator=g, device=device) + 8.0
+    stable = torch.ones((B, L), dtype=torch.bool, device=device)
+    for b in range(B):
+        stable[b, idx[b, :counts[b]].long()] = False
+    stable_idx = torch.full((B, L), -1, dtype=torch.int32, device=device)
+    stable_count = stable.sum(1).to(torch.int32)
+    for b in range(B):
+        pos = torch.nonzero(stable[b]).flatten().to(torch.int32)
+        stable_idx[b, :pos.numel()] = pos
+    N = int(stable_count.sum())
+    masked = (~torch.isinf(lp.score)).to(torch.uint8)
+    sf = dl.SlowFastDevice(B, 3, 2.0, device=device)
+    plen = torch.full((B,), 8, dtype=torch.int32, device=device)
+    logits_prev = st0["logits"]
+    lock_ws = torch.empty((max(dl.dllm_lock_workspace_bytes(B, Lw, V, sh.dtype), 16),),
+                          dtype=torch.uint8, device=device)
+    kl = torch.empty((B, L), device=device)
+    unc = torch.empty((B, L), device=device)
+    flags = torch.zeros((B, L), dtype=torch.uint8, device=device)
+    score = torch.empty((B, L), device=device)
+    status = torch.zeros((1,), dtype=torch.int32, device=device)
+    el = 2
+    calls = {
+        "dllm_approx_attention_update": (
+            lambda: dl.dllm_approx_attention_update(q_prev, lse_prev, lp.k_cache, v_prev,
+                                                    st1["v_new"], idx, lp.count, stable_idx,
+                                                    stable_count, o, dev_status=status),
+            H * (N * (3 * d * el + 4) + M * 3 * d * el), 4.0 * d * N * M / B * H, "alu"),
+        "dllm_attn_scores": (lambda: dl.dllm_attn_scores(lp.colsum, score_inout=score),
+                             B * H * L * 4 + B * L * 4, 0.0, "hbm"),
+        "dllm_attn_sampler_select": (
+            lambda: dl.dllm_attn_sampler_select(score, candidates=masked, tau=0.0, gamma=0.5,
+                                                k_max=8), B * L * 9 + B * 4, 0.0, "latency"),
+        "dllm_slowfast_observe_device": (lambda: sf.observe(lp.start, plen), B * 40, 0.0,
+                                         "latency"),
+        "dllm_slowfast_select": (
+            lambda: dl.dllm_slowfast_select(lp.score, lp.start, sf.phase, sf.region_end, 0.9,
+                                            64, 4, masked=masked), B * L * 9, 0.0, "latency"),
+        "dllm_lock_criterion": (
+            lambda: dl.dllm_lock_criterion(st1["logits"], logits_prev, 1e-3, gate_q=0.5,
+                                           R_max=Lw, count=lp.count, out_idx=idx, out_cols=L,
+                                           kl_out=kl, unc_out=unc, locked_inout=flags, ws=lock_ws,
+                                           dev_status=status),
+            M * (2 * V * el + 17), 0.0, "hbm"),
+    }
+    pk = peaks()
+    kernels, total_ms = {}, 0.0
+    cap_stream = torch.cuda.Stream(device)
+    for name, (fn, byts, flops, bound) in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=cap_stream):
+            for _ in range(20):
+                fn()
+        ms = statistics.median(time_regions(gr.replay, torch.cuda.current_stream(device),
+                                            est_ms=1.0, warm=gr.replay, min_seconds=0.2,
+                                            min_reps=15)) / 20
+        total_ms += ms
+        k = {"us": ms * 1e3, "alg_bytes": byts, "GB/s": byts / (ms / 1e3) / 1e9, "bound": bound}
+        if bound == "alu":
+            k.update({"alg_flops": flops, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+                      "peak_TFLOP/s": FP32_SIMT_PEAK_TFLOPS,
+                      "frac": flops / (ms / 1e3) / 1e12 / FP32_SIMT_PEAK_TFLOPS})
+        elif bound == "hbm":
+            k["frac"] = k["GB/s"] / pk["hbm_gbs"]
+        kernels[name] = k
+    torch.cuda.synchronize()
+    assert int(status[0]) == 0, "device-side check failed"
+    dom = max(kernels, key=lambda n: kernels[n]["us"])
+    dk = kernels[dom]
+    if dk["bound"] == "alu":
+        roof = {"bound": "alu", "achieved": dk["TFLOP/s"], "peak": FP32_SIMT_PEAK_TFLOPS,
+                "unit": "TFLOP/s", "frac": dk["frac"], "traffic": None, "kernel": dom,
+                "peak_source": "derived: 148 SMs x 128 FP32 lanes x 2 flops x 2032 MHz"}
+    else:
+        roof = {"bound": "hbm", "achieved": dk["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": dk["frac"], "traffic": None, "kernel": dom,
+                "peak_source": pk["source"] + " (burst)"}
+    line = {"metric": METRIC, "value": M / (total_ms / 1e3), "unit": UNIT, "n_gpus": world,
+            "steps": 1, "warmup": args.warmup, "ms_per_step": total_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "the calls around one step of the batch-4 L 2048 loop (step "
+                                   f"1: {M} active rows, {N} stable rows), each timed alone",
+                       "name": "around_b4_2k", "active_rows": M, "stable_rows": N},
+            "roofline": roof, "kernels": kernels,
+            "timing": "each call: median of 15 replays of a graph of 20 calls / 20"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -1083,6 +1212,8 @@ def main():
 
     if args.workload == "loop_b4_2k_128":
         return main_loop(args, rank, world, device, pg)
+    if args.workload == "around_b4_2k":
+        return main_around(args, rank, world, device, pg)
 
     import partial_attention_saliency_b300 as dl
     dl.load_library()

@@ -252,8 +252,9 @@ dllm_status dllm_lock_criterion(const void* logits_cur, const void* logits_prev,
   REQUIRE(row_stride >= V, "dllm_lock_criterion: row_stride %lld < V", (long long)row_stride);
   REQUIRE(B == 1 || batch_stride >= (int64_t)R_src * row_stride,
           "dllm_lock_criterion: batch_stride too small");
-  REQUIRE(row_idx != nullptr || R_max <= R_src,
-          "dllm_lock_criterion: R_max > R_src without row_idx");
+  // as in dllm_confidence: rows past R_src without row_idx are caught on the device
+  REQUIRE(row_idx != nullptr || count != nullptr || R_max <= R_src,
+          "dllm_lock_criterion: R_max > R_src without row_idx or count");
   REQUIRE(out_cols >= 1 && (out_idx != nullptr || R_max <= out_cols),
           "dllm_lock_criterion: out_cols %d too small", out_cols);
   REQUIRE(locked_inout == nullptr || R_max <= 16384,
