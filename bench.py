@@ -1070,7 +1070,8 @@ def main_around(args, rank, world, device, pg):
     calls, median of 15 replays), on the state of the 128-step loop's step 1
     (batch 4, L 2048, the step's active rows): DyLLM's stable-row update
     (every position not active this step is a stable row, the active ones
-    the salient columns), Attn-Sampler's total attention and order,
+    the salient columns; tensor cores, HBM-bound by its arithmetic
+    intensity of about 77 flop/B), Attn-Sampler's total attention and order,
     SlowFast's device controller and token selection, SureLock's lock
     criterion (this step's logit rows against another step's).  Prints one
     line whose value is the step's active rows per second through these
@@ -1124,7 +1125,7 @@ def main_around(args, rank, world, device, pg):
             lambda: dl.dllm_approx_attention_update(q_prev, lse_prev, lp.k_cache, v_prev,
                                                     st1["v_new"], idx, lp.count, stable_idx,
                                                     stable_count, o, dev_status=status),
-            H * (N * (3 * d * el + 4) + M * 3 * d * el), 4.0 * d * N * M / B * H, "alu"),
+            H * (N * (3 * d * el + 4) + M * 3 * d * el), 4.0 * d * N * M / B * H, "hbm"),
         "dllm_attn_scores": (lambda: dl.dllm_attn_scores(lp.colsum, score_inout=score),
                              B * H * L * 4 + B * L * 4, 0.0, "hbm"),
         "dllm_attn_sampler_select": (
@@ -1163,6 +1164,9 @@ def main_around(args, rank, world, device, pg):
                       "frac": flops / (ms / 1e3) / 1e12 / FP32_SIMT_PEAK_TFLOPS})
         elif bound == "hbm":
             k["frac"] = k["GB/s"] / pk["hbm_gbs"]
+            if flops:
+                k.update({"alg_flops": flops, "TFLOP/s": flops / (ms / 1e3) / 1e12,
+                          "tensor_frac": flops / (ms / 1e3) / 1e12 / pk["bf16_tflops"]})
         kernels[name] = k
     torch.cuda.synchronize()
     assert int(status[0]) == 0, "device-side check failed"

@@ -17,7 +17,9 @@
 //                       shared memory, each thread computes a 4 x 4 block of
 //                       S and of P, then a 4 x (d/16) block of P dV is added
 //                       to its accumulators.  FMA-pipe (SIMT) arithmetic in
-//                       float32.
+//                       float32; float32 inputs and head dims 32 and 64 (bf16
+//                       with head dim 128 runs on the tensor cores,
+//                       approx_update_tc.cu).
 #include <type_traits>
 
 #include "common.cuh"
@@ -267,6 +269,10 @@ cudaError_t launch_approx_attention_update(const void* q, const float* lse, cons
                                            const int32_t* stable_idx,
                                            const int32_t* stable_count, float scale, void* o,
                                            int32_t* dev_status, cudaStream_t stream) {
+  // bf16 with head dim 128: the tensor-core kernel (approx_update_tc.cu)
+  if (approx_update_tc_supported(dtype, d, q, k, v, v_new, o))
+    return launch_approx_update_tc(q, lse, k, v, v_new, B, L, H, M_max, idx, count, N_max,
+                                   stable_idx, stable_count, scale, o, dev_status, stream);
   if (dtype == DLLM_BF16)
     return launch_au_d<__nv_bfloat16>(d, q, lse, k, v, v_new, B, L, H, M_max, idx, count, N_max,
                                       stable_idx, stable_count, scale, o, dev_status, stream);

@@ -89,6 +89,16 @@ cudaError_t launch_approx_attention_update(const void* q, const float* lse, cons
                                            const int32_t* stable_count, float scale, void* o,
                                            int32_t* dev_status, cudaStream_t stream);
 
+bool approx_update_tc_supported(int dtype, int d, const void* q, const void* k, const void* v,
+                                const void* v_new, const void* o);
+
+cudaError_t launch_approx_update_tc(const void* q, const float* lse, const void* k, const void* v,
+                                    const void* v_new, int B, int L, int H, int M_max,
+                                    const int32_t* idx, const int32_t* count, int N_max,
+                                    const int32_t* stable_idx, const int32_t* stable_count,
+                                    float scale, void* o, int32_t* dev_status,
+                                    cudaStream_t stream);
+
 cudaError_t launch_snap_prefix(const int32_t* tokens, int B, int L, int V, const uint8_t* delim,
                                const int32_t* start, int32_t* len, int min_len,
                                int32_t* dev_status, cudaStream_t stream);

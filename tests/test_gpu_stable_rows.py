@@ -145,3 +145,40 @@ def test_update_edge_cases(dl):
     bad[0, 0] = L + 5
     out = _run(dl, q, lse, k, v, v_new, idx, count, bad, s_count, o, st=st)
     assert int(st[0]) != 0
+
+
+@pytest.mark.parametrize("counts", [[1, 129], [128, 0], [257, 64]])
+def test_update_bf16_tensor_cores_ragged(dl, counts):
+    """bf16 with head dim 128 (the tensor-core kernel): salient counts on
+    both sides of the 128-column passes, a batch row with none, stable lists
+    that leave rows out and end in a ragged tile; against the oracle, rows
+    outside the lists bitwise unchanged, and the exact identity when only
+    values change."""
+    g = torch.Generator().manual_seed(sum(counts))
+    B, L, H, d = 2, 700, 4, 128
+    bf = torch.bfloat16
+    q, k, v = (torch.randn((B, L, H, d), generator=g).to(bf) for _ in range(3))
+    o_ref, lse_ref, _ = oracle.partial_attention(f64(q), f64(k), f64(v), [L] * B)
+    o = torch.from_numpy(o_ref).to(bf)
+    lse = torch.from_numpy(lse_ref).float()
+    idx, count, stable, s_count = _sets(g, B, L, counts, 300, 450)
+    v_new = torch.randn((B, 300, H, d), generator=g).to(bf)
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    out = _run(dl, q, lse, k, v, v_new, idx, count, stable, s_count, o, st=st)
+    assert int(st[0]) == 0
+    ref = oracle.approx_attention_update(f64(o), f64(q), f64(lse), f64(k), f64(v), f64(v_new),
+                                         idx.numpy(), count.numpy(), stable.numpy(),
+                                         s_count.numpy())
+    got = f64(out)
+    assert np.all(np.abs(got - ref) <= BF16_ATOL + BF16_RTOL * np.abs(ref)), np.max(np.abs(got - ref))
+    assert _untouched(out, o, stable, s_count)
+    if counts[1] == 0:
+        assert torch.equal(out[1].cpu(), o[1])
+    # the identity: attention recomputed over the updated values (float64 on
+    # the same bf16 inputs), to within the bf16 rounding of the outputs
+    _, v_upd = oracle.kv_scatter(f64(k), f64(v), f64(k), f64(v_new), idx.numpy(), count.numpy())
+    o_exact, _, _ = oracle.partial_attention(f64(q), f64(k), v_upd, [L] * B)
+    for b in range(B):
+        rows = stable[b, :int(s_count[b])].numpy()
+        e = o_exact[b, rows]
+        assert np.all(np.abs(got[b, rows] - e) <= BF16_ATOL + BF16_RTOL * np.abs(e))
