@@ -113,6 +113,9 @@ def parse():
     ap.add_argument("--surelock", action="store_true",
                     help="long_4k, long_4k_schedule: add the lock criterion between this and "
                          "the previous step's logits of the active rows and the adaptive prefix")
+    ap.add_argument("--min-seconds", type=float, default=1.0,
+                    help="how long the timed region is repeated (median reported; at least 5 "
+                         "repetitions)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="approximate CPU time spent on the oracle baseline sample")
@@ -704,9 +707,9 @@ def reference_arm(args, rank):
 # ----------------------------------------------------------------------------- decoding loop
 
 LOOP_ORDER = ENTRY_ORDER  # the six calls of a loop step, in order
-LOOP_LAUNCHES_PER_STEP = 10  # cos_rows + compact, kv_scatter, attn_fwd + split merge,
-                             # colsum (persistent + key-tile-group), conf_stream + conf_merge,
-                             # stable_prefix
+LOOP_LAUNCHES_PER_STEP = 8  # cos_rows + compact, kv_scatter, attn_fwd (no workspace: no
+                            # split merge), attn_colsum_stream (no row above 2 query tiles),
+                            # conf_stream + conf_merge, stable_prefix
 
 
 def loop_desc(sh) -> str:
@@ -887,7 +890,8 @@ def main_loop(args, rank, world, device, pg):
     if pg: pg.barrier()
     torch.cuda.synchronize()
     clocks.start()
-    reps = time_regions(g_timed.replay, stream, est_ms=0.15 * K, warm=g_timed.replay)
+    reps = time_regions(g_timed.replay, stream, est_ms=0.15 * K, warm=g_timed.replay,
+                        min_seconds=args.min_seconds)
     clocks.stop()
     if pg: pg.barrier()
     g_events.replay()
@@ -997,7 +1001,7 @@ def loop_e2e(lp, sh, steps, pools, dpools, counts, cap_rows, run, stream, pg, de
     out = {"idx": torch.empty((sh.B * Lw_max,), dtype=torch.int32).pin_memory(),
            "count": torch.empty((sh.B,), dtype=torch.int32).pin_memory(),
            "o": torch.empty((sh.B, cap_rows, sh.H, sh.d), dtype=sh.dtype).pin_memory(),
-           "lse": torch.empty((sh.B * sh.H * Lw_max,), dtype=torch.float32).pin_memory(),
+           "lse": torch.empty((sh.B, sh.H, cap_rows), dtype=torch.float32).pin_memory(),
            "colsum": torch.empty((sh.B, sh.H, sh.L), dtype=torch.float32).pin_memory(),
            "score": torch.empty((sh.B, sh.L), dtype=torch.float32).pin_memory(),
            "argmax": torch.empty((sh.B, sh.L), dtype=torch.int32).pin_memory(),
@@ -1013,24 +1017,23 @@ def loop_e2e(lp, sh, steps, pools, dpools, counts, cap_rows, run, stream, pg, de
         # each batch row are contiguous; the batch rows are not)
         for b in range(sh.B):
             ds["cur"][b, w:].copy_(hs["cur"][b], non_blocking=True)
-            for k in ("q", "k_new", "v_new"):
+            for k in ("k_new", "v_new"):
                 ds[k][b, :cap_rows].copy_(hs[k][b], non_blocking=True)
+        ds["q"].copy_(hs["q"], non_blocking=True)
         ds["logits"].copy_(hs["logits"], non_blocking=True)
         run(t)
         out["idx"][:sh.B * Lw].copy_(lp.idx(Lw).view(-1), non_blocking=True)
         out["count"].copy_(lp.count, non_blocking=True)
-        o = lp.o(Lw)
-        for b in range(sh.B):
-            out["o"][b].copy_(o[b, :cap_rows], non_blocking=True)
-        out["lse"][:sh.B * sh.H * Lw].copy_(lp.lse(Lw).view(-1), non_blocking=True)
+        out["o"].copy_(lp.o, non_blocking=True)
+        out["lse"].copy_(lp.lse, non_blocking=True)
         for k, src in (("colsum", lp.colsum), ("score", lp.score), ("argmax", lp.argmax),
                        ("length", lp.length), ("start", lp.start)):
             out[k].copy_(src, non_blocking=True)
         h2d.append(sum(hs[k].numel() * hs[k].element_size()
                        for k in ("cur", "q", "k_new", "v_new", "logits")))
-        d2h.append(sh.B * Lw * 4 + sh.B * 4 + out["o"].numel() * 2 + sh.B * sh.H * Lw * 4
-                   + sum(out[k].numel() * out[k].element_size()
-                         for k in ("colsum", "score", "argmax", "length", "start")))
+        d2h.append(sh.B * Lw * 4 + sum(out[k].numel() * out[k].element_size()
+                                       for k in ("count", "o", "lse", "colsum", "score",
+                                                 "argmax", "length", "start")))
 
     lp.reset_positions()
     for t in range(E):
@@ -1280,7 +1283,7 @@ def main():
     torch.cuda.synchronize()
     clocks.start()
     reps = time_regions(lambda: [g_timed.replay() for _ in range(K // S)], stream,
-                        est_ms=0.1 * K, warm=g_timed.replay)
+                        est_ms=0.1 * K, warm=g_timed.replay, min_seconds=args.min_seconds)
     clocks.stop()
     if pg: pg.barrier()
     g_events.replay()

@@ -1422,6 +1422,7 @@ cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, 
     launch_pdl(attn_colsum_stream_kernel, sms, kCsThreads, kCsSmem, stream, tq, tk, cp, B);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (M_max <= kCsMaxQt * kBM) return cudaSuccess;  // no row can have more query tiles
     cp.min_qt = kCsMaxQt + 1;
   }
   // Key tiles per CTA: 4 (one query tile feeds four key tiles, four warps

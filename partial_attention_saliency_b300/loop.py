@@ -28,10 +28,13 @@ class BlockDecodeLoop:
     """Device state and buffers of the loop, allocated once.
 
     B batch rows of L positions, the first ``prompt`` of them committed from
-    the start; H x d heads; V vocabulary; ``row_cap`` logit rows per batch
-    row in a step's logit buffer (the most active rows a step can have);
-    ``tau`` the cosine threshold, ``tau_c`` the confidence a position needs to
-    be committed.
+    the start; H x d heads; V vocabulary; ``row_cap`` the most active rows a
+    step can have per batch row (the rows of a step's query and logit
+    buffers, and of the attention outputs); ``tau`` the cosine threshold,
+    ``tau_c`` the confidence a position needs to be committed.
+
+    The attention gets no workspace when B * H already covers half the SMs:
+    it then never splits the key range, so no merge launch follows it.
     """
 
     def __init__(self, B: int, L: int, H: int, d: int, V: int, dtype: torch.dtype,
@@ -53,8 +56,8 @@ class BlockDecodeLoop:
         # uses the first B * Lw rows of each as a contiguous [B, Lw, ...] view
         self._cos = torch.empty((B * L,), dtype=f32, device=dev)
         self._idx = torch.empty((B * L,), dtype=i32, device=dev)
-        self._o = torch.empty((B * L * H * d,), dtype=dtype, device=dev)
-        self._lse = torch.empty((B * H * L,), dtype=f32, device=dev)
+        self.o = torch.empty((B, row_cap, H, d), dtype=dtype, device=dev)
+        self.lse = torch.empty((B, H, row_cap), dtype=f32, device=dev)
         self.count = torch.zeros((B,), dtype=i32, device=dev)
         self.colsum = torch.empty((B, H, L), dtype=f32, device=dev)
         self.argmax = torch.zeros((B, L), dtype=i32, device=dev)
@@ -63,9 +66,11 @@ class BlockDecodeLoop:
         self.dev_status = torch.zeros((1,), dtype=i32, device=dev)
         cw = _lib.dllm_confidence_workspace_bytes(B, L, V, dtype)
         self.conf_ws = torch.empty((max(cw, 16),), dtype=torch.uint8, device=dev)
-        aw = max(_lib.dllm_attention_workspace_bytes(B, L, H, d, m, dtype)
-                 for m in (L - prompt, L))
-        self.attn_ws = torch.empty((max(aw, 16),), dtype=torch.uint8, device=dev)
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        self.attn_ws = None
+        if 2 * B * H < sms:
+            aw = _lib.dllm_attention_workspace_bytes(B, L, H, d, row_cap, dtype)
+            self.attn_ws = torch.empty((max(aw, 16),), dtype=torch.uint8, device=dev)
 
     # ------------------------------------------------------------------ views
     def cos(self, Lw: int) -> torch.Tensor:
@@ -73,12 +78,6 @@ class BlockDecodeLoop:
 
     def idx(self, Lw: int) -> torch.Tensor:
         return self._idx[:self.B * Lw].view(self.B, Lw)
-
-    def o(self, Lw: int) -> torch.Tensor:
-        return self._o[:self.B * Lw * self.H * self.d].view(self.B, Lw, self.H, self.d)
-
-    def lse(self, Lw: int) -> torch.Tensor:
-        return self._lse[:self.B * self.H * Lw].view(self.B, self.H, Lw)
 
     # ------------------------------------------------------------------ state
     def reset(self, k_cache: torch.Tensor, v_cache: torch.Tensor):
@@ -104,9 +103,10 @@ class BlockDecodeLoop:
         """Launch one partial step over the window [win_start, L).
 
         ``cur``/``prev`` [B, L, D] hidden states (only the window's rows are
-        read); ``q``/``k_new``/``v_new`` [B, Lw, H, d], row i the fresh row of
-        the i-th active position; ``logits`` [B, R, V] (R <= row_cap rows
-        allocated), row r the logits of the r-th active position.  Optional
+        read); ``k_new``/``v_new`` [B, Lw, H, d] and ``q`` [B, row_cap, H,
+        d], row i the fresh row of the i-th active position; ``logits``
+        [B, R, V] (R <= row_cap rows allocated), row r the logits of the r-th
+        active position.  Optional
         ``events`` (7) are recorded on the current stream around the six
         calls (pass ``stream=None`` with them).
         """
@@ -123,11 +123,11 @@ class BlockDecodeLoop:
         _lib.dllm_kv_scatter(self.k_cache, self.v_cache, k_new, v_new, idx, self.count,
                              dev_status=st, stream=stream)
         if ev: ev[2].record()
-        _lib.dllm_partial_attention(q, self.k_cache, self.v_cache, self.count, o_out=self.o(Lw),
-                                    lse_out=self.lse(Lw), with_colsum=False, ws=self.attn_ws,
+        _lib.dllm_partial_attention(q, self.k_cache, self.v_cache, self.count, o_out=self.o,
+                                    lse_out=self.lse, with_colsum=False, ws=self.attn_ws,
                                     dev_status=st, stream=stream)
         if ev: ev[3].record()
-        _lib.dllm_attention_colsum(q, self.k_cache, self.count, self.lse(Lw),
+        _lib.dllm_attention_colsum(q, self.k_cache, self.count, self.lse,
                                    colsum_out=self.colsum, dev_status=st, stream=stream)
         if ev: ev[4].record()
         _lib.dllm_confidence(logits, R_max=Lw, count=self.count, out_idx=idx, out_cols=self.L,

@@ -51,7 +51,8 @@ def test_step_inputs_layout():
     for t in (0, 1, 7):
         inp = workloads.loop_step_inputs(s, pools, t, cap)
         w = inp["win_start"]
-        assert inp["q"].shape == (s.B, s.L - w, s.H, s.d)
+        assert inp["q"].shape == (s.B, cap, s.H, s.d)
+        assert inp["k_new"].shape == (s.B, s.L - w, s.H, s.d)
         assert inp["logits"].shape == (s.B, cap, s.V)
         blo, bhi = workloads.loop_boosted(s, t)
         for b in range(s.B):

@@ -337,8 +337,9 @@ def loop_step_inputs(shape: LoopShape, pools: dict, s: int, row_cap: int,
 
     Only selection and indexing: the same pools give the same bits on the
     CPU and on a GPU.  ``cur`` [B, L, D]: ``hot`` at the planted positions,
-    ``cold`` elsewhere; ``q``/``k_new``/``v_new`` [B, Lw, H, d] (Lw = the
-    window's length): row i < count[b] is pool row (offset + i) mod
+    ``cold`` elsewhere; ``k_new``/``v_new`` [B, Lw, H, d] (Lw = the
+    window's length, the layout of the compacted indices) and ``q``
+    [B, row_cap, H, d]: row i < count[b] is pool row (offset + i) mod
     pool_rows, the rest zero; ``logits`` [B, row_cap, V]: row r < count[b] is
     logit-pool row (offset + r) mod pool_rows, from ``boost_pool`` when the
     r-th planted position lies in the boosted range, the rest zero.
@@ -354,9 +355,9 @@ def loop_step_inputs(shape: LoopShape, pools: dict, s: int, row_cap: int,
     for b in range(B):
         mask[b, planted[b]] = True
     cur = torch.where(mask.to(dev)[:, :, None], pools["hot"], pools["cold"])
-    q = torch.zeros((B, Lw, H, d), dtype=shape.dtype, device=dev)
-    k_new = torch.zeros_like(q)
-    v_new = torch.zeros_like(q)
+    q = torch.zeros((B, row_cap, H, d), dtype=shape.dtype, device=dev)
+    k_new = torch.zeros((B, Lw, H, d), dtype=shape.dtype, device=dev)
+    v_new = torch.zeros_like(k_new)
     logits = torch.zeros((B, row_cap, V), dtype=shape.dtype, device=dev)
     blo, bhi = loop_boosted(shape, s)
     for b in range(B):
