@@ -68,7 +68,8 @@ constexpr int kWarpMma = 9;
 // rate.  The column sums are not (measured faster with MUFU alone: their
 // FMA pipe is busy with the scaling and the sums).
 constexpr int kFwdPoly = 2;
-constexpr int kColsumPoly = 0;
+constexpr int kColsumPoly = 0;       // persistent column-sum kernel
+constexpr int kColsumGroupPoly = 0;  // key-tile-group kernel (2 or 3 of 8 measured slower)
 
 struct FwdParams {
   const int32_t* count;
@@ -995,28 +996,21 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
         break;
       }
       tc_fence_after();
+      // the S row in 8 chunks of 16 queries, two register buffers: the next
+      // chunk's scores load while this one is summed
+      auto add16 = [&](const uint32_t(&rw)[16], int c16) {
+        const float4* nl4 = reinterpret_cast<const float4*>(lb + c16 * 16);
 #pragma unroll
-      for (int c = 0; c < kBM / 32; ++c) {
-        uint32_t raw[32];
-        tmem_ld_32x32b_x32(tS + c * 32, raw);
-        tmem_ld_wait();
-        if (c == kBM / 32 - 1) {  // S_X is read: the next query tile may overwrite it
-          tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&s_free[x]);
-        }
-        const float4* nl4 = reinterpret_cast<const float4*>(lb + c * 32);
-#pragma unroll
-        for (int q4 = 0; q4 < 8; ++q4) {
+        for (int q4 = 0; q4 < 4; ++q4) {
           const float4 L4 = nl4[q4];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
             const int q = q4 * 4 + hh * 2;
             const float2 a = __ffma2_rn(
-                make_float2(__uint_as_float(raw[q]), __uint_as_float(raw[q + 1])), sl2x2,
+                make_float2(__uint_as_float(rw[q]), __uint_as_float(rw[q + 1])), sl2x2,
                 hh ? make_float2(L4.z, L4.w) : make_float2(L4.x, L4.y));
             float2 e;
-            if (((q >> 1) & 7) >= 8 - kColsumPoly) {
+            if ((((c16 * 16 + q) >> 1) & 7) >= 8 - kColsumGroupPoly) {
               e = exp2_poly2(a);
             } else {
               e.x = ex2_approx(a.x);
@@ -1028,6 +1022,24 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
               acc0 = __fadd2_rn(acc0, e);
           }
         }
+      };
+      uint32_t ra[16], rb[16];
+      tmem_ld_32x32b_x16(tS, ra);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < kBM / 16; c += 2) {
+        tmem_ld_32x32b_x16(tS + (c + 1) * 16, rb);
+        add16(ra, c);
+        tmem_ld_wait();
+        if (c + 2 < kBM / 16) {
+          tmem_ld_32x32b_x16(tS + (c + 2) * 16, ra);
+        } else {  // S_X is read: the next query tile may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[x]);
+        }
+        add16(rb, c + 1);
+        if (c + 2 < kBM / 16) tmem_ld_wait();
       }
       __syncwarp();  // lb is rewritten two tiles later
     }
@@ -1414,9 +1426,11 @@ cudaError_t launch_colsum_tc(const void* q, const void* k, int B, int L, int H, 
   const int64_t bh = (int64_t)B * H;
   const int sms = num_sms();
   cudaError_t e;
-  if (B <= kPlanMaxB) {
-    // batch rows with at most kCsMaxQt query tiles: the persistent kernel;
-    // the key-tile-group kernel below then takes only the larger ones
+  if (B <= kPlanMaxB && bh * nkt >= 4 * (int64_t)sms) {
+    // batch rows with at most kCsMaxQt query tiles: the persistent kernel
+    // (when there are at least four key tiles per SM to amortise its
+    // set-up); the key-tile-group kernel below then takes only the larger
+    // ones
     e = ensure_smem_limit(reinterpret_cast<const void*>(attn_colsum_stream_kernel), (int)kCsSmem);
     if (e != cudaSuccess) return e;
     launch_pdl(attn_colsum_stream_kernel, sms, kCsThreads, kCsSmem, stream, tq, tk, cp, B);
