@@ -829,7 +829,12 @@ def main_loop(args, rank, world, device, pg):
     dpools = {k: v.to(device) for k, v in pools.items()}
     cap_rows = workloads.loop_row_cap(sh)
     counts = workloads.loop_counts(sh).tolist()  # [T][B], the planted sets
-    steps = [workloads.loop_step_inputs(sh, dpools, t, cap_rows) for t in range(T)]
+    K = args.steps if args.steps is not None else T
+    W = args.warmup
+    # the inputs of every step the run touches (the timed K, the warm-up W,
+    # the first 8 for the end-to-end leg), each its own buffers
+    n_build = min(T, max(K, W, 8))
+    steps = [workloads.loop_step_inputs(sh, dpools, t, cap_rows) for t in range(n_build)]
     for st in steps:
         st.pop("planted")
     torch.cuda.synchronize()
@@ -842,10 +847,10 @@ def main_loop(args, rank, world, device, pg):
         lp.step(st["cur"], dpools["prev"], st["q"], st["k_new"], st["v_new"], st["logits"],
                 st["win_start"], events=events)
 
-    # one eager pass over the whole loop: every step selects its planted set
-    # and commits the block's next positions, so start ends at L
+    # one eager pass over the built steps: each selects its planted set and
+    # commits the block's next positions (over the whole loop start ends at L)
     lp.reset(dpools["k_cache"], dpools["v_cache"])
-    for t in range(T):
+    for t in range(n_build):
         run(t)
         if t < 8:
             torch.cuda.synchronize()
@@ -853,7 +858,8 @@ def main_loop(args, rank, world, device, pg):
             assert lp.length.cpu().tolist() == [sh.commit] * sh.B, (t, lp.length.cpu().tolist())
     torch.cuda.synchronize()
     assert int(lp.dev_status[0]) == 0, "device-side check failed"
-    assert lp.start.cpu().tolist() == [sh.L] * sh.B, lp.start.cpu().tolist()
+    assert lp.start.cpu().tolist() == [sh.prompt + sh.commit * n_build] * sh.B, \
+        lp.start.cpu().tolist()
 
     # ---------------------------------------------------------------- device-timed
     # The K timed steps (the loop's steps 0 .. K-1, restarting the loop from a
@@ -861,8 +867,6 @@ def main_loop(args, rank, world, device, pg):
     # first node resets score and start.  It is replayed once untimed, then
     # the K-step region is timed repeatedly for about a second (events on the
     # stream around each replay) and the median is reported.
-    K = args.steps if args.steps is not None else T
-    W = args.warmup
     cap = torch.cuda.Stream(device)
     g_warm = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_warm, stream=cap):

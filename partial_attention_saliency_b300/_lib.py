@@ -238,6 +238,8 @@ def dllm_partial_attention(q, k_cache, v_cache, count, *, scale: float = 0.0, o_
                            with_colsum: bool = True, ws=None, dev_status=None, stream=None):
     """Attention of the active query rows over the whole cache (+ column sums).
 
+    ``ws``: the workspace for key-range splits; None allocates one, False
+    passes none (the key range is then never split and no merge runs).
     Returns (o [B, M_max, H, d], lse [B, H, M_max] or None, colsum [B, H, L] or None).
     """
     lib = load_library()
@@ -262,6 +264,8 @@ def dllm_partial_attention(q, k_cache, v_cache, count, *, scale: float = 0.0, o_
     need = int(lib.dllm_attention_workspace_bytes(B, L, H, d, M_max, dt))
     if ws is None and need > 0:  # the workspace is optional: without it no key-range split
         ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if ws is False:
+        ws = None
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(lib.dllm_partial_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), dt, B, L, H, d,
                                       M_max, _ptr(count), float(scale), _ptr(o_out),

@@ -124,7 +124,8 @@ class BlockDecodeLoop:
                              dev_status=st, stream=stream)
         if ev: ev[2].record()
         _lib.dllm_partial_attention(q, self.k_cache, self.v_cache, self.count, o_out=self.o,
-                                    lse_out=self.lse, with_colsum=False, ws=self.attn_ws,
+                                    lse_out=self.lse, with_colsum=False,
+                                    ws=False if self.attn_ws is None else self.attn_ws,
                                     dev_status=st, stream=stream)
         if ev: ev[3].record()
         _lib.dllm_attention_colsum(q, self.k_cache, self.count, self.lse,
