@@ -259,19 +259,6 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
                    const __grid_constant__ CUtensorMap tv, FwdParams p) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  __shared__ int s_cnt[kPlanMaxB];
-  stage_counts(p, s_cnt);
-  if (blockIdx.x == 0 && threadIdx.x == 0) {
-    for (int b = 0; b < p.B; ++b) {
-      const int c = __ldca(p.count + b);
-      if (c < 0 || c > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
-    }
-  }
-  __syncthreads();
-  const FwdPlan plan = make_plan(p, s_cnt, gridDim.x);
-  const int n_items = plan_items(plan);
-  if ((int)blockIdx.x >= n_items) return;
-
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   const uint32_t base = (raw_addr + 1023u) & ~1023u;
@@ -294,6 +281,11 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
   float* x_ml = reinterpret_cast<float*>(gbase + kFwdX);  // [2][128]: m, then l
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == kWarpTma && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+    tma_prefetch_desc(&tv);
+  }
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
@@ -317,18 +309,33 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
     fence_barrier_init();
   }
   if (warp == kWarpTma) tmem_alloc(tmem_slot, 512);
+  __shared__ int s_cnt[kPlanMaxB];
+  stage_counts(p, s_cnt);
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (int b = 0; b < p.B; ++b) {
+      const int c = __ldca(p.count + b);
+      if (c < 0 || c > p.M_max) report(p.dev_status, DLLM_ERR_DEVICE_CHECK);
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   volatile int* abort = abort_flag;
+  const FwdPlan plan = make_plan(p, s_cnt, gridDim.x);
+  const int n_items = plan_items(plan);
+  if ((int)blockIdx.x >= n_items) {  // no work: give the tensor memory back
+    if (warp == kWarpTma) tmem_dealloc(tmem, 512);
+    return;
+  }
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
+      // keys stay in L2 for the column-sum pass that reads them next; values
+      // are read once
+      const uint64_t pol_k = l2_policy_evict_last();
+      const uint64_t pol_v = l2_policy_evict_first();
       int j = 0, gk = 0, gv = 0;  // items, K tiles and V tiles issued
       bool ok = true;
       for (int v = blockIdx.x; ok && v < n_items; v += gridDim.x, ++j) {
@@ -353,8 +360,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           }
           uint8_t* kdst = gbase + kFwdK + sk * kTile;
           mbar_expect_tx(&k_full[sk], kTile);
-          tma_load_4d(kdst, &tk, &k_full[sk], 0, h, key0, b);
-          tma_load_4d(kdst + kBox, &tk, &k_full[sk], 64, h, key0, b);
+          tma_load_4d_hint(kdst, &tk, &k_full[sk], 0, h, key0, b, pol_k);
+          tma_load_4d_hint(kdst + kBox, &tk, &k_full[sk], 64, h, key0, b, pol_k);
           ++gk;
           const int sv = gv % kVStages;
           if (gv >= kVStages && !mbar_wait(&v_empty[sv], ((gv / kVStages) - 1) & 1, abort, p.wait_limit)) {
@@ -363,8 +370,8 @@ attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant
           }
           uint8_t* vdst = gbase + kFwdV + sv * kTile;
           mbar_expect_tx(&v_full[sv], kTile);
-          tma_load_4d(vdst, &tv, &v_full[sv], 0, h, key0, b);
-          tma_load_4d(vdst + kBox, &tv, &v_full[sv], 64, h, key0, b);
+          tma_load_4d_hint(vdst, &tv, &v_full[sv], 0, h, key0, b, pol_v);
+          tma_load_4d_hint(vdst + kBox, &tv, &v_full[sv], 64, h, key0, b, pol_v);
           ++gv;
         }
       }
@@ -910,11 +917,12 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
     if (lane == 0) {
       tma_prefetch_desc(&tq);
       tma_prefetch_desc(&tk);
+      const uint64_t pol_k = l2_policy_evict_first();  // the keys' last read of the step
       mbar_expect_tx(k_full, (uint32_t)nk * kTile);
       for (int x = 0; x < nk; ++x) {
         const int key0 = key_base + x * kBN;
-        tma_load_4d(gbase + x * kTile, &tk, k_full, 0, h, key0, b);
-        tma_load_4d(gbase + x * kTile + kBox, &tk, k_full, 64, h, key0, b);
+        tma_load_4d_hint(gbase + x * kTile, &tk, k_full, 0, h, key0, b, pol_k);
+        tma_load_4d_hint(gbase + x * kTile + kBox, &tk, k_full, 64, h, key0, b, pol_k);
       }
       int issued = 0;
       for (int it = 0; it < nqt; ++it) {
@@ -1061,14 +1069,20 @@ attn_colsum_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_const
 // (batch row, head, key tile) items.  Warp 8 loads the query tiles of a head
 // once (they stay resident while its key tiles pass) and streams the key
 // tiles through a four-stage ring; warp 9 issues S^T = K Q^T for each query
-// tile of the item into the TMEM buffer of softmax warpgroup g = item % 2
-// (256 columns each), so one warpgroup adds up the exponentials of one key
-// tile while the tensor cores and the other warpgroup work on the next.  Each
-// softmax thread owns one key: it adds 2^(s * scale * log2 e - lse * log2 e)
-// over the active query rows (chunks of 32 queries past the count are
-// skipped; -lse sits in a warp-private shared buffer per head) and writes the
-// key's column sum.  Rows with no active query get zeros.  Each key has one
-// owner thread: no atomics, run-to-run identical.
+// tile of the item into the TMEM of softmax warpgroup g = item % 2, so one
+// warpgroup adds up the exponentials of one key tile while the tensor cores
+// and the other warpgroup work on the next.  Each softmax thread owns one
+// key: it adds 2^(s * scale * log2 e - lse * log2 e) over the active query
+// rows (chunks of 32 queries past the count are skipped; -lse sits in a
+// warp-private shared buffer per head) and writes the key's column sum.  Rows
+// with no active query get zeros.  Each key has one owner thread: no atomics,
+// run-to-run identical.
+//
+// When every batch row of the CTA's range has at most one query tile (S^T
+// then takes 128 TMEM columns), each warpgroup gets two S buffers, so the
+// product of its next item is ready when it finishes the current one, and the
+// query tiles of consecutive heads go to alternate Q slots, so the next
+// head's query tile loads while the current head's last products run.
 constexpr int kCsThreads = 320;  // warps 0-7 softmax (two groups), 8 TMA, 9 MMA
 constexpr int kCsKStages = 4;
 constexpr uint32_t kCsQ = 0;                                   // kCsMaxQt query tiles
@@ -1082,7 +1096,46 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
                           const __grid_constant__ CUtensorMap tk, ColsumParams p, int B) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  const uint32_t base = (raw_addr + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw_addr);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kCsBar);
+  uint64_t* q_full = bars + 0;   // [2] Q slots
+  uint64_t* q_empty = bars + 2;  // [2]
+  uint64_t* k_full = bars + 4;                // [kCsKStages]
+  uint64_t* k_empty = bars + 4 + kCsKStages;  // [kCsKStages]
+  uint64_t* s_full = bars + 4 + 2 * kCsKStages;  // [group * 2 + buffer]
+  uint64_t* s_free = bars + 8 + 2 * kCsKStages;  // [group * 2 + buffer] (4 warps each)
+  uint64_t* mma_done = bars + 12 + 2 * kCsKStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13 + 2 * kCsKStages);
+  int* abort_flag = reinterpret_cast<int*>(bars + 14 + 2 * kCsKStages);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 8 && lane == 0) {
+    tma_prefetch_desc(&tq);
+    tma_prefetch_desc(&tk);
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&q_full[s], 1);
+      mbar_init(&q_empty[s], 1);
+    }
+    for (int s = 0; s < kCsKStages; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+    }
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);
+    }
+    mbar_init(mma_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 8) tmem_alloc(tmem_slot, 512);
   __shared__ int s_nqt[kPlanMaxB];      // query tiles of each batch row; -1: not handled here
+  __shared__ int s_n[kPlanMaxB];        // active rows of each batch row (clamped)
   __shared__ int s_first[kPlanMaxB + 1];  // first item of each batch row
   const int nkt = (p.L + kBN - 1) / kBN;
   if (threadIdx.x == 0) {
@@ -1091,17 +1144,29 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
       int n = __ldca(p.count + b);
       n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
       const int nqt = (n + kBM - 1) / kBM;
+      s_n[b] = n;
       s_first[b] = acc;
       s_nqt[b] = nqt <= kCsMaxQt ? nqt : -1;
       if (nqt <= kCsMaxQt) acc += p.H * nkt;
     }
     s_first[B] = acc;
   }
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  volatile int* abort = abort_flag;
   const int N = s_first[B];
   const int i0 = (int)((long long)blockIdx.x * N / gridDim.x);
   const int i1 = (int)((long long)(blockIdx.x + 1) * N / gridDim.x);
-  if (i0 >= i1) return;
+  if (i0 >= i1) {  // no work: give the tensor memory back
+    if (warp == 8) tmem_dealloc(tmem, 512);
+    return;
+  }
+  // double buffering of S and Q: every batch row in [i0, i1) has <= 1 query tile
+  bool dbl = true;
+  for (int b = 0; b < B; ++b)
+    if (s_nqt[b] > 1 && s_first[b] < i1 && s_first[b + 1] > i0) dbl = false;
   // item i -> (b, h, kt).  The key tiles of a head are taken last first:
   // the forward pass that usually runs just before streams every head's key
   // tiles first to last, so its last tiles are the ones still in L2.
@@ -1113,50 +1178,18 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
     *h = r / nkt;
     *kt = nkt - 1 - (r - *h * nkt);
   };
-
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw_addr = smem_u32(smem_raw);
-  const uint32_t base = (raw_addr + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw_addr);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + kCsBar);
-  uint64_t* q_full = bars + 0;
-  uint64_t* q_empty = bars + 1;
-  uint64_t* k_full = bars + 2;                // [kCsKStages]
-  uint64_t* k_empty = bars + 2 + kCsKStages;  // [kCsKStages]
-  uint64_t* s_full = bars + 2 + 2 * kCsKStages;  // [2]
-  uint64_t* s_free = bars + 4 + 2 * kCsKStages;  // [2] (4 warps each)
-  uint64_t* mma_done = bars + 6 + 2 * kCsKStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * kCsKStages);
-  int* abort_flag = reinterpret_cast<int*>(bars + 8 + 2 * kCsKStages);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  if (threadIdx.x == 0) {
-    mbar_init(q_full, 1);
-    mbar_init(q_empty, 1);
-    for (int s = 0; s < kCsKStages; ++s) {
-      mbar_init(&k_full[s], 1);
-      mbar_init(&k_empty[s], 1);
-    }
-    for (int g = 0; g < 2; ++g) {
-      mbar_init(&s_full[g], 1);
-      mbar_init(&s_free[g], 4);
-    }
-    mbar_init(mma_done, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 8) tmem_alloc(tmem_slot, 512);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  volatile int* abort = abort_flag;
+  // the n-th item with query tiles of a warpgroup uses S buffer sbuf(n), for
+  // the suse(n)-th time; the sq-th head uses Q slot qslot(sq) for the
+  // quse(sq)-th time
+  auto sbuf = [&](int n) { return dbl ? (n & 1) : 0; };
+  auto suse = [&](int n) { return dbl ? (n >> 1) : n; };
+  auto qslot = [&](int sq) { return dbl ? (sq & 1) : 0; };
+  auto quse = [&](int sq) { return dbl ? (sq >> 1) : sq; };
 
   if (warp == 8) {
     // ------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
+      const uint64_t pol_k = l2_policy_evict_first();  // the keys' last read of the step
       int kc = 0, sq = 0, cur = -1;
       for (int i = i0; i < i1; ++i) {
         int b, h, kt;
@@ -1164,11 +1197,13 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
         const int nqt = s_nqt[b];
         if (nqt == 0) continue;
         if (b * p.H + h != cur) {  // a new head: its query tiles, once
-          if (sq > 0 && !mbar_wait(q_empty, (sq - 1) & 1, abort)) break;
-          mbar_expect_tx(q_full, (uint32_t)nqt * kTile);
+          const int qs = qslot(sq), qu = quse(sq);
+          if (qu > 0 && !mbar_wait(&q_empty[qs], (qu - 1) & 1, abort)) break;
+          mbar_expect_tx(&q_full[qs], (uint32_t)nqt * kTile);
           for (int qt = 0; qt < nqt; ++qt) {
-            tma_load_4d(gbase + kCsQ + qt * kTile, &tq, q_full, 0, h, qt * kBM, b);
-            tma_load_4d(gbase + kCsQ + qt * kTile + kBox, &tq, q_full, 64, h, qt * kBM, b);
+            uint8_t* qdst = gbase + kCsQ + (qs + qt) * kTile;
+            tma_load_4d(qdst, &tq, &q_full[qs], 0, h, qt * kBM, b);
+            tma_load_4d(qdst + kBox, &tq, &q_full[qs], 64, h, qt * kBM, b);
           }
           cur = b * p.H + h;
           ++sq;
@@ -1177,12 +1212,16 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
         if (kc >= kCsKStages && !mbar_wait(&k_empty[s], ((kc / kCsKStages) - 1) & 1, abort))
           break;
         mbar_expect_tx(&k_full[s], kTile);
-        tma_load_4d(gbase + kCsK + s * kTile, &tk, &k_full[s], 0, h, kt * kBN, b);
-        tma_load_4d(gbase + kCsK + s * kTile + kBox, &tk, &k_full[s], 64, h, kt * kBN, b);
+        tma_load_4d_hint(gbase + kCsK + s * kTile, &tk, &k_full[s], 0, h, kt * kBN, b, pol_k);
+        tma_load_4d_hint(gbase + kCsK + s * kTile + kBox, &tk, &k_full[s], 64, h, kt * kBN, b,
+                         pol_k);
         ++kc;
       }
+      // Drain: the query tiles of the last head of each slot (earlier ones
+      // were consumed before their slot was reused) and the last key tiles.
       int none = 0;
-      if (sq > 0) mbar_wait(q_full, (sq - 1) & 1, &none);
+      for (int s = sq - (dbl ? 2 : 1) < 0 ? 0 : sq - (dbl ? 2 : 1); s < sq; ++s)
+        mbar_wait(&q_full[qslot(s)], quse(s) & 1, &none);
       for (int k = kc - kCsKStages < 0 ? 0 : kc - kCsKStages; k < kc; ++k)
         mbar_wait(&k_full[k % kCsKStages], (k / kCsKStages) & 1, &none);
       if (none) report(p.dev_status, DLLM_ERR_TIMEOUT);
@@ -1191,7 +1230,7 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t id = idesc_bf16_f32(kBN, kBM, false, false);
-      int kc = 0, sq = 0, cur = -1;
+      int kc = 0, sq = 0, cur = -1, cq = 0;
       int ng[2] = {0, 0};  // items with query tiles per softmax group
       bool ok = true;
       for (int i = i0; ok && i < i1; ++i) {
@@ -1201,26 +1240,29 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
         if (nqt == 0) continue;
         const int g = (i - i0) & 1;
         if (b * p.H + h != cur) {
-          if (sq > 0) mma_commit(q_empty);  // every product with the previous head's Q issued
-          if (!mbar_wait(q_full, sq & 1, abort)) break;
+          // every product with the previous head's query tiles is issued
+          if (sq > 0) mma_commit(&q_empty[qslot(sq - 1)]);
+          if (!mbar_wait(&q_full[qslot(sq)], quse(sq) & 1, abort)) break;
+          cq = qslot(sq);
           cur = b * p.H + h;
           ++sq;
         }
         const int s = kc % kCsKStages;
         if (!mbar_wait(&k_full[s], (kc / kCsKStages) & 1, abort)) break;
-        if (ng[g] > 0 && !mbar_wait(&s_free[g], (ng[g] - 1) & 1, abort)) break;
+        const int sb = sbuf(ng[g]), su = suse(ng[g]);
+        if (su > 0 && !mbar_wait(&s_free[g * 2 + sb], (su - 1) & 1, abort)) break;
         tc_fence_after();
         const uint32_t sK = base + kCsK + s * kTile;
         for (int qt = 0; qt < nqt; ++qt) {
-          const uint32_t sQ = base + kCsQ + qt * kTile;
+          const uint32_t sQ = base + kCsQ + (cq + qt) * kTile;
 #pragma unroll
           for (int kk = 0; kk < kHD / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            mma_bf16_ss(tmem + g * 256 + qt * kBM, smem_desc_sw128(sK + off, 16, 1024),
+            mma_bf16_ss(tmem + g * 256 + sb * 128 + qt * kBM, smem_desc_sw128(sK + off, 16, 1024),
                         smem_desc_sw128(sQ + off, 16, 1024), id, kk > 0);
           }
         }
-        mma_commit(&s_full[g]);
+        mma_commit(&s_full[g * 2 + sb]);
         mma_commit(&k_empty[s]);
         ++kc;
         ++ng[g];
@@ -1235,7 +1277,7 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
     const int g = warp >> 2;
     const int quarter = warp & 3;
     const int j = quarter * 32 + lane;  // key of this thread within the tile
-    const uint32_t tS = tmem + ((uint32_t)(quarter * 32) << 16) + g * 256;
+    const uint32_t tS0 = tmem + ((uint32_t)(quarter * 32) << 16) + g * 256;
     float* lb = reinterpret_cast<float*>(gbase + kCsL) + warp * (kCsMaxQt * kBM);
     const float sl2 = p.scale_log2;
     const float2 sl2x2 = make_float2(sl2, sl2);
@@ -1253,18 +1295,27 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
       }
       if (b * p.H + h != cur) {  // -lse (log2 units) of the head's query rows, -inf past the count
         cur = b * p.H + h;
-        n = __ldca(p.count + b);
-        n = n < 0 ? 0 : (n > p.M_max ? p.M_max : n);
+        n = s_n[b];
         const float* lse_g = p.lse + ((int64_t)b * p.H + h) * p.M_max;
+        constexpr int kPer = kCsMaxQt * kBM / 32;
+        float v[kPer];
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) {  // all loads first, then the stores
+          const int q = lane + 32 * u;
+          v[u] = q < n ? __ldca(lse_g + q) : INFINITY;
+        }
         __syncwarp();
-        for (int q = lane; q < nqt * kBM; q += 32) lb[q] = q < n ? -__ldca(lse_g + q) * kLog2e : -INFINITY;
+#pragma unroll
+        for (int u = 0; u < kPer; ++u) lb[lane + 32 * u] = -v[u] * kLog2e;
         __syncwarp();
       }
-      if (!warp_wait(&s_full[g], ng & 1, abort)) {
+      const int sb = sbuf(ng), su = suse(ng);
+      if (!warp_wait(&s_full[g * 2 + sb], su & 1, abort)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      const uint32_t tS = tS0 + sb * 128;
       float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
       const int nch = (n + 31) / 32;  // chunks of 32 queries holding an active row
       auto add_chunk = [&](const uint32_t(&rw)[32], int c) {
@@ -1307,7 +1358,7 @@ attn_colsum_stream_kernel(const __grid_constant__ CUtensorMap tq,
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[g]);  // S_g is read: the item after next may overwrite it
+      if (lane == 0) mbar_arrive(&s_free[g * 2 + sb]);  // this S buffer may be overwritten
       ++ng;
       if (key < p.L) out[key] = (acc0.x + acc0.y) + (acc1.x + acc1.y);
     }
