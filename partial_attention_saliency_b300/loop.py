@@ -35,6 +35,11 @@ class BlockDecodeLoop:
 
     The attention gets no workspace when B * H already covers half the SMs:
     it then never splits the key range, so no merge launch follows it.
+
+    The column sums feed nothing later in the step, so they run on a second
+    stream, concurrently with the confidence and the prefix commit; the step
+    joins the two streams before it returns (a fork and a join in a captured
+    graph).
     """
 
     def __init__(self, B: int, L: int, H: int, d: int, V: int, dtype: torch.dtype,
@@ -66,6 +71,9 @@ class BlockDecodeLoop:
         self.dev_status = torch.zeros((1,), dtype=i32, device=dev)
         cw = _lib.dllm_confidence_workspace_bytes(B, L, V, dtype)
         self.conf_ws = torch.empty((max(cw, 16),), dtype=torch.uint8, device=dev)
+        self._side = torch.cuda.Stream(dev)
+        self._fork = torch.cuda.Event()
+        self._join = torch.cuda.Event()
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         self.attn_ws = None
         if 2 * B * H < sms:
@@ -108,7 +116,9 @@ class BlockDecodeLoop:
         [B, R, V] (R <= row_cap rows allocated), row r the logits of the r-th
         active position.  Optional
         ``events`` (7) are recorded on the current stream around the six
-        calls (pass ``stream=None`` with them).
+        calls (pass ``stream=None`` with them); the calls then run one after
+        the other on that stream, the column sums included.  ``stream`` is
+        None (the current stream) or a ``torch.cuda.Stream``.
         """
         w = win_start
         Lw = self.L - w
@@ -127,10 +137,17 @@ class BlockDecodeLoop:
                                     lse_out=self.lse, with_colsum=False,
                                     ws=False if self.attn_ws is None else self.attn_ws,
                                     dev_status=st, stream=stream)
-        if ev: ev[3].record()
-        _lib.dllm_attention_colsum(q, self.k_cache, self.count, self.lse,
-                                   colsum_out=self.colsum, dev_status=st, stream=stream)
-        if ev: ev[4].record()
+        if ev:
+            ev[3].record()
+            _lib.dllm_attention_colsum(q, self.k_cache, self.count, self.lse,
+                                       colsum_out=self.colsum, dev_status=st)
+            ev[4].record()
+        else:  # fork: the column sums on the side stream
+            main = torch.cuda.current_stream() if stream is None else stream
+            self._fork.record(main)
+            self._side.wait_event(self._fork)
+            _lib.dllm_attention_colsum(q, self.k_cache, self.count, self.lse,
+                                       colsum_out=self.colsum, dev_status=st, stream=self._side)
         _lib.dllm_confidence(logits, R_max=Lw, count=self.count, out_idx=idx, out_cols=self.L,
                              conf_out=self.score, argmax_out=self.argmax,
                              margin_out=self.margin, ws=self.conf_ws, dev_status=st,
@@ -139,5 +156,9 @@ class BlockDecodeLoop:
         _lib.dllm_stable_prefix(self.score, self.start, self.tau_c, min_commit=True,
                                 advance_start=True, len_out=self.length, dev_status=st,
                                 stream=stream)
-        if ev: ev[6].record()
+        if ev:
+            ev[6].record()
+        else:  # join
+            self._join.record(self._side)
+            main.wait_event(self._join)
         return self
