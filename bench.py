@@ -308,6 +308,48 @@ def time_regions(region, stream, est_ms: float, warm=None, min_seconds: float = 
     return out
 
 
+def read_ceiling(sizes: dict, device, reps: int = 5) -> dict:
+    """Reference time of one read-bound launch per byte count: dllm_read_stream
+    (one persistent CTA per SM streaming the bytes into shared memory with
+    cp.async.bulk, nothing else) timed like the calls, with an external event
+    on each side of every launch in a replayed CUDA graph.  Each launch reads
+    its own region of a buffer three times the largest size, so consecutive
+    launches find nothing in L2.  Returns {name: median us}."""
+    import partial_attention_saliency_b300 as dl
+    if not sizes:
+        return {}
+    nb = {n: max(16, int(v) // 16 * 16) for n, v in sizes.items()}
+    span = max(nb.values())
+    buf = torch.ones((3 * span + 4096,), dtype=torch.uint8, device=device)
+    sink = torch.zeros((1,), dtype=torch.int32, device=device)
+    st = torch.zeros((1,), dtype=torch.int32, device=device)
+    names = list(nb)
+    ev = [[(torch.cuda.Event(enable_timing=True, external=True),
+            torch.cuda.Event(enable_timing=True, external=True)) for _ in names]
+          for _ in range(reps)]
+    cap = torch.cuda.Stream(device)
+    g = torch.cuda.CUDAGraph()
+    k = 0
+    with torch.cuda.graph(g, stream=cap):
+        for r in range(reps):
+            for i, n in enumerate(names):
+                off = (k % 3) * span
+                k += 1
+                ev[r][i][0].record()
+                dl.dllm_read_stream(buf[off:off + nb[n]], nb[n], sink, dev_status=st)
+                ev[r][i][1].record()
+    g.replay()
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    if int(st[0]) != 0:
+        raise RuntimeError("dllm_read_stream: a pipeline wait ran out")
+    out = {n: statistics.median(ev[r][i][0].elapsed_time(ev[r][i][1]) * 1e3
+                                for r in range(reps)) for i, n in enumerate(names)}
+    del buf
+    return out
+
+
 # ----------------------------------------------------------------------------- workloads
 
 @dataclasses.dataclass
@@ -931,6 +973,13 @@ def main_loop(args, rank, world, device, pg):
                       "GB/s": gbs, "TFLOP/s": tfs, "bound": bound,
                       "frac": (tfs / pk["bf16_tflops"]) if bound == "tensor"
                       else gbs / pk["hbm_gbs"], "kernels": KERNELS[n][0]}
+    # the single-launch read reference at each memory-bound call's byte count
+    ceil = read_ceiling({n: kernels[n]["alg_bytes"] for n in LOOP_ORDER
+                         if kernels[n]["bound"] == "hbm" and kernels[n]["alg_bytes"] >= 1 << 20},
+                        device)
+    for n, us in ceil.items():
+        kernels[n]["read_ceiling_us"] = us
+        kernels[n]["frac_of_read_ceiling"] = us / kernels[n]["us"]
     dom = max(kernels, key=lambda n: kernels[n]["us"])
     dk = kernels[dom]
     if dk["bound"] == "tensor":
@@ -939,6 +988,13 @@ def main_loop(args, rank, world, device, pg):
     else:
         roof = {"bound": "hbm", "achieved": dk["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": dk["GB/s"] / pk["hbm_gbs"]}
+        if dom in ceil:
+            roof["read_ceiling"] = {
+                "us": ceil[dom], "GB/s": dk["alg_bytes"] / ceil[dom] / 1e3,
+                "frac_of_peak": dk["alg_bytes"] / ceil[dom] / 1e3 / pk["hbm_gbs"],
+                "frac": ceil[dom] / dk["us"],
+                "what": "dllm_read_stream over the same bytes: one launch that only streams "
+                        "them into shared memory, timed the same way"}
     tr = TRAFFIC.get(("loop_b4_2k_128", dom))
     traffic = None
     if tr is not None and tr["src_sha"] == src_sha(KERNELS[dom][1]):

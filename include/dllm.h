@@ -603,8 +603,9 @@ dllm_status dllm_slowfast_observe(dllm_slowfast* sf, const int32_t* start,
 void dllm_slowfast_destroy(dllm_slowfast* sf);
 
 /*
- * Diagnostics.  Neither computes anything of the step; they let tests check
- * the library's own machinery.  The pages have no counterpart to them.
+ * Diagnostics.  None computes anything of the step; they let tests check
+ * the library's own machinery and give the bench its reference for the
+ * memory-bound calls.  The pages have no counterpart to them.
  *
  * dllm_exp2_fma_eval -- y[i] = 2^x[i] through the FMA-pipe exponential the
  * attention kernels use for part of their exponentials (Cody-Waite split
@@ -621,10 +622,24 @@ void dllm_slowfast_destroy(dllm_slowfast* sf);
  * memory and returns, leaving that call's outputs incomplete.  For tests of
  * that path; not thread-safe against concurrent launches.  Errors:
  * INVALID_ARG for a negative count.
+ *
+ * dllm_read_stream -- reads `bytes` bytes of `buf` (device memory, 16-byte
+ * aligned, bytes a positive multiple of 16) once, in one launch of one
+ * persistent CTA per SM that copies 32 KB chunks into a four-stage
+ * shared-memory ring with cp.async.bulk and computes nothing: its duration is
+ * the time one launch of a read-bound kernel of that size needs at least on
+ * this GPU, launch, ramp-up and tail included, the reference the memory-bound
+ * calls are measured against.  A byte of each chunk is added into *sink (one
+ * uint32 in device memory, accumulated with atomicAdd) so that the copies are
+ * observable.  A pipeline wait that runs out records DLLM_ERR_TIMEOUT in
+ * *dev_status.  Errors: INVALID_ARG (NULLs, size, alignment), CUDA (launch).
  */
 dllm_status dllm_exp2_fma_eval(const float* x, float* y, int n, void* stream);
 
 dllm_status dllm_set_wait_limit(long long cycles);
+
+dllm_status dllm_read_stream(const void* buf, size_t bytes, uint32_t* sink,
+                             int32_t* dev_status, void* stream);
 
 #ifdef __cplusplus
 }  /* extern "C" */

@@ -27,6 +27,7 @@ from ._lib import (  # noqa: F401
     dllm_lock_criterion,
     dllm_lock_workspace_bytes,
     dllm_partial_attention,
+    dllm_read_stream,
     dllm_saliency_select,
     dllm_slowfast_select,
     dllm_snap_prefix,

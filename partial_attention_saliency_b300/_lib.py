@@ -59,6 +59,7 @@ SIGNATURES = {
     "dllm_slowfast_state_bytes": (_SZ, [_I, _I]),
     "dllm_exp2_fma_eval": (_I, [_P, _P, _I, _P]),
     "dllm_set_wait_limit": (_I, [ctypes.c_longlong]),
+    "dllm_read_stream": (_I, [_P, _SZ, _P, _P, _P]),
     "dllm_slowfast_observe_device": (_I, [_P, _I, _I, ctypes.c_double, _P, _P, _P, _P, _P, _P]),
     "dllm_slowfast_select": (_I, [_P, _P, _I, _I, _P, _P, _P, _F, _I, _I, _P, _P, _P, _P]),
 }
@@ -548,3 +549,16 @@ def dllm_slowfast_select(conf, start, phase, region_end, tau_high: float, width:
                                     _ptr(idx_out), _ptr(count_out), _ptr(dev_status),
                                     _stream(stream)))
     return idx_out, count_out
+
+
+def dllm_read_stream(buf, nbytes: int, sink, *, dev_status, stream=None):
+    """Reads the first ``nbytes`` bytes of ``buf`` (a contiguous device
+    tensor) once, in one launch that does nothing else: the reference time of
+    a read-bound launch of that size.  ``sink`` int32 [1] accumulates a byte
+    of every 32 KB chunk; ``dev_status`` int32 [1]."""
+    if not buf.is_contiguous() or nbytes > buf.numel() * buf.element_size():
+        raise ValueError("dllm_read_stream: buf must be contiguous and hold nbytes")
+    _need(sink, torch.int32, (1,), "sink")
+    _need(dev_status, torch.int32, (1,), "dev_status")
+    _check(load_library().dllm_read_stream(_ptr(buf), int(nbytes), _ptr(sink), _ptr(dev_status),
+                                           _stream(stream)))

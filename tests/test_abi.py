@@ -139,6 +139,17 @@ def test_sampler_and_stable_row_update_rejected_before_launch(lib):
     assert upd(B=0) == 1
 
 
+def test_diagnostics_rejected_before_launch(lib):
+    p = ctypes.c_void_p(0x1000)  # never dereferenced: validation fails first
+    assert lib.dllm_set_wait_limit(-1) == 1
+    assert lib.dllm_exp2_fma_eval(None, p, 4, None) == 1
+    assert lib.dllm_read_stream(None, 4096, p, p, None) == 1
+    assert lib.dllm_read_stream(p, 4100, p, p, None) == 1  # not a multiple of 16
+    assert b"multiple of 16" in lib.dllm_last_error()
+    assert lib.dllm_read_stream(ctypes.c_void_p(0x1008), 4096, p, p, None) == 1  # misaligned
+    assert lib.dllm_read_stream(p, 4096, None, p, None) == 1
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     from partial_attention_saliency_b300 import _lib
     with pytest.raises(ImportError):

@@ -1,5 +1,6 @@
 """The library's own machinery on the GPU: the FMA-pipe exponential against
-its error bound, and a bounded pipeline wait that runs out.
+its error bound, a bounded pipeline wait that runs out, and the read-stream
+reference kernel reading every chunk it is given.
 
 Bounded waits: every mbarrier wait of the kernels gives up after a limit,
 records DLLM_ERR_TIMEOUT in dev_status, drains the kernel's own copies and
@@ -86,3 +87,25 @@ def test_attention_wait_runs_out_and_next_call_is_clean(dl):
         go = o[b, :n, h].double().cpu().numpy()
         assert np.all(np.abs(go - ro[0, :n, 0]) <= 2e-2 + 1e-2 * np.abs(ro[0, :n, 0]))
         assert np.max(np.abs(cs[b, h].double().cpu().numpy() - rcs[0, 0])) <= 1e-4
+
+
+@pytest.mark.parametrize("nbytes", [16, 32768 * 3 + 4096, 64 << 20])
+def test_read_stream_reads_each_chunk(dl, nbytes):
+    # chunk c (32 KB, the last one shorter) is the (c // grid)-th chunk of CTA
+    # c % grid, which adds its byte at offset ((c // grid) % 16) * 16 (0 when
+    # the chunk is shorter than that) into the sink
+    g = torch.Generator().manual_seed(nbytes)
+    buf = torch.randint(0, 256, (nbytes,), generator=g, dtype=torch.uint8)
+    sink = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    dl.dllm_read_stream(buf.cuda(), nbytes, sink, dev_status=st)
+    torch.cuda.synchronize()
+    grid = torch.cuda.get_device_properties(0).multi_processor_count
+    nch = (nbytes + 32767) // 32768
+    c = np.arange(nch)
+    size = np.minimum(nbytes - c * 32768, 32768)
+    off = ((c // grid) % 16) * 16
+    off = np.where(off < size, off, 0)
+    want = int(buf.numpy()[c * 32768 + off].astype(np.int64).sum())
+    assert int(st[0]) == 0
+    assert int(sink[0]) == want
