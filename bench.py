@@ -74,8 +74,8 @@ KERNELS = {  # kernels each entry point launches, and the source they come from
                               "attention_tc.cu"),
     "dllm_confidence": (["conf_stream_kernel", "conf_merge_kernel"], "confidence.cu"),
     "dllm_stable_prefix": (["stable_prefix_kernel"], "stable_prefix.cu"),
-    "dllm_lock_criterion": (["lock_partial_kernel", "lock_merge_kernel", "lock_gate_kernel"],
-                            "lock.cu"),
+    "dllm_lock_criterion": (["lock_partial_persistent_kernel", "lock_partial_kernel",
+                             "lock_merge_kernel", "lock_gate_kernel"], "lock.cu"),
     "dllm_adaptive_prefix": (["adaptive_prefix_kernel"], "lock.cu"),
 }
 

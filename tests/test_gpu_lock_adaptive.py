@@ -68,6 +68,23 @@ def test_lock_kl_dense(dl, dtype, V):
     assert float(ref_kl.min()) < 1e-3 and float(ref_kl.max()) > 0.3  # the spread is real
 
 
+@pytest.mark.parametrize("B", [3, 65])
+def test_lock_kl_ragged_counts(dl, B):
+    # B <= 64: the persistent partial kernel over the valid rows; 65: one CTA
+    # per row slot.  Counts from 0 to R, so many row slots are empty.
+    g = torch.Generator().manual_seed(B)
+    R, V = 9, 1000
+    z, y = _pair(g, B, R, V, torch.bfloat16, 1.0)
+    count = torch.tensor([(7 * b) % (R + 1) for b in range(B)], dtype=torch.int32)
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    kl, unc, _ = dl.dllm_lock_criterion(z.cuda(), y.cuda(), 0.0, count=count.cuda(), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    ref_kl, ref_unc = oracle.lock_kl(f64(z), f64(y))
+    mask = np.arange(R)[None, :] < count.numpy()[:, None]
+    _check_kl(kl, unc, ref_kl, ref_unc, mask)
+
+
 def test_lock_kl_identical_rows_give_zero(dl):
     g = torch.Generator().manual_seed(5)
     z = workloads.normal(g, (1, 8, 126464), 3.0, torch.bfloat16)
