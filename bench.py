@@ -90,6 +90,10 @@ TRAFFIC = {
                                                           "src_sha": "e7e48f69adabdd83"},
     ("batch8_2k_f05_random", "dllm_partial_attention"): {"bytes": 284102912,
                                                           "src_sha": "e7e48f69adabdd83"},
+    # steady-state loop steps, single-pass capture without cache flush (the
+    # mean of a generated-rows-window step and a whole-sequence step)
+    ("loop_b4_2k_128", "dllm_partial_attention"): {"bytes": 137420000,
+                                                   "src_sha": "ac7533d2287a20e8"},
 }
 
 
