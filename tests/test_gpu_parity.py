@@ -193,6 +193,34 @@ def test_confidence_ragged_vocab_and_ties(dl, dtype, V):
         assert i32(am)[0, 3] == V // 2 and f64(mg)[0, 3] == 0.0
 
 
+@pytest.mark.parametrize("B,R,V,counts", [
+    (3, 40, 126464, [40, 0, 17]),   # ragged counts, an empty batch row
+    (2, 9, 300000, None),           # 10 chunks of 64 KB per row
+    (65, 3, 1000, None),            # more batch rows than the streaming kernel stages counts for
+])
+def test_confidence_kernel_paths(dl, B, R, V, counts):
+    # the streaming kernel and the merge on aligned rows: rows past a count
+    # are not written, every other row matches the oracle
+    g = torch.Generator().manual_seed(V + B)
+    z = workloads.normal(g, (B, R, V), 2.0, torch.bfloat16)
+    cnt = None if counts is None else torch.tensor(counts, dtype=torch.int32)
+    st = dev(torch.zeros((1,), dtype=torch.int32))
+    conf = dev(torch.full((B, R), -7.0))
+    am = dev(torch.full((B, R), -7, dtype=torch.int32))
+    mg = dev(torch.full((B, R), -7.0))
+    dl.dllm_confidence(dev(z), count=None if cnt is None else dev(cnt), conf_out=conf,
+                       argmax_out=am, margin_out=mg, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    rc, ra, rm = oracle.confidence(f64(z), count=None if cnt is None else cnt.numpy())
+    for b in range(B):
+        n = R if cnt is None else int(cnt[b])
+        if n > 0:
+            _conf_compare(f64(conf)[b:b + 1, :n], i32(am)[b:b + 1, :n], f64(mg)[b:b + 1, :n],
+                          rc[b:b + 1, :n], ra[b:b + 1, :n], rm[b:b + 1, :n])
+        assert np.all(f64(conf)[b, n:] == -7.0)  # rows past the count are not written
+
+
 def test_confidence_strided_rows_row_idx_count_out_idx(dl):
     g = torch.Generator().manual_seed(11)
     B, R_src, V = 2, 20, 3000
