@@ -98,6 +98,9 @@ struct ColsumParams {
 // persistent column-sum kernel; the others the key-tile-group kernel.
 constexpr int kCsMaxQt = 2;
 
+// Key tiles of 128 below which the forward never splits the key range.
+constexpr int kMinSplitTiles = 12;
+
 // shared-memory map of the forward kernel (offsets from a 1024-aligned base).
 // K and V have rings of their own: a K tile is free once the Q K^T products
 // of its tile are done, a V tile only after the P V products, so K runs a
@@ -1437,8 +1440,13 @@ cudaError_t launch_attention_tc(const void* q, const void* k, const void* v, int
     return cudaErrorInvalidValue;
   const int n_ctas = num_sms();
   const size_t need = attention_tc_workspace_bytes(n_ctas);
-  const bool can_split =
-      ws != nullptr && ws_bytes >= need && reinterpret_cast<uintptr_t>(ws) % 16 == 0;
+  // Splitting the key range costs the merge launch (about 4 us with its
+  // start-up): below kMinSplitTiles key tiles a CTA's whole range takes
+  // less than that (L 1024, 32 heads: 14.7 us unsplit against 16.4 us split
+  // and merged; L 2048: 23.4 against 19.3 us).
+  const int nkt = (L + kBN - 1) / kBN;
+  const bool can_split = ws != nullptr && ws_bytes >= need &&
+                         reinterpret_cast<uintptr_t>(ws) % 16 == 0 && nkt >= kMinSplitTiles;
   FwdParams fp;
   fp.count = count;
   fp.o = static_cast<__nv_bfloat16*>(o);
