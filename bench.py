@@ -77,6 +77,11 @@ KERNELS = {  # kernels each entry point launches, and the source they come from
     "dllm_lock_criterion": (["lock_partial_persistent_kernel", "lock_partial_kernel",
                              "lock_merge_kernel", "lock_gate_kernel"], "lock.cu"),
     "dllm_adaptive_prefix": (["adaptive_prefix_kernel"], "lock.cu"),
+    "dllm_approx_attention_update": (["approx_update_tc_kernel"], "approx_update_tc.cu"),
+    "dllm_attn_scores": (["attn_scores_kernel"], "sampler.cu"),
+    "dllm_attn_sampler_select": (["attn_sampler_select_kernel"], "sampler.cu"),
+    "dllm_slowfast_observe_device": (["slowfast_observe_kernel"], "slowfast_device.cu"),
+    "dllm_slowfast_select": (["slowfast_select_kernel"], "slowfast_device.cu"),
 }
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of an
@@ -92,8 +97,12 @@ TRAFFIC = {
                                                           "src_sha": "e7e48f69adabdd83"},
     # steady-state loop steps, single-pass capture without cache flush (the
     # mean of a generated-rows-window step and a whole-sequence step)
-    ("loop_b4_2k_128", "dllm_partial_attention"): {"bytes": 137420000,
-                                                   "src_sha": "ac7533d2287a20e8"},
+    ("loop_b4_2k_128", "dllm_partial_attention"): {"bytes": 143480000,
+                                                   "src_sha": "f7092d2beca757ee"},
+    # the calls around the loop's step 1, single-kernel captures
+    ("around_b4_2k", "dllm_approx_attention_update"): {"bytes": 160583680,
+                                                       "src_sha": "d56bc4837a78c2c7"},
+    ("around_b4_2k", "dllm_lock_criterion"): {"bytes": 254935296, "src_sha": "592007ee4f3dc03f"},
 }
 
 
@@ -1247,6 +1256,13 @@ def main_around(args, rank, world, device, pg):
         roof = {"bound": "hbm", "achieved": dk["GB/s"], "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": dk["frac"], "traffic": None, "kernel": dom,
                 "peak_source": pk["source"] + " (burst)"}
+    for n, k in kernels.items():  # ncu DRAM traffic of each call's main kernel, while current
+        tr = TRAFFIC.get(("around_b4_2k", n))
+        if tr is not None and n in KERNELS and tr["src_sha"] == src_sha(KERNELS[n][1]):
+            k["traffic"] = tr["bytes"]
+            if n == dom:
+                roof["traffic"] = tr["bytes"]
+    roof["kernels"] = KERNELS.get(dom, ([], ""))[0]
     line = {"metric": METRIC, "value": M / (total_ms / 1e3), "unit": UNIT, "n_gpus": world,
             "steps": 1, "warmup": args.warmup, "ms_per_step": total_ms, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
