@@ -15,7 +15,12 @@
 //                           (descending score, ascending position) of the
 //                           candidates in shared memory, bitonic sort, the
 //                           ordered positions, and the number of leading
-//                           entries that reach the threshold.
+//                           entries that reach the threshold.  The sort's
+//                           stages with partners less than 64 keys apart run
+//                           in registers, each warp on 64-key segments (two
+//                           keys per lane, partners by warp shuffle); only the
+//                           wider stages go through shared memory, one pair
+//                           per thread and one CTA barrier each.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,6 +30,7 @@ namespace {
 constexpr int kScoreThreads = 256;
 constexpr int kSelectThreads = 1024;
 constexpr int kSelectMaxL = 16384;  // 64-bit keys of a batch row in shared memory (128 KB)
+constexpr int kSegKeys = 64;        // keys a warp sorts in registers (two per lane)
 
 __device__ __forceinline__ int warp_sum_int(int v) {
 #pragma unroll
@@ -66,7 +72,7 @@ attn_sampler_select_kernel(const float* score, int L, int N, const uint8_t* cand
                            float gamma, int k_max, int32_t* order, int32_t* n_out) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  extern __shared__ uint64_t keys[];  // [N], N a power of two >= L
+  extern __shared__ uint64_t keys[];  // [N], N a power of two >= L and >= 64
   __shared__ int s_cnt[kSelectThreads / 32], s_fail[kSelectThreads / 32];
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* sc = score + (int64_t)b * L;
@@ -86,22 +92,50 @@ attn_sampler_select_kernel(const float* score, int L, int N, const uint8_t* cand
   __syncthreads();
   int n_cand = 0;
   for (int w = 0; w < kSelectThreads / 32; ++w) n_cand += s_cnt[w];
-  // 2. bitonic sort, ascending
-  for (int k = 2; k <= N; k <<= 1) {
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < N; i += kSelectThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const uint64_t x = keys[i], y = keys[ixj];
-          const bool up = (i & k) == 0;
-          if ((x > y) == up) {
-            keys[i] = y;
-            keys[ixj] = x;
-          }
+  // 2. bitonic sort, ascending.  Stage (k, j) orders each pair (i, i ^ j)
+  // ascending where i & k is 0 and descending elsewhere.
+  // The stages j = min(k, 64) / 2 .. 1 of every k <= N, in registers: lane
+  // l of a warp holds keys base + 2l and base + 2l + 1 of a 64-key segment.
+  auto register_stages = [&](int k_lo, int k_hi) {
+    for (int base = warp * kSegKeys; base < N; base += kSelectThreads / 32 * kSegKeys) {
+      const int i0 = base + 2 * lane;
+      uint64_t a = keys[i0], c = keys[i0 + 1];
+      for (int k = k_lo; k <= k_hi; k <<= 1) {
+        const bool up = (i0 & k) == 0;
+        for (int j = (k < kSegKeys ? k : kSegKeys) >> 1; j > 1; j >>= 1) {
+          const uint64_t pa = __shfl_xor_sync(0xffffffffu, a, j >> 1);
+          const uint64_t pc = __shfl_xor_sync(0xffffffffu, c, j >> 1);
+          const bool keep_min = ((lane & (j >> 1)) == 0) == up;  // lower of the pair, ascending
+          a = keep_min ? (a < pa ? a : pa) : (a > pa ? a : pa);
+          c = keep_min ? (c < pc ? c : pc) : (c > pc ? c : pc);
+        }
+        if ((a > c) == up) {  // j = 1: the lane's own two keys
+          const uint64_t x = a;
+          a = c;
+          c = x;
+        }
+      }
+      keys[i0] = a;
+      keys[i0 + 1] = c;
+    }
+    __syncthreads();
+  };
+  register_stages(2, kSegKeys);
+  for (int k = 2 * kSegKeys; k <= N; k <<= 1) {
+    // the stages with partners at least 64 keys apart: pair p of N / 2 is
+    // (i, i + j), i the index p with a zero bit inserted at j
+    for (int j = k >> 1; j >= kSegKeys; j >>= 1) {
+      for (int p = tid; p < N / 2; p += kSelectThreads) {
+        const int i = ((p & ~(j - 1)) << 1) | (p & (j - 1)), ixj = i | j;
+        const uint64_t x = keys[i], y = keys[ixj];
+        if ((x > y) == ((i & k) == 0)) {
+          keys[i] = y;
+          keys[ixj] = x;
         }
       }
       __syncthreads();
     }
+    register_stages(k, k);
   }
   // 3. the ordered positions, and the first entry below the threshold
   float thr = tau;
@@ -148,7 +182,7 @@ cudaError_t launch_attn_sampler_select(const float* score, int B, int L,
                                        int k_max, int32_t* order, int32_t* n_out,
                                        cudaStream_t stream) {
   if (L < 1 || L > kSelectMaxL) return cudaErrorInvalidValue;
-  int N = 1;
+  int N = kSegKeys;
   while (N < L) N <<= 1;
   // the limit is set once per kernel: raise it to the largest size any call uses
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_sampler_select_kernel),
