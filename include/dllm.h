@@ -13,7 +13,8 @@
  *   dllm_partial_attention (with or without column sums; the sums alone:
  *   dllm_attention_colsum), dllm_confidence (dllm_confidence_static_ws for
  *   callers that cannot allocate), dllm_stable_prefix.
- *   Around it: dllm_lock_criterion (SureLock), dllm_adaptive_prefix and
+ *   Around it: dllm_lock_criterion (SureLock; dllm_lock_criterion_conf also
+ *   gives dllm_confidence's outputs), dllm_adaptive_prefix and
  *   dllm_snap_prefix (LSP), dllm_approx_attention_update (DyLLM's stable
  *   rows), dllm_attn_scores and dllm_attn_sampler_select (Attn-Sampler), and
  *   the host-side SlowFast controller dllm_slowfast_create / _observe /
@@ -357,6 +358,39 @@ dllm_status dllm_lock_criterion(const void* logits_cur, const void* logits_prev,
                                 uint8_t* locked_inout, void* ws,
                                 size_t ws_bytes, int32_t* dev_status,
                                 void* stream);
+
+/*
+ * dllm_lock_criterion_conf -- dllm_lock_criterion and the confidence of the
+ * current rows (dllm_confidence's outputs) from one read of the logits.
+ *
+ * SureLock, technical summary section 2: criterion 2's uncertainty is
+ * 1 - max_v p_t(v), the complement of the confidence that SlowFast (section
+ * 2, certainty principle) and LSP (technical summary section 2, step 1, with
+ * the logit margin) score the same rows by; both criteria read the current
+ * step's logits, so one pass over them yields every output.
+ *
+ *   Arguments as in dllm_lock_criterion (same workspace size), plus
+ *   conf_out    [B, out_cols] float32: max_j softmax_j of the current row.
+ *   argmax_out  [B, out_cols] int32: lowest index of its maximum logit.
+ *   margin_out  [B, out_cols] float32 or NULL: top-1 minus top-2 logit (0 on
+ *               a tie for the maximum).
+ * The columns written are those of kl_out, and conf_out equals 1 - unc_out
+ * before the clamp at 0.  V must be at least 2.  Errors: as
+ * dllm_lock_criterion, and INVALID_ARG for NULL conf_out or argmax_out.
+ */
+dllm_status dllm_lock_criterion_conf(const void* logits_cur,
+                                     const void* logits_prev, int dtype, int B,
+                                     int R_src, int V, int64_t row_stride,
+                                     int64_t batch_stride, int R_max,
+                                     const int32_t* row_idx,
+                                     const int32_t* count,
+                                     const int32_t* out_idx, int out_cols,
+                                     float eps, float gate_q, float* kl_out,
+                                     float* unc_out, float* conf_out,
+                                     int32_t* argmax_out, float* margin_out,
+                                     uint8_t* locked_inout, void* ws,
+                                     size_t ws_bytes, int32_t* dev_status,
+                                     void* stream);
 
 /*
  * dllm_adaptive_prefix -- the longest stable prefix with an adaptive

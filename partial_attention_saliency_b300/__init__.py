@@ -25,6 +25,7 @@ from ._lib import (  # noqa: F401
     dllm_confidence_workspace_bytes,
     dllm_kv_scatter,
     dllm_lock_criterion,
+    dllm_lock_criterion_conf,
     dllm_lock_workspace_bytes,
     dllm_partial_attention,
     dllm_read_stream,

@@ -47,6 +47,8 @@ SIGNATURES = {
     "dllm_lock_workspace_bytes": (_SZ, [_I, _I, _I, _I]),
     "dllm_lock_criterion": (_I, [_P, _P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _F, _F,
                                  _P, _P, _P, _P, _SZ, _P, _P]),
+    "dllm_lock_criterion_conf": (_I, [_P, _P, _I, _I, _I, _I, _I64, _I64, _I, _P, _P, _P, _I, _F,
+                                      _F, _P, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "dllm_adaptive_prefix": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
     "dllm_attn_scores": (_I, [_P, _I, _I, _I, _I, _P, _P, _P]),
     "dllm_attn_sampler_select": (_I, [_P, _I, _I, _P, _F, _F, _I, _P, _P, _P, _P]),
@@ -326,6 +328,33 @@ def dllm_lock_criterion(logits_cur, logits_prev, eps: float, *, gate_q: float = 
     ``logits_cur``/``logits_prev`` [B, R_src, V] with identical strides.
     Returns (kl [B, out_cols], unc [B, out_cols], locked_inout or None).
     """
+    return _lock_call(False, logits_cur, logits_prev, eps, gate_q, R_max, row_idx, count,
+                      out_idx, out_cols, kl_out, unc_out, None, None, None, locked_inout, ws,
+                      dev_status, stream)[:3]
+
+
+def dllm_lock_criterion_conf(logits_cur, logits_prev, eps: float, *, gate_q: float = 0.0,
+                             R_max: Optional[int] = None, row_idx=None, count=None,
+                             out_idx=None, out_cols: Optional[int] = None, kl_out=None,
+                             unc_out=None, conf_out=None, argmax_out=None, margin_out=None,
+                             with_margin: bool = True, locked_inout=None, ws=None,
+                             dev_status=None, stream=None):
+    """dllm_lock_criterion plus the current rows' confidence, argmax and
+    margin (dllm_confidence's outputs) from one read of the logits.
+    Returns (kl, unc, locked_inout or None, conf, argmax, margin or None)."""
+    if margin_out is None and with_margin and logits_cur.dim() == 3:
+        B = logits_cur.shape[0]
+        cols = (logits_cur.shape[1] if R_max is None else int(R_max)) if out_cols is None \
+            else int(out_cols)
+        margin_out = torch.empty((B, cols), dtype=torch.float32, device=logits_cur.device)
+    return _lock_call(True, logits_cur, logits_prev, eps, gate_q, R_max, row_idx, count,
+                      out_idx, out_cols, kl_out, unc_out, conf_out, argmax_out, margin_out,
+                      locked_inout, ws, dev_status, stream)
+
+
+def _lock_call(conf: bool, logits_cur, logits_prev, eps, gate_q, R_max, row_idx, count, out_idx,
+               out_cols, kl_out, unc_out, conf_out, argmax_out, margin_out, locked_inout, ws,
+               dev_status, stream):
     lib = load_library()
     dt = _dtype(logits_cur, logits_prev)
     if logits_cur.dim() != 3 or logits_cur.shape != logits_prev.shape \
@@ -339,6 +368,15 @@ def dllm_lock_criterion(logits_cur, logits_prev, eps: float, *, gate_q: float = 
     unc_out = torch.empty((B, out_cols), dtype=torch.float32, device=dev) if unc_out is None else unc_out
     _need(kl_out, torch.float32, (B, out_cols), "kl_out")
     _need(unc_out, torch.float32, (B, out_cols), "unc_out")
+    if conf:
+        if conf_out is None:
+            conf_out = torch.empty((B, out_cols), dtype=torch.float32, device=dev)
+        if argmax_out is None:
+            argmax_out = torch.empty((B, out_cols), dtype=torch.int32, device=dev)
+        _need(conf_out, torch.float32, (B, out_cols), "conf_out")
+        _need(argmax_out, torch.int32, (B, out_cols), "argmax_out")
+        if margin_out is not None:
+            _need(margin_out, torch.float32, (B, out_cols), "margin_out")
     if locked_inout is not None:
         _need(locked_inout, torch.uint8, (B, out_cols), "locked_inout")
     for t, n in ((row_idx, "row_idx"), (out_idx, "out_idx")):
@@ -349,13 +387,17 @@ def dllm_lock_criterion(logits_cur, logits_prev, eps: float, *, gate_q: float = 
     need = lib.dllm_lock_workspace_bytes(B, R_max, V, dt)
     if ws is None:
         ws = torch.empty((max(int(need), 16),), dtype=torch.uint8, device=dev)
-    _check(lib.dllm_lock_criterion(_ptr(logits_cur), _ptr(logits_prev), dt, B, R_src, V,
-                                   logits_cur.stride(1), logits_cur.stride(0), R_max,
-                                   _ptr(row_idx), _ptr(count), _ptr(out_idx), out_cols,
-                                   float(eps), float(gate_q), _ptr(kl_out), _ptr(unc_out),
-                                   _ptr(locked_inout), _ptr(ws), ws.numel() * ws.element_size(),
-                                   _ptr(dev_status), _stream(stream)))
-    return kl_out, unc_out, locked_inout
+    common = (_ptr(logits_cur), _ptr(logits_prev), dt, B, R_src, V, logits_cur.stride(1),
+              logits_cur.stride(0), R_max, _ptr(row_idx), _ptr(count), _ptr(out_idx), out_cols,
+              float(eps), float(gate_q), _ptr(kl_out), _ptr(unc_out))
+    tail = (_ptr(locked_inout), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+            _stream(stream))
+    if conf:
+        _check(lib.dllm_lock_criterion_conf(*common, _ptr(conf_out), _ptr(argmax_out),
+                                            _ptr(margin_out), *tail))
+    else:
+        _check(lib.dllm_lock_criterion(*common, *tail))
+    return kl_out, unc_out, locked_inout, conf_out, argmax_out, margin_out
 
 
 def dllm_adaptive_prefix(score, start, lo: float, hi: float, *, advance_start: bool = False,

@@ -70,6 +70,45 @@ bool valid_dtype(int dt) { return dt == DLLM_F32 || dt == DLLM_BF16; }
     if (!(cond)) return fail(DLLM_ERR_INVALID_ARG, __VA_ARGS__); \
   } while (0)
 
+// The checks and the launch of dllm_lock_criterion and dllm_lock_criterion_conf
+// (conf_out NULL: the criterion alone).
+dllm_status lock_criterion_call(const char* name, const void* logits_cur,
+                                const void* logits_prev, int dtype, int B, int R_src, int V,
+                                int64_t row_stride, int64_t batch_stride, int R_max,
+                                const int32_t* row_idx, const int32_t* count,
+                                const int32_t* out_idx, int out_cols, float eps, float gate_q,
+                                float* kl_out, float* unc_out, float* conf_out,
+                                int32_t* argmax_out, float* margin_out, uint8_t* locked_inout,
+                                void* ws, size_t ws_bytes, int32_t* dev_status, void* stream) {
+  REQUIRE(logits_cur && logits_prev && kl_out && unc_out, "%s: NULL logits or output pointer",
+          name);
+  REQUIRE(valid_dtype(dtype), "%s: unknown dtype %d", name, dtype);
+  REQUIRE(B >= 1 && R_src >= 1 && R_max >= 1, "%s: B=%d R_src=%d R_max=%d", name, B, R_src,
+          R_max);
+  REQUIRE(V >= 1, "%s: V=%d must be >= 1", name, V);
+  REQUIRE(row_stride >= V, "%s: row_stride %lld < V", name, (long long)row_stride);
+  REQUIRE(B == 1 || batch_stride >= (int64_t)R_src * row_stride, "%s: batch_stride too small",
+          name);
+  // as in dllm_confidence: rows past R_src without row_idx are caught on the device
+  REQUIRE(row_idx != nullptr || count != nullptr || R_max <= R_src,
+          "%s: R_max > R_src without row_idx or count", name);
+  REQUIRE(out_cols >= 1 && (out_idx != nullptr || R_max <= out_cols), "%s: out_cols %d too small",
+          name, out_cols);
+  REQUIRE(locked_inout == nullptr || R_max <= 16384, "%s: R_max %d above 16384 with lock flags",
+          name, R_max);
+  REQUIRE((int64_t)B * R_max <= 2147483647, "%s: B*R_max too large", name);
+  const size_t need = dllm::lock_workspace_bytes(B, R_max, V, dtype);
+  REQUIRE(ws != nullptr && ws_bytes >= need, "%s: workspace %zu bytes < %zu required", name,
+          ws_bytes, need);
+  REQUIRE(reinterpret_cast<uintptr_t>(ws) % 16 == 0, "%s: workspace misaligned", name);
+  return from_cuda(dllm::launch_lock_criterion(logits_cur, logits_prev, dtype, B, R_src, V,
+                                               row_stride, batch_stride, R_max, row_idx, count,
+                                               out_idx, out_cols, eps, gate_q, kl_out, unc_out,
+                                               conf_out, argmax_out, margin_out, locked_inout,
+                                               ws, dev_status, static_cast<cudaStream_t>(stream)),
+                   "lock criterion launch");
+}
+
 }  // namespace
 
 extern "C" {
@@ -243,33 +282,26 @@ dllm_status dllm_lock_criterion(const void* logits_cur, const void* logits_prev,
                                 float eps, float gate_q, float* kl_out, float* unc_out,
                                 uint8_t* locked_inout, void* ws, size_t ws_bytes,
                                 int32_t* dev_status, void* stream) {
-  REQUIRE(logits_cur && logits_prev && kl_out && unc_out,
-          "dllm_lock_criterion: NULL logits or output pointer");
-  REQUIRE(valid_dtype(dtype), "dllm_lock_criterion: unknown dtype %d", dtype);
-  REQUIRE(B >= 1 && R_src >= 1 && R_max >= 1, "dllm_lock_criterion: B=%d R_src=%d R_max=%d", B,
-          R_src, R_max);
-  REQUIRE(V >= 1, "dllm_lock_criterion: V=%d must be >= 1", V);
-  REQUIRE(row_stride >= V, "dllm_lock_criterion: row_stride %lld < V", (long long)row_stride);
-  REQUIRE(B == 1 || batch_stride >= (int64_t)R_src * row_stride,
-          "dllm_lock_criterion: batch_stride too small");
-  // as in dllm_confidence: rows past R_src without row_idx are caught on the device
-  REQUIRE(row_idx != nullptr || count != nullptr || R_max <= R_src,
-          "dllm_lock_criterion: R_max > R_src without row_idx or count");
-  REQUIRE(out_cols >= 1 && (out_idx != nullptr || R_max <= out_cols),
-          "dllm_lock_criterion: out_cols %d too small", out_cols);
-  REQUIRE(locked_inout == nullptr || R_max <= 16384,
-          "dllm_lock_criterion: R_max %d above 16384 with lock flags", R_max);
-  REQUIRE((int64_t)B * R_max <= 2147483647, "dllm_lock_criterion: B*R_max too large");
-  const size_t need = dllm::lock_workspace_bytes(B, R_max, V, dtype);
-  REQUIRE(ws != nullptr && ws_bytes >= need,
-          "dllm_lock_criterion: workspace %zu bytes < %zu required", ws_bytes, need);
-  REQUIRE(reinterpret_cast<uintptr_t>(ws) % 16 == 0, "dllm_lock_criterion: workspace misaligned");
-  return from_cuda(dllm::launch_lock_criterion(logits_cur, logits_prev, dtype, B, R_src, V,
-                                               row_stride, batch_stride, R_max, row_idx, count,
-                                               out_idx, out_cols, eps, gate_q, kl_out, unc_out,
-                                               locked_inout, ws, dev_status,
-                                               static_cast<cudaStream_t>(stream)),
-                   "dllm_lock_criterion launch");
+  return lock_criterion_call("dllm_lock_criterion", logits_cur, logits_prev, dtype, B, R_src, V,
+                             row_stride, batch_stride, R_max, row_idx, count, out_idx, out_cols,
+                             eps, gate_q, kl_out, unc_out, nullptr, nullptr, nullptr,
+                             locked_inout, ws, ws_bytes, dev_status, stream);
+}
+
+dllm_status dllm_lock_criterion_conf(const void* logits_cur, const void* logits_prev, int dtype,
+                                     int B, int R_src, int V, int64_t row_stride,
+                                     int64_t batch_stride, int R_max, const int32_t* row_idx,
+                                     const int32_t* count, const int32_t* out_idx, int out_cols,
+                                     float eps, float gate_q, float* kl_out, float* unc_out,
+                                     float* conf_out, int32_t* argmax_out, float* margin_out,
+                                     uint8_t* locked_inout, void* ws, size_t ws_bytes,
+                                     int32_t* dev_status, void* stream) {
+  REQUIRE(conf_out && argmax_out, "dllm_lock_criterion_conf: NULL conf_out or argmax_out");
+  REQUIRE(V >= 2, "dllm_lock_criterion_conf: V=%d must be >= 2", V);
+  return lock_criterion_call("dllm_lock_criterion_conf", logits_cur, logits_prev, dtype, B, R_src,
+                             V, row_stride, batch_stride, R_max, row_idx, count, out_idx,
+                             out_cols, eps, gate_q, kl_out, unc_out, conf_out, argmax_out,
+                             margin_out, locked_inout, ws, ws_bytes, dev_status, stream);
 }
 
 dllm_status dllm_adaptive_prefix(const float* score, int B, int L, int32_t* start, float lo,

@@ -64,8 +64,9 @@ cudaError_t launch_lock_criterion(const void* z, const void* y, int dtype, int B
                                   int V, int64_t rs, int64_t bs, int R_max,
                                   const int32_t* row_idx, const int32_t* count,
                                   const int32_t* out_idx, int out_cols, float eps, float gate_q,
-                                  float* kl_out, float* unc_out, uint8_t* locked, void* ws,
-                                  int32_t* dev_status, cudaStream_t stream);
+                                  float* kl_out, float* unc_out, float* conf_out,
+                                  int32_t* argmax_out, float* margin_out, uint8_t* locked,
+                                  void* ws, int32_t* dev_status, cudaStream_t stream);
 
 cudaError_t launch_adaptive_prefix(const float* score, int B, int L, int32_t* start, float lo,
                                    float hi, int advance_start, int32_t* len_out, float* tau_out,

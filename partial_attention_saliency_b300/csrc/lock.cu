@@ -56,8 +56,34 @@ constexpr int kGateMaxRows = 16384;  // uncertainty keys held in shared memory (
 constexpr int kLockMaxB = 64;        // batch rows the persistent partial kernel stages
 
 struct LockPartial {
-  float mz, lz, a, my, ly, pad0, pad1, pad2;  // 32 bytes
+  float mz, lz, a, my, ly;
+  float m2z;   // with the confidence: second largest current logit (mz on a tie)
+  int argz;    // with the confidence: lowest index of mz
+  float pad;   // 32 bytes
 };
+
+// Shared scratch of one CTA's reduction.
+struct LockRed {
+  float max[2][kLockThreads / 32];
+  float sum[3][kLockThreads / 32];
+  float m2[kLockThreads / 32];  // with the confidence
+  int arg[kLockThreads / 32];
+};
+
+// (top, second, lowest index of top) of two sets, the second counting ties.
+__device__ __forceinline__ void top2_merge(float& m1, float& m2, int& arg, float o1, float o2,
+                                           int oa) {
+  if (o1 > m1) {
+    m2 = fmaxf(o2, m1);
+    m1 = o1;
+    arg = oa;
+  } else if (o1 < m1) {
+    m2 = fmaxf(m2, o1);
+  } else {
+    m2 = m1;
+    arg = min(arg, oa);
+  }
+}
 
 template <typename T> __host__ __device__ constexpr int lvec() { return 16 / (int)sizeof(T); }
 template <typename T> __host__ __device__ constexpr int lock_chunk_elems() {
@@ -135,24 +161,48 @@ __device__ __forceinline__ void lock_load(const T* zrow, const T* yrow, int V, i
 }
 
 // The partial of one (row, chunk) from the CTA's loaded vectors; thread 0
-// writes it to *out_slot.
-template <typename T>
+// writes it to *out_slot.  CONF: also the top two current logits and the
+// lowest index of the top one.
+template <typename T, bool CONF>
 __device__ __forceinline__ void lock_reduce(const uint4 (&vz)[kLockU], const uint4 (&vy)[kLockU],
-                                            LockPartial* out_slot,
-                                            float (&red_max)[2][kLockThreads / 32],
-                                            float (&red_sum)[3][kLockThreads / 32]) {
+                                            int chunk, LockPartial* out_slot, LockRed& red) {
   constexpr int E = lvec<T>();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   // 1. this thread's maxima and its sums relative to them: no block-wide
   //    step before the exponentials
-  float mz = -INFINITY, my = -INFINITY;
+  float mz = -INFINITY, my = -INFINITY, m2z = -INFINITY;
+  int argz = INT_MAX;
+  if constexpr (CONF) {
 #pragma unroll
-  for (int u = 0; u < kLockU; ++u)
+    for (int u = 0; u < kLockU; ++u)
 #pragma unroll
-    for (int e = 0; e < E; e += 2) {
-      mz = fmax3(mz, lelem<T>(vz[u], e), lelem<T>(vz[u], e + 1));
-      my = fmax3(my, lelem<T>(vy[u], e), lelem<T>(vy[u], e + 1));
+      for (int e = 0; e < E; ++e) {
+        const float x = lelem<T>(vz[u], e);
+        m2z = fmaxf(m2z, fminf(mz, x));
+        mz = fmaxf(mz, x);
+      }
+#pragma unroll
+    for (int u = 0; u < kLockU; ++u)
+#pragma unroll
+      for (int e = 0; e < E; e += 2) my = fmax3(my, lelem<T>(vy[u], e), lelem<T>(vy[u], e + 1));
+    if (mz != -INFINITY) {
+      // elements ascend with u, then e: the first match is the lowest index
+      const int vbase = chunk * (kLockThreads * kLockU);
+#pragma unroll
+      for (int u = kLockU - 1; u >= 0; --u)
+#pragma unroll
+        for (int e = E - 1; e >= 0; --e)
+          if (lelem<T>(vz[u], e) == mz) argz = (vbase + u * kLockThreads + (int)threadIdx.x) * E + e;
     }
+  } else {
+#pragma unroll
+    for (int u = 0; u < kLockU; ++u)
+#pragma unroll
+      for (int e = 0; e < E; e += 2) {
+        mz = fmax3(mz, lelem<T>(vz[u], e), lelem<T>(vz[u], e + 1));
+        my = fmax3(my, lelem<T>(vy[u], e), lelem<T>(vy[u], e + 1));
+      }
+  }
   float lz = 0.f, a = 0.f, ly = 0.f;
   if (mz != -INFINITY) {
     const float nz = -mz * kLog2e, ny = -my * kLog2e;
@@ -180,17 +230,46 @@ __device__ __forceinline__ void lock_reduce(const uint4 (&vz)[kLockU], const uin
       }
   }
   // 2. block maxima (one exchange), each thread rescales its own sums
-  const float wz = warp_max(mz), wy = warp_max(my);
+  float wz = mz;
+  if constexpr (CONF) {
+    float w2 = m2z;
+    int wa = argz;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const float o1 = __shfl_xor_sync(0xffffffffu, wz, off);
+      const float o2 = __shfl_xor_sync(0xffffffffu, w2, off);
+      const int oa = __shfl_xor_sync(0xffffffffu, wa, off);
+      top2_merge(wz, w2, wa, o1, o2, oa);
+    }
+    if (lane == 0) {
+      red.m2[warp] = w2;
+      red.arg[warp] = wa;
+    }
+  } else {
+    wz = warp_max(mz);
+  }
+  const float wy = warp_max(my);
   if (lane == 0) {
-    red_max[0][warp] = wz;
-    red_max[1][warp] = wy;
+    red.max[0][warp] = wz;
+    red.max[1][warp] = wy;
   }
   __syncthreads();
-  float Mz = red_max[0][0], My = red_max[1][0];
+  float Mz = red.max[0][0], My = red.max[1][0];
 #pragma unroll
   for (int w = 1; w < kLockThreads / 32; ++w) {
-    Mz = fmaxf(Mz, red_max[0][w]);
-    My = fmaxf(My, red_max[1][w]);
+    Mz = fmaxf(Mz, red.max[0][w]);
+    My = fmaxf(My, red.max[1][w]);
+  }
+  // the block's second logit and index, read before the next barrier (after
+  // it, a warp may already be writing the next item's maxima)
+  float bm2 = -INFINITY;
+  int barg = INT_MAX;
+  if (CONF && threadIdx.x == 0) {
+    float m1 = red.max[0][0];
+    bm2 = red.m2[0];
+    barg = red.arg[0];
+    for (int w = 1; w < kLockThreads / 32; ++w)  // fixed order
+      top2_merge(m1, bm2, barg, red.max[0][w], red.m2[w], red.arg[w]);
   }
   const float cz = mz == -INFINITY ? 0.f : ex2_approx((mz - Mz) * kLog2e);
   const float cy = my == -INFINITY ? 0.f : ex2_approx((my - My) * kLog2e);
@@ -198,9 +277,9 @@ __device__ __forceinline__ void lock_reduce(const uint4 (&vz)[kLockU], const uin
   a = warp_sum(a * cz);
   ly = warp_sum(ly * cy);
   if (lane == 0) {
-    red_sum[0][warp] = lz;
-    red_sum[1][warp] = a;
-    red_sum[2][warp] = ly;
+    red.sum[0][warp] = lz;
+    red.sum[1][warp] = a;
+    red.sum[2][warp] = ly;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -209,25 +288,26 @@ __device__ __forceinline__ void lock_reduce(const uint4 (&vz)[kLockU], const uin
     out.my = My;
     out.lz = out.a = out.ly = 0.f;
     for (int w = 0; w < kLockThreads / 32; ++w) {  // fixed order
-      out.lz += red_sum[0][w];
-      out.a += red_sum[1][w];
-      out.ly += red_sum[2][w];
+      out.lz += red.sum[0][w];
+      out.a += red.sum[1][w];
+      out.ly += red.sum[2][w];
     }
-    out.pad0 = out.pad1 = out.pad2 = 0.f;
+    out.m2z = bm2;
+    out.argz = barg;
+    out.pad = 0.f;
     *out_slot = out;
   }
 }
 
 // One CTA per (row slot, chunk): slots past their batch row's count exit at
 // once.  For batch counts beyond kLockMaxB.
-template <typename T, bool VEC>
+template <typename T, bool VEC, bool CONF>
 __global__ void __launch_bounds__(kLockThreads, DLLM_LOCK_MINB)
 lock_partial_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs, int64_t bs, int R_max,
                     const int32_t* row_idx, const int32_t* count, int nchunks, LockPartial* ws) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  __shared__ float red_max[2][kLockThreads / 32];
-  __shared__ float red_sum[3][kLockThreads / 32];
+  __shared__ LockRed red;
   const int br = blockIdx.x, chunk = blockIdx.y;
   const int b = br / R_max, r = br - b * R_max;
   int row;
@@ -236,7 +316,7 @@ lock_partial_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs, int6
   uint4 vz[kLockU], vy[kLockU];
   lock_load<T, VEC>(zs + (int64_t)b * bs + (int64_t)row * rs,
                     ys + (int64_t)b * bs + (int64_t)row * rs, V, chunk, vz, vy);
-  lock_reduce<T>(vz, vy, ws + (int64_t)br * nchunks + chunk, red_max, red_sum);
+  lock_reduce<T, CONF>(vz, vy, chunk, ws + (int64_t)br * nchunks + chunk, red);
 }
 
 // Persistent: the CTAs take the valid (row, chunk) items, row-major, dealt
@@ -245,15 +325,14 @@ lock_partial_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs, int6
 // window with 124 active rows per batch row took 108 us, this kernel 83 us;
 // 77 us and 81 us with 128 slots).  Rows whose index is out of range are
 // skipped (the merge kernel reports them).
-template <typename T, bool VEC>
+template <typename T, bool VEC, bool CONF>
 __global__ void __launch_bounds__(kLockThreads, DLLM_LOCK_MINB)
 lock_partial_persistent_kernel(const T* zs, const T* ys, int R_src, int V, int64_t rs,
                                int64_t bs, int B, int R_max, const int32_t* row_idx,
                                const int32_t* count, int nchunks, LockPartial* ws) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
-  __shared__ float red_max[2][kLockThreads / 32];
-  __shared__ float red_sum[3][kLockThreads / 32];
+  __shared__ LockRed red;
   __shared__ int s_pre[kLockMaxB + 1];  // valid rows before each batch row
   if (threadIdx.x == 0) {
     int acc = 0;
@@ -295,17 +374,27 @@ lock_partial_persistent_kernel(const T* zs, const T* ys, int R_src, int V, int64
   uint4 za[kLockU], ya[kLockU];
   while (next(v, &v, &zr, &yr, &chunk, &slot)) {
     lock_load<T, VEC>(zr, yr, V, chunk, za, ya);
-    lock_reduce<T>(za, ya, slot, red_max, red_sum);
+    lock_reduce<T, CONF>(za, ya, chunk, slot, red);
     v += gridDim.x;
   }
 }
 
 struct LockAcc {
-  float mz, lz, a, my, ly;
+  float mz, lz, a, my, ly, m2z;
+  int argz;
 };
 
+template <bool CONF>
 __device__ __forceinline__ LockAcc lock_fold(const LockAcc& p, const LockAcc& q) {
   LockAcc r;
+  r.m2z = -INFINITY;
+  r.argz = INT_MAX;
+  if constexpr (CONF) {
+    float m1 = p.mz;
+    r.m2z = p.m2z;
+    r.argz = p.argz;
+    top2_merge(m1, r.m2z, r.argz, q.mz, q.m2z, q.argz);
+  }
   r.mz = fmaxf(p.mz, q.mz);
   r.my = fmaxf(p.my, q.my);
   const float cp = p.mz == -INFINITY ? 0.f : ex2_approx((p.mz - r.mz) * kLog2e);
@@ -318,10 +407,12 @@ __device__ __forceinline__ LockAcc lock_fold(const LockAcc& p, const LockAcc& q)
   return r;
 }
 
+template <bool CONF>
 __global__ void lock_merge_kernel(int B, int R_src, int R_max, const int32_t* row_idx,
                                   const int32_t* count, const int32_t* out_idx, int out_cols,
                                   int nchunks, const LockPartial* ws, float* kl_out,
-                                  float* unc_out, int32_t* dev_status) {
+                                  float* unc_out, float* conf_out, int32_t* argmax_out,
+                                  float* margin_out, int32_t* dev_status) {
   pdl_wait();  // the previous kernel on the stream has completed
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -341,11 +432,11 @@ __global__ void lock_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
       return;
     }
   }
-  LockAcc acc{-INFINITY, 0.f, 0.f, -INFINITY, 0.f};
+  LockAcc acc{-INFINITY, 0.f, 0.f, -INFINITY, 0.f, -INFINITY, INT_MAX};
   for (int c = lane; c < nchunks; c += 32) {
     const float4* src = reinterpret_cast<const float4*>(ws + br * nchunks + c);
     const float4 p0 = __ldca(src), p1 = __ldca(src + 1);
-    acc = lock_fold(acc, LockAcc{p0.x, p0.y, p0.z, p0.w, p1.x});
+    acc = lock_fold<CONF>(acc, LockAcc{p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, __float_as_int(p1.z)});
   }
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) {
@@ -355,7 +446,13 @@ __global__ void lock_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
     o.a = __shfl_xor_sync(0xffffffffu, acc.a, off);
     o.my = __shfl_xor_sync(0xffffffffu, acc.my, off);
     o.ly = __shfl_xor_sync(0xffffffffu, acc.ly, off);
-    acc = lock_fold(acc, o);
+    o.m2z = -INFINITY;
+    o.argz = INT_MAX;
+    if constexpr (CONF) {
+      o.m2z = __shfl_xor_sync(0xffffffffu, acc.m2z, off);
+      o.argz = __shfl_xor_sync(0xffffffffu, acc.argz, off);
+    }
+    acc = lock_fold<CONF>(acc, o);
   }
   if (lane == 0) {
     const double lse_z = (double)acc.mz + log((double)acc.lz);
@@ -365,6 +462,11 @@ __global__ void lock_merge_kernel(int B, int R_src, int R_max, const int32_t* ro
     kl_out[o] = (float)kl;
     // lz >= 1 up to rounding (the largest term is exp(0)): clamp at 0
     unc_out[o] = fmaxf(1.0f - 1.0f / acc.lz, 0.0f);
+    if constexpr (CONF) {
+      conf_out[o] = 1.0f / acc.lz;
+      argmax_out[o] = acc.argz;
+      if (margin_out != nullptr) margin_out[o] = acc.mz - acc.m2z;
+    }
   }
 }
 
@@ -555,13 +657,14 @@ int lock_nchunks(int V) {
   return n < 1 ? 1 : n;
 }
 
-template <typename T>
-cudaError_t launch_lock_typed(const T* z, const T* y, int B, int R_src, int V, int64_t rs,
-                              int64_t bs, int R_max, const int32_t* row_idx,
-                              const int32_t* count, const int32_t* out_idx, int out_cols,
-                              float eps, float gate_q, float* kl_out, float* unc_out,
-                              uint8_t* locked, void* ws, int32_t* dev_status,
-                              cudaStream_t stream) {
+template <typename T, bool CONF>
+cudaError_t launch_lock_variant(const T* z, const T* y, int B, int R_src, int V, int64_t rs,
+                                int64_t bs, int R_max, const int32_t* row_idx,
+                                const int32_t* count, const int32_t* out_idx, int out_cols,
+                                float eps, float gate_q, float* kl_out, float* unc_out,
+                                float* conf_out, int32_t* argmax_out, float* margin_out,
+                                uint8_t* locked, void* ws, int32_t* dev_status,
+                                cudaStream_t stream) {
   constexpr int E = lvec<T>();
   const int nchunks = lock_nchunks<T>(V);
   if (nchunks > 65535 || (int64_t)B * R_max > INT_MAX) return cudaErrorInvalidConfiguration;
@@ -574,25 +677,26 @@ cudaError_t launch_lock_typed(const T* z, const T* y, int B, int R_src, int V, i
     const int64_t cap = (int64_t)num_sms() * DLLM_LOCK_MINB;
     const int grid = (int)(items < cap ? items : cap);
     if (vec)
-      launch_pdl(lock_partial_persistent_kernel<T, true>, grid, kLockThreads, 0, stream, z, y,
-                 R_src, V, rs, bs, B, R_max, row_idx, count, nchunks, part);
+      launch_pdl(lock_partial_persistent_kernel<T, true, CONF>, grid, kLockThreads, 0, stream,
+                 z, y, R_src, V, rs, bs, B, R_max, row_idx, count, nchunks, part);
     else
-      launch_pdl(lock_partial_persistent_kernel<T, false>, grid, kLockThreads, 0, stream, z, y,
-                 R_src, V, rs, bs, B, R_max, row_idx, count, nchunks, part);
+      launch_pdl(lock_partial_persistent_kernel<T, false, CONF>, grid, kLockThreads, 0, stream,
+                 z, y, R_src, V, rs, bs, B, R_max, row_idx, count, nchunks, part);
   } else {
     dim3 grid(B * R_max, nchunks);
     if (vec)
-      launch_pdl(lock_partial_kernel<T, true>, grid, kLockThreads, 0, stream, z, y, R_src, V,
-                 rs, bs, R_max, row_idx, count, nchunks, part);
+      launch_pdl(lock_partial_kernel<T, true, CONF>, grid, kLockThreads, 0, stream, z, y, R_src,
+                 V, rs, bs, R_max, row_idx, count, nchunks, part);
     else
-      launch_pdl(lock_partial_kernel<T, false>, grid, kLockThreads, 0, stream, z, y, R_src, V,
-                 rs, bs, R_max, row_idx, count, nchunks, part);
+      launch_pdl(lock_partial_kernel<T, false, CONF>, grid, kLockThreads, 0, stream, z, y, R_src,
+                 V, rs, bs, R_max, row_idx, count, nchunks, part);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t rows = (int64_t)B * R_max;
-  launch_pdl(lock_merge_kernel, (unsigned)((rows + 7) / 8), 256, 0, stream, B, R_src, R_max,
-             row_idx, count, out_idx, out_cols, nchunks, part, kl_out, unc_out, dev_status);
+  launch_pdl(lock_merge_kernel<CONF>, (unsigned)((rows + 7) / 8), 256, 0, stream, B, R_src,
+             R_max, row_idx, count, out_idx, out_cols, nchunks, part, kl_out, unc_out, conf_out,
+             argmax_out, margin_out, dev_status);
   e = cudaGetLastError();
   if (e != cudaSuccess || locked == nullptr) return e;
   const size_t smem = (size_t)R_max * sizeof(uint32_t);
@@ -606,6 +710,23 @@ cudaError_t launch_lock_typed(const T* z, const T* y, int B, int R_src, int V, i
   return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t launch_lock_typed(const T* z, const T* y, int B, int R_src, int V, int64_t rs,
+                              int64_t bs, int R_max, const int32_t* row_idx,
+                              const int32_t* count, const int32_t* out_idx, int out_cols,
+                              float eps, float gate_q, float* kl_out, float* unc_out,
+                              float* conf_out, int32_t* argmax_out, float* margin_out,
+                              uint8_t* locked, void* ws, int32_t* dev_status,
+                              cudaStream_t stream) {
+  if (conf_out != nullptr)
+    return launch_lock_variant<T, true>(z, y, B, R_src, V, rs, bs, R_max, row_idx, count,
+                                        out_idx, out_cols, eps, gate_q, kl_out, unc_out, conf_out,
+                                        argmax_out, margin_out, locked, ws, dev_status, stream);
+  return launch_lock_variant<T, false>(z, y, B, R_src, V, rs, bs, R_max, row_idx, count, out_idx,
+                                       out_cols, eps, gate_q, kl_out, unc_out, nullptr, nullptr,
+                                       nullptr, locked, ws, dev_status, stream);
+}
+
 }  // namespace
 
 size_t lock_workspace_bytes(int B, int R_max, int V, int dtype) {
@@ -617,16 +738,18 @@ cudaError_t launch_lock_criterion(const void* z, const void* y, int dtype, int B
                                   int V, int64_t rs, int64_t bs, int R_max,
                                   const int32_t* row_idx, const int32_t* count,
                                   const int32_t* out_idx, int out_cols, float eps, float gate_q,
-                                  float* kl_out, float* unc_out, uint8_t* locked, void* ws,
-                                  int32_t* dev_status, cudaStream_t stream) {
+                                  float* kl_out, float* unc_out, float* conf_out,
+                                  int32_t* argmax_out, float* margin_out, uint8_t* locked,
+                                  void* ws, int32_t* dev_status, cudaStream_t stream) {
   if (dtype == DLLM_BF16)
     return launch_lock_typed(static_cast<const __nv_bfloat16*>(z),
                              static_cast<const __nv_bfloat16*>(y), B, R_src, V, rs, bs, R_max,
                              row_idx, count, out_idx, out_cols, eps, gate_q, kl_out, unc_out,
-                             locked, ws, dev_status, stream);
+                             conf_out, argmax_out, margin_out, locked, ws, dev_status, stream);
   return launch_lock_typed(static_cast<const float*>(z), static_cast<const float*>(y), B, R_src,
                            V, rs, bs, R_max, row_idx, count, out_idx, out_cols, eps, gate_q,
-                           kl_out, unc_out, locked, ws, dev_status, stream);
+                           kl_out, unc_out, conf_out, argmax_out, margin_out, locked, ws,
+                           dev_status, stream);
 }
 
 cudaError_t launch_adaptive_prefix(const float* score, int B, int L, int32_t* start, float lo,

@@ -113,6 +113,16 @@ def test_lock_and_adaptive_prefix_rejected_before_launch(lib):
     st = lib.dllm_lock_criterion(p, p, 1, 1, 4, 64, 64, 256, 20000, p, None, p, 20000, 0.1, 0.5,
                                  p, p, p, p, big, None, None)
     assert st == 1 and b"16384" in lib.dllm_last_error()
+
+    def lock_conf(conf=p, am=p, V=64, rs=64):
+        return lib.dllm_lock_criterion_conf(p, p, 1, 1, 4, V, rs, 4 * rs, 4, None, None, None, 4,
+                                            0.1, 0.5, p, p, conf, am, None, None, p, big, None,
+                                            None)
+
+    assert lock_conf(conf=None) == 1 and b"conf_out" in lib.dllm_last_error()
+    assert lock_conf(am=None) == 1 and b"argmax_out" in lib.dllm_last_error()
+    assert lock_conf(V=1, rs=1) == 1 and b"V=1" in lib.dllm_last_error()
+    assert lock_conf(rs=32) == 1 and b"row_stride" in lib.dllm_last_error()
     st = lib.dllm_adaptive_prefix(None, 1, 16, p, 0.25, 0.5, 0, p, p, None, None)
     assert st == 1 and b"NULL" in lib.dllm_last_error()
     st = lib.dllm_adaptive_prefix(p, 1, 16, p, 0.25, 1.5, 0, p, p, None, None)

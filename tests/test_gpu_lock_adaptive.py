@@ -229,3 +229,98 @@ def test_adaptive_prefix_bad_start_reports(dl):
                                         0.1, 0.5, dev_status=st)
     torch.cuda.synchronize()
     assert int(st[0]) != 0 and int(length[1]) == 0
+
+
+# ------------------------------------------------ criterion with the confidence
+
+CONF_RTOL = 1e-4  # float32 sum of up to 126464 exponentials, as for dllm_confidence
+
+
+def _check_conf(conf, am, mg, rc, ra, rm, mask):
+    assert np.array_equal(i32_(am)[mask], ra[mask])
+    g, r = f64(conf)[mask], rc[mask]
+    assert np.all(np.abs(g - r) <= 1e-6 + CONF_RTOL * np.abs(r)), np.max(np.abs(g - r) / r)
+    assert np.max(np.abs(f64(mg)[mask] - rm[mask]), initial=0.0) <= 1e-6
+
+
+def i32_(t):
+    return t.detach().cpu().numpy().astype(np.int64)
+
+
+@pytest.mark.parametrize("dtype,V,B", [(torch.float32, 301, 3), (torch.bfloat16, 1000, 3),
+                                       (torch.bfloat16, 126464, 3), (torch.bfloat16, 1000, 65),
+                                       (torch.float32, 4096, 65)])
+def test_lock_conf_matches_oracle(dl, dtype, V, B):
+    """dllm_lock_criterion_conf: the divergences and uncertainties of the
+    criterion and the confidence, argmax and margin of the current rows, with
+    ragged counts (persistent partial kernel at 3 batch rows, one CTA per row
+    slot at 65), against the oracle's lock_kl and confidence."""
+    g = torch.Generator().manual_seed(V + B)
+    R = 9
+    z, y = _pair(g, B, R, V, dtype, 1.0)
+    count = torch.tensor([(5 * b + 3) % (R + 1) for b in range(B)], dtype=torch.int32)
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    kl, unc, _, conf, am, mg = dl.dllm_lock_criterion_conf(z.cuda(), y.cuda(), 0.0,
+                                                           count=count.cuda(), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    mask = np.arange(R)[None, :] < count.numpy()[:, None]
+    ref_kl, ref_unc = oracle.lock_kl(f64(z), f64(y))
+    _check_kl(kl, unc, ref_kl, ref_unc, mask)
+    rc, ra, rm = oracle.confidence(f64(z))
+    _check_conf(conf, am, mg, rc, ra, rm, mask)
+    # the uncertainty is the complement of the confidence, before its clamp at 0
+    assert np.array_equal(f64(unc)[mask], np.maximum(1.0 - f64(conf)[mask].astype(np.float32), 0))
+
+
+def test_lock_conf_ties_gather_scatter_flags(dl):
+    """Ties for the maximum inside one chunk and across chunks (argmax the
+    lowest index, margin 0), rows gathered by index and results scattered to
+    positions, lock flags, and the same outputs as dllm_confidence and
+    dllm_lock_criterion called separately on the same rows."""
+    g = torch.Generator().manual_seed(23)
+    B, R_src, V, L, R_max = 2, 12, 126464, 64, 8
+    z, y = _pair(g, B, R_src, V, torch.bfloat16, 2.0)
+    top = float(z.float().max()) + 1.0
+    z[0, 0, 5] = z[0, 0, 7] = top          # tie inside the first chunk
+    z[0, 1, 100] = z[0, 1, 120000] = top   # tie across chunks: the lower index wins
+    z[1, 2, V - 1] = top                   # maximum on the last element of the row
+    count = torch.tensor([8, 5], dtype=torch.int32)
+    row_idx = torch.stack([torch.arange(R_max), torch.arange(R_max) + 2]).int()
+    out_idx = torch.stack([torch.randperm(L, generator=g)[:R_max] for _ in range(B)]).int()
+    args = dict(gate_q=0.5, R_max=R_max, row_idx=row_idx.cuda(), count=count.cuda(),
+                out_idx=out_idx.cuda(), out_cols=L)
+    lk1 = torch.zeros((B, L), dtype=torch.uint8, device="cuda")
+    lk2 = lk1.clone()
+    st = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    zc, yc = z.cuda(), y.cuda()
+    kl, unc, _, conf, am, mg = dl.dllm_lock_criterion_conf(
+        zc, yc, 1e-2, locked_inout=lk1, conf_out=torch.full((B, L), -7.0, device="cuda"),
+        dev_status=st, **args)
+    kl2, unc2, _ = dl.dllm_lock_criterion(zc, yc, 1e-2, locked_inout=lk2, dev_status=st, **args)
+    conf2, am2, mg2 = dl.dllm_confidence(zc, R_max=R_max, row_idx=row_idx.cuda(),
+                                         count=count.cuda(), out_idx=out_idx.cuda(), out_cols=L,
+                                         dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st[0]) == 0
+    rc, ra, rm = oracle.confidence(f64(z), count=count.numpy(), row_idx=row_idx.numpy())
+    for b in range(B):
+        n = int(count[b])
+        cols = out_idx[b, :n].numpy()
+        m = np.ones(n, dtype=bool)
+        _check_conf(conf[b:b + 1, cols], am[b:b + 1, cols], mg[b:b + 1, cols],
+                    rc[b:b + 1, :n], ra[b:b + 1, :n], rm[b:b + 1, :n], m[None, :])
+        # against the two separate calls: the same criterion, argmax and margin
+        assert np.array_equal(f64(kl)[b, cols], f64(kl2)[b, cols])
+        assert np.array_equal(f64(unc)[b, cols], f64(unc2)[b, cols])
+        assert np.array_equal(i32_(am)[b, cols], i32_(am2)[b, cols])
+        assert np.array_equal(f64(mg)[b, cols], f64(mg2)[b, cols])
+        gc, sc = f64(conf)[b, cols], f64(conf2)[b, cols]
+        assert np.all(np.abs(gc - sc) <= 2 * CONF_RTOL * sc)
+        # columns of no row keep their values
+        rest = np.setdiff1d(np.arange(L), cols)
+        assert np.all(f64(conf)[b, rest] == -7.0)
+    assert i32_(am)[0, out_idx[0, 0]] == 5 and f64(mg)[0, out_idx[0, 0]] == 0.0
+    assert i32_(am)[0, out_idx[0, 1]] == 100 and f64(mg)[0, out_idx[0, 1]] == 0.0
+    assert i32_(am)[1, out_idx[1, 0]] == V - 1
+    assert torch.equal(lk1, lk2)
