@@ -102,7 +102,7 @@ TRAFFIC = {
     # the calls around the loop's step 1, single-kernel captures
     ("around_b4_2k", "dllm_approx_attention_update"): {"bytes": 160583680,
                                                        "src_sha": "d56bc4837a78c2c7"},
-    ("around_b4_2k", "dllm_lock_criterion"): {"bytes": 255105024, "src_sha": "3416aa225c42e91d"},
+    ("around_b4_2k", "dllm_lock_criterion"): {"bytes": 255105024, "src_sha": "25208f92b94a3400"},
     ("around_b4_2k", "dllm_attn_sampler_select"): {"bytes": 52480, "src_sha": "dccded94e04e80a9"},
 }
 

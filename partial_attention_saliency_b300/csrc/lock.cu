@@ -22,6 +22,12 @@
 // lock_merge_kernel    one warp per row folds the chunks in a fixed order and
 //                      evaluates KL = A / lz - (Mz + ln lz) + (My + ln ly) in
 //                      double; the uncertainty is 1 - 1 / lz.
+//                      With the confidence (a second instantiation of the
+//                      partial and merge kernels), the same pass also keeps
+//                      the top two current logits and the lowest index of the
+//                      top one, and the merge writes the confidence 1 / lz,
+//                      that index and the margin: dllm_confidence's outputs
+//                      without a second read of the current row.
 // lock_gate_kernel     one CTA per batch row: radix select of the k-th
 //                      smallest uncertainty among the active rows (the
 //                      percentile gate), then the lock flags (only ever set).
