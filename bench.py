@@ -60,9 +60,12 @@ CSRC = os.path.join(ROOT, "partial_attention_saliency_b300", "csrc")
 
 ENTRY_ORDER = ["dllm_saliency_select", "dllm_kv_scatter", "dllm_partial_attention",
                "dllm_attention_colsum", "dllm_confidence", "dllm_stable_prefix"]
-# the lock criterion between consecutive steps' logits and the adaptive prefix
-# threshold, appended to the step with --surelock
-SURELOCK_ORDER = ["dllm_lock_criterion", "dllm_adaptive_prefix"]
+# with --surelock: the lock criterion between consecutive steps' logits takes
+# the confidence's place (one call reads the current logits once for both),
+# and the adaptive prefix threshold follows the step
+SURELOCK_ORDER = ["dllm_saliency_select", "dllm_kv_scatter", "dllm_partial_attention",
+                  "dllm_attention_colsum", "dllm_lock_criterion_conf", "dllm_stable_prefix",
+                  "dllm_adaptive_prefix"]
 LOCK_EPS, LOCK_GATE_Q = 1e-3, 0.5     # KL threshold, uncertainty percentile gate
 ADAPT_LO, ADAPT_HI = 0.25, 0.5        # fraction of the active length the prefix covers
 KERNELS = {  # kernels each entry point launches, and the source they come from
@@ -76,6 +79,8 @@ KERNELS = {  # kernels each entry point launches, and the source they come from
     "dllm_stable_prefix": (["stable_prefix_kernel"], "stable_prefix.cu"),
     "dllm_lock_criterion": (["lock_partial_persistent_kernel", "lock_partial_kernel",
                              "lock_merge_kernel", "lock_gate_kernel"], "lock.cu"),
+    "dllm_lock_criterion_conf": (["lock_partial_persistent_kernel", "lock_partial_kernel",
+                                  "lock_merge_kernel", "lock_gate_kernel"], "lock.cu"),
     "dllm_adaptive_prefix": (["adaptive_prefix_kernel"], "lock.cu"),
     "dllm_approx_attention_update": (["approx_update_tc_kernel"], "approx_update_tc.cu"),
     "dllm_attn_scores": (["attn_scores_kernel"], "sampler.cu"),
@@ -102,7 +107,7 @@ TRAFFIC = {
     # the calls around the loop's step 1, single-kernel captures
     ("around_b4_2k", "dllm_approx_attention_update"): {"bytes": 160583680,
                                                        "src_sha": "d56bc4837a78c2c7"},
-    ("around_b4_2k", "dllm_lock_criterion"): {"bytes": 255105024, "src_sha": "25208f92b94a3400"},
+    ("around_b4_2k", "dllm_lock_criterion"): {"bytes": 254773760, "src_sha": "78d1876c6127b808"},
     ("around_b4_2k", "dllm_attn_sampler_select"): {"bytes": 52480, "src_sha": "dccded94e04e80a9"},
 }
 
@@ -391,7 +396,7 @@ class Workload:
 
 
 def entries(wl: "Workload"):
-    return ENTRY_ORDER + (SURELOCK_ORDER if wl.surelock else [])
+    return SURELOCK_ORDER if wl.surelock else ENTRY_ORDER
 
 
 def make_workload(args) -> Workload:
@@ -401,9 +406,10 @@ def make_workload(args) -> Workload:
             raise SystemExit("--surelock needs a long_4k workload (logits of every position)")
         wl = dataclasses.replace(
             wl, name=wl.name + "_surelock", surelock=True,
-            desc=wl.desc + f"; then the lock criterion (KL < {LOCK_EPS}, uncertainty gate at "
-                           f"the {round(100 * LOCK_GATE_Q)}th percentile) between these and the "
-                           f"previous step's logits of the active rows, and the adaptive prefix "
+            desc=wl.desc + f"; the confidence comes with the lock criterion (KL < {LOCK_EPS}, "
+                           f"uncertainty gate at the {round(100 * LOCK_GATE_Q)}th percentile) "
+                           f"between these and the previous step's logits of the active rows, "
+                           f"one call; after the prefix commit, the adaptive prefix "
                            f"({round(100 * ADAPT_LO)}-{round(100 * ADAPT_HI)}% of the active "
                            f"length)")
     return wl
@@ -576,6 +582,13 @@ def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None, locked=None)
         dl.dllm_confidence(d["logits"], out_cols=s.L, conf_out=d["score"][:, w:],
                            argmax_out=bf.argmax[:, w:], margin_out=bf.margin[:, w:],
                            ws=bf.conf_ws, dev_status=bf.dev_status, stream=stream)
+    elif wl.conf == "gather" and wl.surelock:
+        dl.dllm_lock_criterion_conf(d["logits"], d["logits_prev"], LOCK_EPS, gate_q=LOCK_GATE_Q,
+                                    R_max=s.Lw, row_idx=bf.idx, count=bf.count, out_idx=bf.idx,
+                                    out_cols=s.L, kl_out=bf.kl, unc_out=bf.unc,
+                                    conf_out=d["score"], argmax_out=bf.argmax,
+                                    margin_out=bf.margin, locked_inout=bf.lock_flags,
+                                    ws=bf.lock_ws, dev_status=bf.dev_status, stream=stream)
     elif wl.conf == "gather":
         dl.dllm_confidence(d["logits"], R_max=s.Lw, row_idx=bf.idx, count=bf.count,
                            out_idx=bf.idx, out_cols=s.L, conf_out=d["score"],
@@ -592,15 +605,9 @@ def run_step(dl, wl: Workload, bf: Buffers, d, stream, events=None, locked=None)
     if ev: ev[6].record(stream)
     if not wl.surelock:
         return
-    dl.dllm_lock_criterion(d["logits"], d["logits_prev"], LOCK_EPS, gate_q=LOCK_GATE_Q,
-                           R_max=s.Lw, row_idx=bf.idx, count=bf.count, out_idx=bf.idx,
-                           out_cols=s.L, kl_out=bf.kl, unc_out=bf.unc,
-                           locked_inout=bf.lock_flags, ws=bf.lock_ws, dev_status=bf.dev_status,
-                           stream=stream)
-    if ev: ev[7].record(stream)
     dl.dllm_adaptive_prefix(d["score"], d["start"], ADAPT_LO, ADAPT_HI, len_out=bf.alen,
                             tau_out=bf.atau, dev_status=bf.dev_status, stream=stream)
-    if ev: ev[8].record(stream)
+    if ev: ev[7].record(stream)
 
 
 def launches_per_step(wl: Workload, bf: Buffers) -> int:
@@ -608,10 +615,10 @@ def launches_per_step(wl: Workload, bf: Buffers) -> int:
     # (persistent kernel for small heads, key-tile-group kernel for the
     # rest), prefix 1; confidence 2 (streaming kernel, row merge)
     n = 2 + 1 + (2 if bf.attn_split else 1) + 2 + 1
-    if wl.conf is not None:
-        n += 2
-    if wl.surelock:
+    if wl.surelock:  # lock criterion with the confidence (partials, merge, gate), adaptive prefix
         n += 3 + 1
+    elif wl.conf is not None:
+        n += 2
     return n
 
 
@@ -640,6 +647,8 @@ def algorithmic_work(wl: Workload, counts):
     lock_b = M * (2 * s.V * el + 4 + 4 + 4 + 4 + 1)
     return {
         "dllm_lock_criterion": {"bytes": lock_b, "flops": 0.0},
+        # both logit rows once, the criterion's and the confidence's outputs
+        "dllm_lock_criterion_conf": {"bytes": lock_b + M * 12, "flops": 0.0},
         "dllm_adaptive_prefix": {"bytes": s.B * s.Lw * 4, "flops": 0.0},
         "dllm_saliency_select": {"bytes": select_b, "flops": 6.0 * s.B * s.Lw * s.D},
         "dllm_kv_scatter": {"bytes": scatter_b, "flops": 0.0},

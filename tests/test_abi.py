@@ -176,7 +176,8 @@ def test_every_kernel_waits_for_its_predecessor():
     # be resident while the previous kernel on the stream still runs; it must
     # execute pdl_wait() before touching global memory.  Static check of the
     # sources: each __global__ body starts with pdl_wait(), and no launch
-    # bypasses launch_pdl.
+    # bypasses launch_pdl (or launch_serial, the same launch without early
+    # residency, where pdl_wait() returns at once).
     src_dir = os.path.join(ROOT, "partial_attention_saliency_b300", "csrc")
     kernels = 0
     for name in sorted(os.listdir(src_dir)):

@@ -89,7 +89,11 @@ def test_workload_names_and_options():
     assert _wl("--workload", "long_4k", "--locked", "0.9").name == "long_4k_locked90"
     wl = _wl("--workload", "long_4k_schedule", "--surelock")
     assert wl.name == "long_4k_schedule_surelock" and wl.surelock and wl.schedule == 64
-    assert bench.entries(wl) == bench.ENTRY_ORDER + bench.SURELOCK_ORDER
+    # the lock criterion with the confidence takes the confidence's place
+    order = bench.entries(wl)
+    assert order == bench.SURELOCK_ORDER and "dllm_confidence" not in order
+    assert order.index("dllm_lock_criterion_conf") < order.index("dllm_stable_prefix") \
+        < order.index("dllm_adaptive_prefix") == len(order) - 1
     assert bench.entries(_wl("--workload", "step_1k")) == bench.ENTRY_ORDER
     with pytest.raises(SystemExit):
         _wl("--workload", "step_1k", "--surelock")  # needs logits of every position
@@ -102,7 +106,7 @@ def test_launch_counts():
     nolog = _wl("--workload", "batch8_2k")
     assert bench.launches_per_step(nolog, types.SimpleNamespace(attn_split=True)) == 8
     sl = _wl("--workload", "long_4k", "--surelock")
-    assert bench.launches_per_step(sl, types.SimpleNamespace(attn_split=False)) == 13
+    assert bench.launches_per_step(sl, types.SimpleNamespace(attn_split=False)) == 11
 
 
 def test_lock_schedule_is_nested_and_linear():
